@@ -1,0 +1,330 @@
+"""Benchmark of the fused DSA decode step (lightning indexer -> exact top-2048 ->
+sparse MLA) through libdsa on synthetic data, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one dsa_decode over the whole batch of the workload (one layer).
+Default workload: b4_ctx1m (4 requests x 1,048,576-token context, FP8 index keys
+and latents, 64-token pages, random block tables) -- the long-context,
+bandwidth-bound case. Its inputs (2.97 GB per step) are larger than the 129 MB
+L2, so consecutive steps are timed back to back with no flush.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload on its
+own GPU (requests are independent; no data-path collective); the step time is
+the max over ranks and `value` counts the layer-steps of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode layer-steps/sec and achieved HBM GB/s (% of GB300 roofline)"
+UNIT = "layer-steps/s"
+KEY_B, LAT_B = 132, 576
+Q_OUT_B = 32 * 128 * 2 + 32 * 4 + 96 * 576 * 2 + 96 * 512 * 2
+
+
+def step_bytes(ctx, n_q, topk):
+    """Algorithmic bytes of one step: every index key, each selected latent, q/w/out."""
+    tot = 0
+    for c in ctx:
+        union = min(int(c), topk + n_q - 1) if n_q > 1 else min(int(c), topk)
+        tot += KEY_B * int(c) + LAT_B * union + n_q * Q_OUT_B
+    return tot
+
+
+def indexer_bytes(ctx, n_q):
+    """Algorithmic bytes of the indexer stage: keys + scales once, the query and weights."""
+    return sum(KEY_B * int(c) for c in ctx) + len(ctx) * n_q * (32 * 128 * 2 + 32 * 4)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(inp, budget_s=15.0):
+    """The oracle, as it stands, on whole requests of the workload until ~budget_s."""
+    from oracle import dsa as O
+
+    t0 = time.perf_counter()
+    done = 0
+    for b in range(inp.batch):
+        O.decode(inp, requests=[b])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    per_step = dt / done * inp.batch
+    return {"value": 1.0 / per_step, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{done} of {inp.batch} requests of one step (numpy float64; BLAS threads = default)",
+            "seconds": dt}
+
+
+def run_reference(args, rank):
+    import gen
+
+    line = {"impl": "reference", "metric": METRIC, "unit": UNIT, "higher_is_better": True, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "data": "synthetic", "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64"}
+    if rank != 0:
+        return
+    from oracle import dsa as O
+
+    inp = gen.make_workload(args.workload)
+    # one step of the reference arm = the oracle on one request (a bounded sample
+    # of the workload's step); throughput is scaled to whole steps
+    def one(i):
+        O.decode(inp, requests=[i % inp.batch])
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    per_step = dt / args.steps * inp.batch
+    v = 1.0 / per_step
+    line.update({"value": v, "ms_per_step": per_step * 1e3,
+                 "config": {"workload": args.workload, "batch": inp.batch, "n_q": inp.n_q,
+                            "ctx": int(inp.ctx.max()), "topk": inp.topk},
+                 "cpu_baseline": {"value": v, "unit": UNIT, "kind": "oracle", "cores": len(os.sched_getaffinity(0)),
+                                  "sample": "one request per step (1/batch of a layer-step)"},
+                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import dsa_sparse_mla_paged_gb300 as dsa
+    import gen
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from dsa_testlib import Dev
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dsa.load()
+
+    inp = gen.make_workload(args.workload)
+    cpu = cpu_baseline(inp) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    d = Dev(inp)
+    stream = torch.cuda.Stream()
+    out = torch.empty((d.rows, 96, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((d.rows, 96), dtype=torch.float32, device="cuda")
+    idx = torch.empty((d.rows, inp.topk), dtype=torch.int32, device="cuda")
+
+    def step(s):
+        dsa.decode(d.p, d.q_idx, d.w, d.key_pool, d.q, d.lat_pool, d.block_table, d.ctx, out, lse, idx, d.ws,
+                   stream=s)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    if dsa.get_device_error(d.ws) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.15)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+        barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # per-stage times (the three stage entry points, events on the launching stream)
+    stage_ms = {"indexer": 0.0, "topk": 0.0, "sparse_mla": 0.0}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    sc = torch.empty((d.rows, d.cap), dtype=torch.float32, device="cuda")
+    nst = max(10, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for i in range(nst + 3):
+            ev[0].record(stream)
+            dsa.indexer_scores(d.p, d.q_idx, d.w, d.key_pool, d.block_table, d.ctx, sc, d.cap, d.ws, stream=stream)
+            ev[1].record(stream)
+            dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws, stream=stream)
+            ev[2].record(stream)
+            dsa.sparse_mla_decode(d.p, d.q, d.lat_pool, d.block_table, d.ctx, idx, out, lse, d.ws, stream=stream)
+            ev[3].record(stream)
+            stream.synchronize()
+            if i >= 3:
+                stage_ms["indexer"] += ev[0].elapsed_time(ev[1]) / nst
+                stage_ms["topk"] += ev[1].elapsed_time(ev[2]) / nst
+                stage_ms["sparse_mla"] += ev[2].elapsed_time(ev[3]) / nst
+
+    # end to end through the public call, host buffers, copies inside the timed region
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = [pin(x) for x in (d.q_idx, d.w, d.q, d.block_table, d.ctx)]
+    d_in = [d.q_idx, d.w, d.q, d.block_table, d.ctx]
+    h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory(), torch.empty(lse.shape, dtype=lse.dtype).pin_memory()]
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    ke2e = max(5, min(args.steps, 100))
+    barrier()
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for _ in range(ke2e):
+            for hsrc, ddst in zip(h_in, d_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            step(stream)
+            h_out[0].copy_(out, non_blocking=True)
+            h_out[1].copy_(lse, non_blocking=True)
+        ev[1].record(stream)
+    barrier()
+    e2e_ms = ev[0].elapsed_time(ev[1]) / ke2e
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank == 0:
+        peak, peak_kind = peaks()
+        sbytes = step_bytes(inp.ctx, inp.n_q, inp.topk)
+        ibytes = indexer_bytes(inp.ctx, inp.n_q)
+        gbs = sbytes / (ms * 1e-3) / 1e9
+        idx_gbs = ibytes / (stage_ms["indexer"] * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": world * 1e3 / ms, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8+bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": inp.batch, "n_q": inp.n_q,
+                       "ctx": int(inp.ctx.max()), "topk": inp.topk, "page_size": inp.page_size,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (%.2f GB per step), no flush" % (
+                           (inp.key_pool.nbytes + inp.lat_pool.nbytes) / 1e9)},
+            "achieved_gbs": gbs, "hbm_frac": gbs / peak, "step_bytes": sbytes,
+            "stage_ms": stage_ms,
+            "roofline": {"bound": "hbm", "kernel": "indexer (dsa_indexer_scores)", "achieved": idx_gbs,
+                         "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
+                         "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": ibytes},
+            "e2e": {"value": world * 1e3 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * dsa.KERNELS_PER_DECODE,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="b4_ctx1m")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+// libdsa C ABI: host-side validation, workspace carving and stage launches.
+#include <cstdint>
+#include <cstring>
+
+#include "dsa_internal.cuh"
+
+using namespace dsa;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dsa_status_t check_params(const dsa_params_t* p) {
+  if (!p) return DSA_ERR_INVALID;
+  if (p->batch < 1 || p->n_q < 1 || p->max_pages_per_req < 1 || p->num_pages < 1) return DSA_ERR_INVALID;
+  if (p->topk < 1) return DSA_ERR_INVALID;
+  if (p->n_q > kMaxNQ || p->topk > kMaxTopK) return DSA_ERR_UNSUPPORTED;
+  if (p->page_size != kPage || p->idx_heads != kIdxHeads || p->idx_dim != kIdxDim ||
+      p->heads != kHeads || p->d_nope != kDNope || p->d_rope != kDRope)
+    return DSA_ERR_UNSUPPORTED;
+  if (p->key_fmt != DSA_KEY_FP8_132 && p->key_fmt != DSA_KEY_MXFP4_68) return DSA_ERR_INVALID;
+  if (p->lat_fmt != DSA_LAT_FP8_576 && p->lat_fmt != DSA_LAT_NVFP4_352) return DSA_ERR_INVALID;
+  const int64_t key_row = p->key_fmt == DSA_KEY_FP8_132 ? p->idx_dim + 4 : p->idx_dim / 2 + p->idx_dim / 32;
+  const int64_t lat_row = p->lat_fmt == DSA_LAT_FP8_576 ? p->d_nope + p->d_rope
+                                                        : p->d_nope / 2 + p->d_nope / 16 + p->d_rope;
+  const int64_t key_page = int64_t(p->page_size) * key_row;
+  const int64_t lat_page = int64_t(p->page_size) * lat_row;
+  if (p->key_page_stride < key_page || (p->key_page_stride & 15)) return DSA_ERR_INVALID;
+  if (p->lat_page_stride < lat_page || (p->lat_page_stride & 15)) return DSA_ERR_INVALID;
+  if (!(p->softmax_scale > 0.f) || !(p->latent_scale > 0.f)) return DSA_ERR_INVALID;
+  if (p->flags & ~int32_t(DSA_EMIT_PHYS_ROWS)) return DSA_ERR_INVALID;
+  if (p->key_fmt != DSA_KEY_FP8_132 || p->lat_fmt != DSA_LAT_FP8_576) return DSA_ERR_UNSUPPORTED;
+  // keep every index of the kernels inside int32 / the grid limits
+  if (int64_t(p->max_pages_per_req) * p->page_size > (int64_t(1) << 28)) return DSA_ERR_UNSUPPORTED;
+  if (int64_t(p->batch) * p->n_q > 65535) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+dsa_status_t check_ws(const dsa_params_t* p, void* ws, size_t ws_bytes, WsLayout* L) {
+  if (!ws || !aligned16(ws)) return DSA_ERR_INVALID;
+  *L = ws_layout(*p);
+  if (ws_bytes < L->total) return DSA_ERR_WORKSPACE;
+  return DSA_OK;
+}
+
+dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+dsa_status_t check_indexer_args(const dsa_params_t* p, const void* q_idx, const float* w,
+                                const void* key_pool, const int32_t* bt, const int32_t* ctx) {
+  if (!q_idx || !w || !key_pool || !bt || !ctx) return DSA_ERR_INVALID;
+  if (!aligned16(q_idx) || !aligned16(key_pool) || (reinterpret_cast<uintptr_t>(w) & 3)) return DSA_ERR_INVALID;
+  return DSA_OK;
+}
+
+dsa_status_t check_mla_args(const void* q, const void* lat_pool, const int32_t* bt, const int32_t* ctx,
+                            void* out) {
+  if (!q || !lat_pool || !bt || !ctx || !out) return DSA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(lat_pool) || !aligned16(out)) return DSA_ERR_INVALID;
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_workspace_size(const dsa_params_t* params, size_t* bytes) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if (!bytes) return DSA_ERR_INVALID;
+  *bytes = ws_layout(*params).total;
+  return DSA_OK;
+}
+
+dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, const float* w,
+                                const void* key_pool, const int32_t* block_table,
+                                const int32_t* ctx_lens, float* scores, int64_t score_stride,
+                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if ((s = check_indexer_args(params, q_idx, w, key_pool, block_table, ctx_lens)) != DSA_OK) return s;
+  if (!scores || !aligned16(scores) || score_stride < 1 || (score_stride & 3)) return DSA_ERR_INVALID;
+  WsLayout L;
+  if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
+  char* w8 = static_cast<char*>(ws);
+  int* err = reinterpret_cast<int*>(w8 + L.err);
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(w8 + L.q8);
+  float* wq = reinterpret_cast<float*>(w8 + L.wq);
+  cudaError_t e = launch_idx_q_quant(*params, q_idx, w, q8, wq, stream);
+  if (e == cudaSuccess)
+    e = launch_indexer(*params, q8, wq, key_pool, block_table, ctx_lens, scores, score_stride, err, stream);
+  return cuda_status(e);
+}
+
+dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t score_stride,
+                      const int32_t* ctx_lens, const int32_t* block_table, int32_t* topk_idx,
+                      int32_t* phys_rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if (!scores || !aligned16(scores) || score_stride < 1 || (score_stride & 3)) return DSA_ERR_INVALID;
+  if (!ctx_lens || !topk_idx) return DSA_ERR_INVALID;
+  if (phys_rows && (!(params->flags & DSA_EMIT_PHYS_ROWS) || !block_table)) return DSA_ERR_INVALID;
+  WsLayout L;
+  if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
+  return cuda_status(launch_topk(*params, L, static_cast<char*>(ws), scores, score_stride, ctx_lens,
+                                 block_table, topk_idx, phys_rows, stream));
+}
+
+dsa_status_t dsa_sparse_mla_decode(const dsa_params_t* params, const void* q, const void* lat_pool,
+                                   const int32_t* block_table, const int32_t* ctx_lens,
+                                   const int32_t* topk_idx, void* out, float* lse, void* ws,
+                                   size_t ws_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if ((s = check_mla_args(q, lat_pool, block_table, ctx_lens, out)) != DSA_OK) return s;
+  if (!topk_idx) return DSA_ERR_INVALID;
+  WsLayout L;
+  if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
+  return cuda_status(launch_sparse_mla(*params, L, static_cast<char*>(ws), q, lat_pool, block_table,
+                                       ctx_lens, topk_idx, out, lse, stream));
+}
+
+dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const float* w,
+                        const void* key_pool, const void* q, const void* lat_pool,
+                        const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
+                        int32_t* topk_idx_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if ((s = check_indexer_args(params, q_idx, w, key_pool, block_table, ctx_lens)) != DSA_OK) return s;
+  if ((s = check_mla_args(q, lat_pool, block_table, ctx_lens, out)) != DSA_OK) return s;
+  WsLayout L;
+  if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
+  char* w8 = static_cast<char*>(ws);
+  if (!topk_idx_out) topk_idx_out = reinterpret_cast<int32_t*>(w8 + L.topk);
+  int* err = reinterpret_cast<int*>(w8 + L.err);
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(w8 + L.q8);
+  float* wq = reinterpret_cast<float*>(w8 + L.wq);
+  float* scores = reinterpret_cast<float*>(w8 + L.scores);
+  cudaError_t e = launch_idx_q_quant(*params, q_idx, w, q8, wq, stream);
+  if (e == cudaSuccess)
+    e = launch_indexer(*params, q8, wq, key_pool, block_table, ctx_lens, scores, L.cap, err, stream);
+  if (e == cudaSuccess)
+    e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream);
+  if (e == cudaSuccess)
+    e = launch_sparse_mla(*params, L, w8, q, lat_pool, block_table, ctx_lens, topk_idx_out, out, lse,
+                          stream);
+  return cuda_status(e);
+}
+
+dsa_status_t dsa_get_device_error(void* ws, cudaStream_t stream, int32_t* code) {
+  if (!ws || !code) return DSA_ERR_INVALID;
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  *code = v;
+  return DSA_OK;
+}
+
+const char* dsa_status_string(dsa_status_t status) {
+  switch (status) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID: return "DSA_ERR_INVALID: invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: size or format not implemented";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE: workspace too small";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA: CUDA launch or runtime error";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: device wait gave up";
+  }
+  return "unknown dsa_status_t";
+}
+
+}  // extern "C"

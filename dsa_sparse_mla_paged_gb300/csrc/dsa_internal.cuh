@@ -1,0 +1,110 @@
+// Internal declarations shared by the libdsa translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+constexpr int kIdxHeads = 32;
+constexpr int kIdxDim = 128;
+constexpr int kHeads = 96;
+constexpr int kDNope = 512;
+constexpr int kDRope = 64;
+constexpr int kDQK = kDNope + kDRope;
+constexpr int kPage = 64;
+constexpr int kKeyPageBytesFp8 = kPage * (kIdxDim + 4);  // 8448
+constexpr int kLatRowFp8 = kDQK;                         // 576
+constexpr int kMaxNQ = 8;
+constexpr int kMaxTopK = 2048;
+
+// top-k: a row of scores is cut into chunks of this many tokens, one CTA each.
+constexpr int kTopkChunk = 4096;
+constexpr int kHist0Bins = 2048;  // bits 31..21 of the order-preserving key
+constexpr int kHist1Bins = 2048;  // bits 20..10
+constexpr int kHist2Bins = 1024;  // bits 9..0
+constexpr int kRowState = 16;     // int32 words of per-row selection state
+
+// sparse attention: at most this many KV splits per row.
+constexpr int kMaxSplits = 16;
+
+// Byte offsets of the workspace regions (all 256-B aligned).
+struct WsLayout {
+  size_t err;       // int32 error word
+  size_t q8;        // uint8 [rows][32][128] quantised indexer query
+  size_t wq;        // float [rows][32] folded head weights
+  size_t hist;      // int32 [rows][2048 + 2048 + 1024]
+  size_t state;     // int32 [rows][kRowState]
+  size_t ticket;    // int32 [rows][4] last-CTA tickets (zero between calls)
+  size_t chunkcnt;  // int32 [rows][max_chunks][2]
+  size_t chunkoff;  // int32 [rows][max_chunks][2]
+  size_t opart;     // float [rows][splits][96][512]
+  size_t lpart;     // float [rows][splits][96]
+  size_t topk;      // int32 [rows][topk] (dsa_decode without topk_idx_out)
+  size_t scores;    // float [rows][cap]
+  size_t total;
+  int rows, cap, max_chunks, splits;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// KV splits of the attention for `rows` rows (same function for sizing and launch).
+inline int attention_splits(int rows) {
+  int s = (512 + rows - 1) / rows;
+  return s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+}
+
+inline WsLayout ws_layout(const dsa_params_t& p) {
+  WsLayout L{};
+  L.rows = p.batch * p.n_q;
+  L.cap = p.max_pages_per_req * p.page_size;
+  L.max_chunks = (L.cap + kTopkChunk - 1) / kTopkChunk;
+  L.splits = attention_splits(L.rows);
+  size_t o = 0;
+  L.err = o; o = align256(o + 256);
+  L.q8 = o; o = align256(o + size_t(L.rows) * kIdxHeads * kIdxDim);
+  L.wq = o; o = align256(o + size_t(L.rows) * kIdxHeads * 4);
+  L.hist = o; o = align256(o + size_t(L.rows) * (kHist0Bins + kHist1Bins + kHist2Bins) * 4);
+  L.state = o; o = align256(o + size_t(L.rows) * kRowState * 4);
+  L.ticket = o; o = align256(o + size_t(L.rows) * 4 * 4);
+  L.chunkcnt = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
+  L.chunkoff = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
+  L.opart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * kDNope * 4);
+  L.lpart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * 4);
+  L.topk = o; o = align256(o + size_t(L.rows) * p.topk * 4);
+  L.scores = o; o = align256(o + size_t(L.rows) * L.cap * 4);
+  L.total = o;
+  return L;
+}
+
+// Visible length of row (b, t): ctx_b - n_q + t + 1, or -1 when ctx_b is invalid.
+__device__ __forceinline__ int row_visible_len(const int32_t* ctx_lens, int b, int t, int n_q,
+                                               int cap, int* err) {
+  int c = ctx_lens[b];
+  if (c < n_q || c > cap) {
+    if (t == 0 && threadIdx.x == 0) atomicOr(err, DSA_DEVERR_CTX);
+    return -1;
+  }
+  return c - n_q + t + 1;
+}
+
+// ---------------------------------------------------------------- launchers
+// (each returns cudaGetLastError() of its launches)
+
+cudaError_t launch_idx_q_quant(const dsa_params_t& p, const void* q_idx, const float* w,
+                               uint8_t* q8, float* wq, cudaStream_t st);
+cudaError_t launch_indexer(const dsa_params_t& p, const uint8_t* q8, const float* wq,
+                           const void* key_pool, const int32_t* block_table,
+                           const int32_t* ctx_lens, float* scores, int64_t score_stride, int* err,
+                           cudaStream_t st);
+cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
+                        int64_t score_stride, const int32_t* ctx_lens, const int32_t* block_table,
+                        int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st);
+cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q,
+                              const void* lat_pool, const int32_t* block_table,
+                              const int32_t* ctx_lens, const int32_t* topk_idx, void* out,
+                              float* lse, cudaStream_t st);
+
+}  // namespace dsa

@@ -126,7 +126,7 @@ def sample_e4m3_normal(rng: np.random.Generator, n: int, out: np.ndarray | None 
     chunk = 1 << 25
     for i in range(0, n, chunk):
         m = min(chunk, n - i)
-        u = np.frombuffer(rng.bytes(2 * m), dtype=np.uint16)
+        u = rng.integers(0, 65536, size=m, dtype=np.uint16)
         out[i:i + m] = _LUT[u]
     return out
 
@@ -290,8 +290,11 @@ def make_inputs(
         raise ValueError(key_fmt)
 
     if lat_fmt == "fp8":
-        vals = sample_e4m3_normal(rng, num_pages * page_size * D_QK)
-        lat_pool[:, :page_size * D_QK] = vals.reshape(num_pages, page_size * D_QK)
+        if lat_page_pad == 0:
+            sample_e4m3_normal(rng, lat_pool.size, out=lat_pool.reshape(-1))
+        else:
+            vals = sample_e4m3_normal(rng, num_pages * page_size * D_QK)
+            lat_pool[:, :page_size * D_QK] = vals.reshape(num_pages, page_size * D_QK)
     elif lat_fmt == "nvfp4":
         for p0 in range(0, num_pages, 256):
             p1 = min(num_pages, p0 + 256)

@@ -1,0 +1,186 @@
+/*
+ * dsa.h -- C ABI of libdsa: the decode step of a DeepSeek-style sparse
+ * attention (DSA) layer over a paged FP8 cache, for one GB300 GPU (sm_103a).
+ *
+ * The step has three stages, as the vLLM article "vLLM 为 Kimi K3.1 Pro 提供
+ * Day-0 支持" states them in its section "K3.1 Pro 中的稀疏注意力" (sparse
+ * attention in K3.1 Pro):
+ *   1. a lightning indexer scores every earlier token of a request with 32
+ *      light heads over a per-token FP8 index key (128 E4M3 values + one fp32
+ *      scale = 132 B):  score(t, s) = sum_h w_h * ReLU(q_h . k_s);
+ *   2. the 2,048 best-scoring tokens are kept (exact top-k);
+ *   3. MLA attention runs exactly over those tokens only, reading each one's
+ *      576-B FP8 latent (512 "nope" + 64 "rope" values) shared by all 96
+ *      query heads.
+ * The caches are paged; the kernels reach them through a block table (section
+ * "面向三种状态的 KV 缓存": "the block table and cache slots are turned into
+ * kernel page addresses before each step").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Notation: B = params.batch requests, n_q = query tokens per request,
+ *   ctx_b = context length of request b INCLUDING its n_q new tokens (whose
+ *   keys and latents are already in the cache), L_{b,t} = ctx_b - n_q + t + 1
+ *   = tokens query t may see (causal within the step), K = params.topk.
+ *   A "row" is one (b, t) pair; rows are ordered b-major: row = b * n_q + t.
+ * - Ownership: the caller owns every buffer, including the workspace. The
+ *   library never allocates, frees or synchronises (dsa_get_device_error is
+ *   the one call that synchronises the stream it is given).
+ * - All pointers except `params`, `bytes` and `code` are DEVICE pointers.
+ *   All calls are asynchronous on `stream` (0 = the legacy default stream).
+ * - Host validation: null pointers, unsupported sizes or formats, misaligned
+ *   buffers (q, q_idx, pools, scores, workspace: 16 B; page strides: a
+ *   multiple of 16 B) and a short workspace are rejected with
+ *   DSA_ERR_INVALID / DSA_ERR_UNSUPPORTED / DSA_ERR_WORKSPACE before anything
+ *   is launched.
+ * - Device-detected bad data (a block-table entry outside [0, num_pages), a
+ *   ctx_b outside [n_q, max_pages_per_req * page_size], a top-k index outside
+ *   [-1, L_{b,t})) never traps: the kernels skip the access, leave the affected
+ *   row's results unspecified (finite), and OR a bit into the workspace's error
+ *   word, which dsa_get_device_error reads back.
+ * - The workspace must be zero-filled once after allocation; afterwards the
+ *   library keeps it consistent itself. Calls that share one workspace must
+ *   be ordered (same stream, or synchronised by the caller).
+ * - Launch failures return DSA_ERR_CUDA.
+ * - Results are deterministic: the same inputs give the same bits, whatever
+ *   the batch composition.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same definition as the CUDA runtime's. */
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID = 1,      /* a null pointer, a bad size or a misaligned buffer */
+  DSA_ERR_UNSUPPORTED = 2,  /* a size or format this build does not implement */
+  DSA_ERR_WORKSPACE = 3,    /* ws_bytes below dsa_workspace_size() */
+  DSA_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+  DSA_ERR_TIMEOUT = 5       /* reserved: a bounded device wait gave up */
+} dsa_status_t;
+
+/* Index-key formats (section "面向三种状态的 KV 缓存": index key 132 B in FP8,
+ * 68 B in MXFP4). Page layout of one page of page_size tokens:
+ *   DSA_KEY_FP8_132 : [page_size x 128 B E4M3][page_size x 4 B fp32 scale]
+ *   DSA_KEY_MXFP4_68: [page_size x 64 B E2M1 pairs][page_size x 4 B E8M0]  */
+typedef enum { DSA_KEY_FP8_132 = 0, DSA_KEY_MXFP4_68 = 1 } dsa_key_fmt_t;
+
+/* Latent formats (same section: 576 B in FP8, 352 B in NVFP4). A page is
+ * page_size consecutive rows:
+ *   DSA_LAT_FP8_576  : [512 E4M3 nope][64 E4M3 rope]
+ *   DSA_LAT_NVFP4_352: [256 B E2M1 pairs][32 B E4M3 scale per 16][64 B E4M3 rope] */
+typedef enum { DSA_LAT_FP8_576 = 0, DSA_LAT_NVFP4_352 = 1 } dsa_lat_fmt_t;
+
+/* flags */
+#define DSA_EMIT_PHYS_ROWS 0x1  /* dsa_topk also writes physical cache rows */
+
+/* Device error word bits (dsa_get_device_error). */
+#define DSA_DEVERR_BLOCK_TABLE 0x1  /* a block-table entry outside [0, num_pages) */
+#define DSA_DEVERR_CTX 0x2          /* ctx_b outside [n_q, max_pages_per_req * page_size] */
+#define DSA_DEVERR_TOPK_INDEX 0x4   /* a top-k index outside [-1, L_{b,t}) */
+
+typedef struct {
+  int32_t batch;              /* B >= 1 */
+  int32_t n_q;                /* query tokens per request, 1..8 */
+  int32_t topk;               /* K; this build: 2048 */
+  int32_t page_size;          /* tokens per page; this build: 64 */
+  int32_t max_pages_per_req;  /* row stride of block_table (entries); ctx_b <= this * page_size */
+  int32_t idx_heads;          /* 32 */
+  int32_t idx_dim;            /* 128 */
+  int32_t heads;              /* 96 */
+  int32_t d_nope;             /* 512 */
+  int32_t d_rope;             /* 64 */
+  int32_t key_fmt;            /* dsa_key_fmt_t */
+  int32_t lat_fmt;            /* dsa_lat_fmt_t */
+  int64_t key_page_stride;    /* bytes between key pages (>= page bytes, multiple of 16) */
+  int64_t lat_page_stride;    /* bytes between latent pages (>= page bytes, multiple of 16) */
+  int32_t num_pages;          /* pages in each pool (bounds check of block-table entries) */
+  float softmax_scale;        /* e.g. 1/sqrt(192) */
+  float latent_scale;         /* per-tensor latent scale (1.0 for unscaled) */
+  int32_t flags;              /* DSA_EMIT_PHYS_ROWS */
+} dsa_params_t;
+
+/* Bytes of workspace the calls below need for `params`. The workspace holds
+ * the device error word, the quantised indexer query, the top-k histograms,
+ * the split-KV partial outputs and (for dsa_decode) the fp32 scores of every
+ * row over max_pages_per_req * page_size tokens. */
+dsa_status_t dsa_workspace_size(const dsa_params_t* params, size_t* bytes);
+
+/* Stage 1, the lightning indexer ("K3.1 Pro 中的稀疏注意力"), with the FP8 query
+ * quantisation of the fused front end ("低延迟解码：融合的 DSA 解码路径": the
+ * indexer query is quantised to FP8 with its scale folded into the head
+ * weights):
+ *   amax_h = max_d |q[h,d]|, q8_h = E4M3_rne_sat(q_h * (448/amax_h)),
+ *   w'_h = w_h * (amax_h/448)        (IEEE fp32, round to nearest);
+ *   score[row][s] = sum_h w'_h * max(0, scale_s * (q8_h . kfp8_s))
+ * for s < L_{b,t}; entries s >= L_{b,t} are left untouched.
+ *   q_idx  bf16 [B, n_q, idx_heads, idx_dim]      (16-B aligned)
+ *   w      fp32 [B, n_q, idx_heads]
+ *   key_pool   num_pages pages of key_page_stride bytes (16-B aligned)
+ *   block_table int32 [B, max_pages_per_req]; entries past ceil(ctx_b/page_size) unused
+ *   ctx_lens   int32 [B]
+ *   scores fp32 [B * n_q, score_stride], score_stride >= max ctx, multiple of 4 */
+dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, const float* w,
+                                const void* key_pool, const int32_t* block_table,
+                                const int32_t* ctx_lens, float* scores, int64_t score_stride,
+                                void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Stage 2, exact top-k ("K3.1 Pro 中的稀疏注意力": keep the top 2,048 tokens).
+ * For each row: the min(K, L) tokens with the highest fp32 score, ties going to
+ * the lower token index (-0 == +0), written in ascending token order to
+ * topk_idx[row][0 .. min(K, L)), the rest of the row set to -1.
+ *   scores   fp32 [B * n_q, score_stride] (only s < L_{b,t} is read)
+ *   topk_idx int32 [B * n_q, K]
+ *   phys_rows int32 [B * n_q, K] or NULL: page * page_size + slot of each
+ *            selected token ("融合的 indexer ... 输出注意力读取的物理 KV 行"),
+ *            -1 padded; needs DSA_EMIT_PHYS_ROWS and block_table. */
+dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t score_stride,
+                      const int32_t* ctx_lens, const int32_t* block_table, int32_t* topk_idx,
+                      int32_t* phys_rows, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Stage 3, exact absorbed-MLA attention over the selected tokens
+ * ("K3.1 Pro 中的稀疏注意力": attention runs exactly, but only over those tokens).
+ * For each row and head h, with c_s = E4M3(latent_s) * latent_scale:
+ *   logit_s = softmax_scale * q_h . c_s  (576 dims), s in S = {topk_idx >= 0}
+ *   out[h]  = sum_s softmax(logit)_s * c_s[0:512]          (bf16, RNE)
+ *   lse[h]  = ln sum_s exp(logit_s)                        (fp32)
+ * An empty S gives out = 0 and lse = -inf.
+ *   q        bf16 [B, n_q, heads, d_nope + d_rope] (16-B aligned)
+ *   lat_pool num_pages pages of lat_page_stride bytes (16-B aligned)
+ *   topk_idx int32 [B * n_q, K] logical token indices, -1 = unused slot
+ *   out      bf16 [B, n_q, heads, d_nope]
+ *   lse      fp32 [B, n_q, heads] or NULL */
+dsa_status_t dsa_sparse_mla_decode(const dsa_params_t* params, const void* q, const void* lat_pool,
+                                   const int32_t* block_table, const int32_t* ctx_lens,
+                                   const int32_t* topk_idx, void* out, float* lse, void* ws,
+                                   size_t ws_bytes, cudaStream_t stream);
+
+/* The fused step: stage 1 -> stage 2 -> stage 3 on one stream, no host sync.
+ * topk_idx_out (int32 [B * n_q, K]) may be NULL; the scores stay in the
+ * workspace. Arguments as above. */
+dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const float* w,
+                        const void* key_pool, const void* q, const void* lat_pool,
+                        const int32_t* block_table, const int32_t* ctx_lens, void* out,
+                        float* lse, int32_t* topk_idx_out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * workspace `ws` into *code (0 = no error; DSA_DEVERR_* bits otherwise). */
+dsa_status_t dsa_get_device_error(void* ws, cudaStream_t stream, int32_t* code);
+
+/* Static description of a status code. */
+const char* dsa_status_string(dsa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

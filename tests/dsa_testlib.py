@@ -1,0 +1,144 @@
+"""Helpers shared by the tests: move generated inputs to the GPU and call libdsa."""
+from __future__ import annotations
+
+import numpy as np
+
+import dsa_sparse_mla_paged_gb300 as dsa
+
+KEY_FMT = {"fp8": dsa.DSA_KEY_FP8_132, "mxfp4": dsa.DSA_KEY_MXFP4_68}
+LAT_FMT = {"fp8": dsa.DSA_LAT_FP8_576, "nvfp4": dsa.DSA_LAT_NVFP4_352}
+
+# acceptance bars
+SCORE_RTOL = 1e-3          # indexer scores, relative
+SCORE_FLOOR = 1e-6         # denominator floor, relative to the row's largest |score|
+TIE_RTOL = 1e-5            # end-to-end selection: tokens this close to tau may differ
+OUT_MAX_ABS = 2e-2         # attention output (bf16)
+OUT_MEAN_ABS = 2e-3
+LSE_ABS = 1e-3             # log-sum-exp (fp32 arithmetic on logits of size ~10)
+
+
+def params_for(inp, flags=0):
+    return dsa.make_params(
+        batch=inp.batch, n_q=inp.n_q, max_pages_per_req=inp.max_pages, num_pages=inp.num_pages,
+        key_page_stride=inp.key_page_stride, lat_page_stride=inp.lat_page_stride, topk=inp.topk,
+        page_size=inp.page_size, key_fmt=KEY_FMT[inp.key_fmt], lat_fmt=LAT_FMT[inp.lat_fmt],
+        softmax_scale=inp.softmax_scale, latent_scale=inp.latent_scale, flags=flags)
+
+
+class Dev:
+    """Device copies of one DSAInputs plus a zeroed workspace."""
+
+    def __init__(self, inp, flags=0, device="cuda"):
+        import torch
+
+        self.inp = inp
+        self.p = params_for(inp, flags)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.q_idx = t(inp.q_idx.view(np.int16)).view(torch.bfloat16)
+        self.w = t(inp.w)
+        self.key_pool = t(inp.key_pool)
+        self.q = t(inp.q.view(np.int16)).view(torch.bfloat16)
+        self.lat_pool = t(inp.lat_pool)
+        self.block_table = t(inp.block_table)
+        self.ctx = t(inp.ctx)
+        self.rows = inp.batch * inp.n_q
+        self.cap = inp.max_pages * inp.page_size
+        self.ws = torch.zeros(dsa.workspace_size(self.p), dtype=torch.uint8, device=device)
+
+    def scores(self, stride=None):
+        import torch
+
+        stride = stride or (self.cap + 3) // 4 * 4
+        sc = torch.full((self.rows, stride), float("nan"), dtype=torch.float32, device="cuda")
+        dsa.indexer_scores(self.p, self.q_idx, self.w, self.key_pool, self.block_table, self.ctx, sc, stride,
+                           self.ws)
+        return sc
+
+    def topk(self, scores_np=None, scores_dev=None, phys=False):
+        import torch
+
+        if scores_dev is None:
+            stride = (scores_np.shape[1] + 3) // 4 * 4
+            scores_dev = torch.zeros((self.rows, stride), dtype=torch.float32, device="cuda")
+            scores_dev[:, :scores_np.shape[1]] = torch.from_numpy(scores_np)
+        idx = torch.full((self.rows, self.inp.topk), -7, dtype=torch.int32, device="cuda")
+        pr = torch.full_like(idx, -7) if phys else None
+        dsa.topk(self.p, scores_dev, scores_dev.shape[1], self.ctx, self.block_table, idx, pr, self.ws)
+        return idx, pr
+
+    def mla(self, topk_idx):
+        import torch
+
+        out = torch.empty((self.rows, 96, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((self.rows, 96), dtype=torch.float32, device="cuda")
+        dsa.sparse_mla_decode(self.p, self.q, self.lat_pool, self.block_table, self.ctx, topk_idx, out, lse,
+                              self.ws)
+        return out, lse
+
+    def decode(self):
+        import torch
+
+        out = torch.empty((self.rows, 96, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((self.rows, 96), dtype=torch.float32, device="cuda")
+        idx = torch.empty((self.rows, self.inp.topk), dtype=torch.int32, device="cuda")
+        dsa.decode(self.p, self.q_idx, self.w, self.key_pool, self.q, self.lat_pool, self.block_table, self.ctx,
+                   out, lse, idx, self.ws)
+        return out, lse, idx
+
+
+def rows_scores_oracle(inp, rows=None):
+    from oracle import dsa as O
+
+    out = {}
+    for b in range(inp.batch):
+        for t in range(inp.n_q):
+            r = b * inp.n_q + t
+            if rows is None or r in rows:
+                out[r] = O.indexer_scores(inp, b, t)
+    return out
+
+
+def check_scores(got: np.ndarray, ref: np.ndarray):
+    """Relative error with denominator max(|ref|, 1e-6 * max |ref|)."""
+    ref64 = ref.astype(np.float64)
+    den = np.maximum(np.abs(ref64), SCORE_FLOOR * max(np.abs(ref64).max(), 1e-30))
+    rel = np.abs(got.astype(np.float64) - ref64) / den
+    assert np.isfinite(got).all(), "non-finite GPU score"
+    assert rel.max() <= SCORE_RTOL, f"max rel score error {rel.max():.3e} at {int(rel.argmax())}"
+    return float(rel.max())
+
+
+def check_selection(got_idx: np.ndarray, ref_idx: np.ndarray, ref_scores: np.ndarray, k: int):
+    """Equal sets except tokens whose oracle score is within TIE_RTOL*|tau| of tau; both ascending, -1 padded."""
+    from oracle import dsa as O
+
+    for arr in (got_idx, ref_idx):
+        v = arr[arr >= 0]
+        assert (np.diff(v) > 0).all(), "not strictly ascending"
+        assert (arr[len(v):] == -1).all(), "padding not -1"
+    g, r = set(got_idx[got_idx >= 0].tolist()), set(ref_idx[ref_idx >= 0].tolist())
+    assert len(g) == len(r)
+    if g == r:
+        return 0
+    tau = O.kth_score(ref_scores, k)
+    diff = np.array(sorted(g ^ r))
+    dev = np.abs(ref_scores[diff].astype(np.float64) - tau)
+    assert (dev <= TIE_RTOL * abs(tau)).all(), f"selection differs beyond near-ties: {diff[dev > TIE_RTOL * abs(tau)][:10]}"
+    return len(diff)
+
+
+def check_attention(out: np.ndarray, lse: np.ndarray, ref_out: np.ndarray, ref_lse: np.ndarray):
+    err = np.abs(out.astype(np.float64) - ref_out)
+    assert err.max() <= OUT_MAX_ABS, f"max abs {err.max():.3e}"
+    assert err.mean() <= OUT_MEAN_ABS, f"mean abs {err.mean():.3e}"
+    fin = np.isfinite(ref_lse)
+    assert (np.isfinite(lse) == fin).all()
+    if fin.any():
+        assert np.abs(lse[fin] - ref_lse[fin]).max() <= LSE_ABS
+    return float(err.max()), float(err.mean())
+
+
+def bf16_to_np(t):
+    import torch
+
+    return t.float().cpu().numpy()

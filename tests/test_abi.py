@@ -1,0 +1,114 @@
+"""The C ABI on the CPU: the library loads, exports every symbol include/dsa.h
+declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dsa_sparse_mla_paged_gb300 as dsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:dsa_status_t|const char\*)\s+(dsa_\w+)\s*\(", src, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    decl = _declared()
+    assert set(decl) == set(dsa.EXPORTS)
+    for name in decl:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert dsa.status_string(s).startswith("DSA_")
+    assert "unknown" in dsa.status_string(99)
+
+
+def _params(**kw):
+    base = dict(batch=2, n_q=1, max_pages_per_req=10, num_pages=20, key_page_stride=8448, lat_page_stride=36864)
+    base.update(kw)
+    return dsa.make_params(**base)
+
+
+def test_workspace_size_and_layout(lib):
+    n1 = dsa.workspace_size(_params())
+    n2 = dsa.workspace_size(_params(batch=4))
+    n3 = dsa.workspace_size(_params(max_pages_per_req=20))
+    assert n1 > 0 and n2 > n1 and n3 > n1 and n1 % 256 == 0
+    # the scores region alone: rows * max_pages * 64 * 4 bytes
+    assert n3 - n1 >= 2 * 10 * 64 * 4
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(batch=0), dsa.DSA_ERR_INVALID),
+    (dict(n_q=0), dsa.DSA_ERR_INVALID),
+    (dict(n_q=9), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(topk=4096), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(topk=0), dsa.DSA_ERR_INVALID),
+    (dict(page_size=32), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(key_page_stride=8440), dsa.DSA_ERR_INVALID),
+    (dict(key_page_stride=8456), dsa.DSA_ERR_INVALID),
+    (dict(lat_page_stride=36800), dsa.DSA_ERR_INVALID),
+    (dict(num_pages=0), dsa.DSA_ERR_INVALID),
+    (dict(key_fmt=7), dsa.DSA_ERR_INVALID),
+    (dict(softmax_scale=0.0), dsa.DSA_ERR_INVALID),
+    (dict(flags=0x100), dsa.DSA_ERR_INVALID),
+])
+def test_bad_params_rejected(lib, kw, status):
+    with pytest.raises(dsa.DSAError) as e:
+        dsa.workspace_size(_params(**kw))
+    assert e.value.status == status
+
+
+FAKE = 0x10000  # never dereferenced: validation fails before any CUDA call
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    p = _params()
+    need = dsa.workspace_size(p)
+    ws = ctypes.c_void_p(FAKE)
+    L = lib
+    # null q_idx
+    st = L.dsa_indexer_scores(ctypes.byref(p), None, FAKE, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    # misaligned key pool
+    st = L.dsa_indexer_scores(ctypes.byref(p), FAKE, FAKE, FAKE + 4, FAKE, FAKE, FAKE, 640, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    # score stride not a multiple of 4
+    st = L.dsa_indexer_scores(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 641, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    # short workspace
+    st = L.dsa_indexer_scores(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need - 1, None)
+    assert st == dsa.DSA_ERR_WORKSPACE
+    # phys rows without the flag
+    st = L.dsa_topk(ctypes.byref(p), FAKE, 640, FAKE, FAKE, FAKE, FAKE, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    # null output of the attention
+    st = L.dsa_sparse_mla_decode(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    # null params
+    st = L.dsa_decode(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    st = L.dsa_get_device_error(None, None, None)
+    assert st == dsa.DSA_ERR_INVALID
+
+
+def test_fp4_formats_report_unsupported_until_built(lib):
+    p = _params(key_fmt=dsa.DSA_KEY_MXFP4_68, key_page_stride=64 * 68,
+                lat_fmt=dsa.DSA_LAT_NVFP4_352, lat_page_stride=64 * 352)
+    try:
+        assert dsa.workspace_size(p) > 0
+    except dsa.DSAError as e:
+        assert e.status == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_library_missing_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(dsa, "_lib", None)
+    monkeypatch.setattr(dsa, "library_path", lambda: str(tmp_path / "libdsa.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        dsa.load()

@@ -1,0 +1,290 @@
+"""GPU parity: every stage of libdsa against the CPU oracle on the same seeded inputs.
+
+Bars: top-k bit-exact on identical fp32 scores; indexer scores within 1e-3
+relative; end-to-end selection equal except tokens within 1e-5 relative of the
+oracle's 2048th score; attention over the oracle's index set within max-abs
+2e-2 and mean-abs 2e-3 (bf16 output).
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import gen
+from oracle import dsa as O
+
+from dsa_testlib import (Dev, bf16_to_np, check_attention, check_scores, check_selection,
+                         rows_scores_oracle)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need(lib, cuda_ok):
+    yield
+
+
+SMALL = [
+    # (batch, n_q, ctx, bt_mode, holes, key_pad, lat_pad, signed_w)
+    (3, 1, [4096 + 37, 2049, 300], "permuted", True, 0, 0, False),
+    (2, 3, [9000, 130], "permuted", False, 16, 32, True),
+    (7, 1, [1, 63, 64, 65, 2047, 2048, 2049], "identity", False, 0, 0, False),
+]
+
+
+@functools.lru_cache(maxsize=None)
+def _small(i):
+    b, nq, ctx, mode, holes, kp, lp, sw = SMALL[i]
+    return gen.make_inputs(b, nq, ctx, seed=100 + i, bt_mode=mode, holes=holes, key_page_pad=kp,
+                           lat_page_pad=lp, signed_w=sw)
+
+
+# ----------------------------------------------------------------------------- stage 1
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_indexer_scores_small(case):
+    inp = _small(case)
+    d = Dev(inp)
+    sc = d.scores().cpu().numpy()
+    ref = rows_scores_oracle(inp)
+    for r, rs in ref.items():
+        check_scores(sc[r, :len(rs)], rs)
+        # entries past L are untouched
+        assert np.isnan(sc[r, len(rs):d.cap]).all()
+
+
+# ----------------------------------------------------------------------------- stage 2
+
+def _score_patterns(L, seed):
+    rng = np.random.default_rng(seed)
+    yield "normal", rng.standard_normal(L).astype(np.float32)
+    yield "constant", np.full(L, 0.75, np.float32)
+    yield "few_levels", (rng.integers(0, 9, L) * 0.5 - 2.0).astype(np.float32)
+    z = rng.standard_normal(L).astype(np.float32)
+    z[rng.random(L) < 0.3] = 0.0
+    z[rng.random(L) < 0.3] = -0.0
+    yield "signed_zeros", z
+    yield "neg_only", -np.abs(rng.standard_normal(L)).astype(np.float32) - 1.0
+    big = rng.standard_normal(L).astype(np.float32)
+    big[rng.integers(0, L, 10)] = np.float32(3e38)
+    big[rng.integers(0, L, 10)] = -np.float32(3e38)
+    yield "extremes", big
+
+
+@pytest.mark.parametrize("ctx", [[1], [2047], [2048], [2049], [4096 * 3 + 5], [70000, 5, 4097, 2048 * 4]])
+def test_topk_bit_exact_on_identical_scores(ctx):
+    B = len(ctx)
+    inp = gen.make_inputs(B, 1, ctx, seed=7)
+    d = Dev(inp)
+    L = max(ctx)
+    for name, _ in _score_patterns(1, 0):
+        mat = np.zeros((B, L), np.float32)
+        for b in range(B):
+            pats = dict(_score_patterns(ctx[b], 1000 * b + len(name)))
+            mat[b, :ctx[b]] = pats[name]
+        idx, _ = d.topk(mat)
+        idx = idx.cpu().numpy()
+        for b in range(B):
+            ref = O.topk_select(mat[b, :ctx[b]], 2048)
+            assert np.array_equal(idx[b], ref), (name, b)
+
+
+def test_topk_multi_token_rows_and_phys_rows():
+    import dsa_sparse_mla_paged_gb300 as dsa
+
+    inp = gen.make_inputs(2, 3, [5000, 9999], seed=8, bt_mode="permuted", holes=True)
+    d = Dev(inp, flags=dsa.DSA_EMIT_PHYS_ROWS)
+    rng = np.random.default_rng(1)
+    mat = (rng.integers(0, 50, (6, 9999)) * 0.125).astype(np.float32)
+    idx, pr = d.topk(mat, phys=True)
+    idx, pr = idx.cpu().numpy(), pr.cpu().numpy()
+    for b in range(2):
+        for t in range(3):
+            r = b * 3 + t
+            L = O.visible_len(inp.ctx[b], 3, t)
+            ref = O.topk_select(mat[r, :L], 2048)
+            assert np.array_equal(idx[r], ref)
+            assert np.array_equal(pr[r], O.physical_rows(inp.block_table[b], ref, 64))
+
+
+def test_topk_small_k():
+    inp = gen.make_inputs(2, 1, [100, 5000], seed=9, topk=16)
+    d = Dev(inp)
+    mat = np.random.default_rng(2).standard_normal((2, 5000)).astype(np.float32)
+    idx, _ = d.topk(mat)
+    for b in range(2):
+        assert np.array_equal(idx.cpu().numpy()[b], O.topk_select(mat[b, :inp.ctx[b]], 16))
+
+
+# ----------------------------------------------------------------------------- stage 3
+
+def _oracle_mla_all(inp, idx):
+    outs, lses = [], []
+    for b in range(inp.batch):
+        for t in range(inp.n_q):
+            o, l = O.sparse_mla(inp, b, t, idx[b * inp.n_q + t])
+            outs.append(o)
+            lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_sparse_mla_over_oracle_indices(case):
+    import torch
+
+    inp = _small(case)
+    d = Dev(inp)
+    ref = {r: O.topk_select(s, 2048) for r, s in rows_scores_oracle(inp).items()}
+    idx = np.stack([ref[r] for r in range(d.rows)])
+    out, lse = d.mla(torch.from_numpy(idx).cuda())
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+
+
+def test_sparse_mla_holes_in_index_list():
+    """-1 entries anywhere in the list are skipped; an all -1 row gives zeros and -inf."""
+    import torch
+
+    inp = gen.make_inputs(3, 1, [3000, 3000, 3000], seed=10, bt_mode="permuted")
+    d = Dev(inp)
+    rng = np.random.default_rng(3)
+    idx = np.full((3, 2048), -1, np.int32)
+    idx[0] = np.sort(rng.choice(3000, 2048, replace=False))
+    idx[0, rng.integers(0, 2048, 300)] = -1
+    idx[1, :5] = [2999, 0, 17, 17, 1500]  # unsorted and duplicated entries are legal
+    out, lse = d.mla(torch.from_numpy(idx).cuda())
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+    assert (bf16_to_np(out)[2] == 0).all() and np.isneginf(lse.cpu().numpy()[2]).all()
+
+
+# ----------------------------------------------------------------------------- fused step
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_decode_end_to_end_small(case):
+    inp = _small(case)
+    d = Dev(inp)
+    out, lse, idx = d.decode()
+    idx = idx.cpu().numpy()
+    res = O.decode(inp)
+    for (b, t), r in res.items():
+        row = b * inp.n_q + t
+        check_selection(idx[row], r["idx"], r["scores"], inp.topk)
+    # attention over the GPU's own (validated) selection
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+
+
+def test_determinism_and_batch_invariance():
+    inp = gen.make_inputs(4, 1, [5000, 7000, 3000, 9000], seed=11, bt_mode="permuted")
+    d = Dev(inp)
+    o1, l1, i1 = d.decode()
+    o2, l2, i2 = d.decode()
+    import torch
+
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert np.array_equal(i1.cpu().numpy(), i2.cpu().numpy())
+    assert np.array_equal(l1.cpu().numpy(), l2.cpu().numpy())
+    # request 2 alone gives the same bits as inside the batch
+    one = gen.make_inputs(4, 1, [5000, 7000, 3000, 9000], seed=11, bt_mode="permuted")
+    one.batch = 1
+    one.ctx = one.ctx[2:3].copy()
+    one.block_table = one.block_table[2:3].copy()
+    for f in ("q_idx", "w", "q"):
+        setattr(one, f, getattr(one, f)[2:3].copy())
+    d1 = Dev(one)
+    o3, l3, i3 = d1.decode()
+    assert np.array_equal(i3.cpu().numpy()[0], i1.cpu().numpy()[2])
+    assert torch.equal(o3.view(torch.int16), o1[2:3].view(torch.int16))
+    assert torch.equal(l3, l1[2:3])
+
+
+def test_device_error_word():
+    """Bad block-table entries, context lengths and top-k indices are caught by the
+    kernels' own bounds checks: they set the error word and never fault."""
+    import torch
+    import dsa_sparse_mla_paged_gb300 as dsa
+
+    inp = gen.make_inputs(2, 1, [3000, 3000], seed=12)
+    d = Dev(inp)
+    assert dsa.get_device_error(d.ws) == 0
+    d.decode()
+    assert dsa.get_device_error(d.ws) == 0
+    d.block_table[1, 3] = inp.num_pages + 5
+    d.decode()
+    assert dsa.get_device_error(d.ws) & dsa.DSA_DEVERR_BLOCK_TABLE
+    assert dsa.get_device_error(d.ws) == 0  # read clears it
+    d.block_table[1, 3] = int(inp.block_table[1, 3])
+    d.ctx[0] = d.cap + 1
+    d.decode()
+    assert dsa.get_device_error(d.ws) & dsa.DSA_DEVERR_CTX
+    d.ctx[0] = 3000
+    idx = torch.full((2, 2048), -1, dtype=torch.int32, device="cuda")
+    idx[0, 0] = 3000  # past the visible context
+    idx[1, 0] = -2
+    d.mla(idx)
+    assert dsa.get_device_error(d.ws) & dsa.DSA_DEVERR_TOPK_INDEX
+
+
+# ----------------------------------------------------------------------------- the five workloads
+
+def plant_tau_ties(inp, b, rng, n_exact=16, n_near=16):
+    """Copy the oracle's rank-2048 key of request b into other positions (exact ties at
+    tau) and into more positions with the scale nudged by one fp32 ulp (near ties)."""
+    sc = O.indexer_scores(inp, b, 0)
+    order = np.lexsort((np.arange(len(sc)), -sc.astype(np.float64)))
+    s_tau = int(order[inp.topk - 1])
+    pg, sl = inp.block_table[b, s_tau // 64], s_tau % 64
+    kb = inp.key_pool[pg, sl * 128:(sl + 1) * 128].copy()
+    scale = inp.key_pool[pg, 8192 + 4 * sl:8192 + 4 * sl + 4].copy().view(np.float32)[0]
+    taken = set(order[:256].tolist()) | {s_tau}
+    cand = [s for s in rng.permutation(len(sc))[:4 * (n_exact + n_near)].tolist() if s not in taken]
+    for j, s in enumerate(cand[:n_exact + n_near]):
+        p2, l2 = inp.block_table[b, s // 64], s % 64
+        inp.key_pool[p2, l2 * 128:(l2 + 1) * 128] = kb
+        v = scale if j < n_exact else np.nextafter(scale, np.float32(np.inf) if j % 2 else np.float32(0))
+        inp.key_pool[p2, 8192 + 4 * l2:8192 + 4 * l2 + 4] = np.array([v], np.float32).view(np.uint8)
+
+
+@functools.lru_cache(maxsize=1)
+def _workload(name):
+    inp = gen.make_workload(name)
+    if name == "b64_ctx16k_128k_ties":
+        rng = np.random.default_rng(77)
+        for b in (0, 31, 63):
+            plant_tau_ties(inp, b, rng)
+    return inp
+
+
+WL_ROWS = {
+    "b1_ctx4k": [0],
+    "b8_ctx32k": list(range(8)),
+    "b64_ctx16k_128k_ties": [0, 31, 63],
+    "b4_ctx1m": [1],
+}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", list(WL_ROWS))
+def test_workload_decode(name):
+    """The full-size workloads in the launch configuration the benchmark times
+    (dsa_decode), checked on sampled requests."""
+    inp = _workload(name)
+    d = Dev(inp)
+    out, lse, idx = d.decode()
+    sc = d.scores().cpu().numpy()
+    idx, out, lse = idx.cpu().numpy(), bf16_to_np(out), lse.cpu().numpy()
+    for b in WL_ROWS[name]:
+        r = O.decode(inp, requests=[b])[(b, 0)]
+        check_scores(sc[b, :len(r["scores"])], r["scores"])
+        nd = check_selection(idx[b], r["idx"], r["scores"], inp.topk)
+        # top-k alone on the oracle's own scores is bit-exact
+        ti, _ = d.topk(np.pad(r["scores"], (0, d.cap - len(r["scores"])))[None].repeat(inp.batch, 0))
+        assert np.array_equal(ti.cpu().numpy()[b], r["idx"])
+        if nd == 0:
+            check_attention(out[b][None], lse[b][None], r["out"][None], r["lse"][None])
+        o2, l2 = O.sparse_mla(inp, b, 0, idx[b])
+        check_attention(out[b][None], lse[b][None], o2[None], l2[None])
+        if name == "b64_ctx16k_128k_ties":
+            hot = set(inp.meta["hot_positions"][b].tolist())
+            assert hot <= set(idx[b].tolist())
