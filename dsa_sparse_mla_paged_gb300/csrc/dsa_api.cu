@@ -82,12 +82,8 @@ dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, c
   WsLayout L;
   if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
   char* w8 = static_cast<char*>(ws);
-  int* err = reinterpret_cast<int*>(w8 + L.err);
-  uint8_t* q8 = reinterpret_cast<uint8_t*>(w8 + L.q8);
-  float* wq = reinterpret_cast<float*>(w8 + L.wq);
-  cudaError_t e = launch_idx_q_quant(*params, q_idx, w, q8, wq, stream);
-  if (e == cudaSuccess)
-    e = launch_indexer(*params, q8, wq, key_pool, block_table, ctx_lens, scores, score_stride, err, stream);
+  cudaError_t e = launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
+  if (e == cudaSuccess) e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, score_stride, stream);
   return cuda_status(e);
 }
 
@@ -131,13 +127,9 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
   if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
   char* w8 = static_cast<char*>(ws);
   if (!topk_idx_out) topk_idx_out = reinterpret_cast<int32_t*>(w8 + L.topk);
-  int* err = reinterpret_cast<int*>(w8 + L.err);
-  uint8_t* q8 = reinterpret_cast<uint8_t*>(w8 + L.q8);
-  float* wq = reinterpret_cast<float*>(w8 + L.wq);
   float* scores = reinterpret_cast<float*>(w8 + L.scores);
-  cudaError_t e = launch_idx_q_quant(*params, q_idx, w, q8, wq, stream);
-  if (e == cudaSuccess)
-    e = launch_indexer(*params, q8, wq, key_pool, block_table, ctx_lens, scores, L.cap, err, stream);
+  cudaError_t e = launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
+  if (e == cudaSuccess) e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, L.cap, stream);
   if (e == cudaSuccess)
     e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream);
   if (e == cudaSuccess)

@@ -35,6 +35,7 @@ struct WsLayout {
   size_t err;       // int32 error word
   size_t q8;        // uint8 [rows][32][128] quantised indexer query
   size_t wq;        // float [rows][32] folded head weights
+  size_t tiles;     // int32 [batch] inclusive prefix of 128-token tiles per request
   size_t hist;      // int32 [rows][2048 + 2048 + 1024]
   size_t state;     // int32 [rows][kRowState]
   size_t ticket;    // int32 [rows][4] last-CTA tickets (zero between calls)
@@ -66,6 +67,7 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.err = o; o = align256(o + 256);
   L.q8 = o; o = align256(o + size_t(L.rows) * kIdxHeads * kIdxDim);
   L.wq = o; o = align256(o + size_t(L.rows) * kIdxHeads * 4);
+  L.tiles = o; o = align256(o + size_t(p.batch) * 4);
   L.hist = o; o = align256(o + size_t(L.rows) * (kHist0Bins + kHist1Bins + kHist2Bins) * 4);
   L.state = o; o = align256(o + size_t(L.rows) * kRowState * 4);
   L.ticket = o; o = align256(o + size_t(L.rows) * 4 * 4);
@@ -93,12 +95,11 @@ __device__ __forceinline__ int row_visible_len(const int32_t* ctx_lens, int b, i
 // ---------------------------------------------------------------- launchers
 // (each returns cudaGetLastError() of its launches)
 
-cudaError_t launch_idx_q_quant(const dsa_params_t& p, const void* q_idx, const float* w,
-                               uint8_t* q8, float* wq, cudaStream_t st);
-cudaError_t launch_indexer(const dsa_params_t& p, const uint8_t* q8, const float* wq,
-                           const void* key_pool, const int32_t* block_table,
-                           const int32_t* ctx_lens, float* scores, int64_t score_stride, int* err,
-                           cudaStream_t st);
+cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
+                               const float* w, const int32_t* ctx_lens, cudaStream_t st);
+cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
+                           const int32_t* block_table, const int32_t* ctx_lens, float* scores,
+                           int64_t score_stride, cudaStream_t st);
 cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                         int64_t score_stride, const int32_t* ctx_lens, const int32_t* block_table,
                         int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st);

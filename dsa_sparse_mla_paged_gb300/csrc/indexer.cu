@@ -7,7 +7,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "dsa_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace dsa {
 
@@ -20,9 +23,41 @@ namespace dsa {
 __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* __restrict__ q_idx,
                                                           const float* __restrict__ w,
                                                           uint8_t* __restrict__ q8,
-                                                          float* __restrict__ wq) {
+                                                          float* __restrict__ wq,
+                                                          const int32_t* __restrict__ ctx_lens, int batch,
+                                                          int n_q, int cap, int* __restrict__ tile_prefix,
+                                                          int* err) {
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (row == gridDim.x - 1) {
+    // Work plan of the scorer: tiles of 128 tokens (two pages) per request,
+    // inclusive prefix over the batch. An invalid context length gets no tiles.
+    __shared__ int wsum[4];
+    int carry = 0;
+    for (int b0 = 0; b0 < batch; b0 += 128) {
+      const int b = b0 + threadIdx.x;
+      int n = 0;
+      if (b < batch) {
+        const int c = ctx_lens[b];
+        if (c < n_q || c > cap) atomicOr(err, DSA_DEVERR_CTX);
+        else n = (c + 127) >> 7;
+      }
+      int x = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wsum[warp] = x;
+      __syncthreads();
+      int pre = carry;
+      for (int i = 0; i < warp; ++i) pre += wsum[i];
+      if (b < batch) tile_prefix[b] = pre + x;
+      carry += wsum[0] + wsum[1] + wsum[2] + wsum[3];
+      __syncthreads();
+    }
+    return;
+  }
   for (int hh = 0; hh < 8; ++hh) {
     const int h = warp * 8 + hh;
     const size_t base = (size_t(row) * kIdxHeads + h) * kIdxDim + lane * 4;
@@ -45,86 +80,332 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
   }
 }
 
-cudaError_t launch_idx_q_quant(const dsa_params_t& p, const void* q_idx, const float* w, uint8_t* q8,
-                               float* wq, cudaStream_t st) {
-  const int rows = p.batch * p.n_q;
-  idx_q_quant_kernel<<<rows, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(q_idx), w, q8, wq);
+cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
+                               const float* w, const int32_t* ctx_lens, cudaStream_t st) {
+  idx_q_quant_kernel<<<L.rows + 1, 128, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(q_idx), w, reinterpret_cast<uint8_t*>(ws + L.q8),
+      reinterpret_cast<float*>(ws + L.wq), ctx_lens, p.batch, p.n_q, L.cap,
+      reinterpret_cast<int*>(ws + L.tiles), reinterpret_cast<int*>(ws + L.err));
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// Reference-shaped SIMT scorer: one CTA per (page, request), all n_q rows.
+// Tensor-core scorer (sm_103a): a persistent CTA per SM walks a contiguous
+// range of the batch's 128-token tiles (two pages each), so every CTA streams
+// the same number of keys whatever the context lengths ("key-balanced").
+//   warp 0     : TMA producer -- key pages (128-B swizzled), their scales,
+//                and the request's FP8 query when the request changes
+//   warp 1     : TMEM owner and MMA issuer -- D[128 tok x 32*n_q] =
+//                keys[128 x 128] * q8^T, four K=32 FP8 MMAs per tile
+//   warps 2..5 : epilogue -- one token row per thread out of TMEM,
+//                score = sum_h w'_h * max(scale * D_h, 0), coalesced store
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float e4m3_to_float(uint8_t c) {
-  __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
-  return __half2float(__half(hr));
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kTileTok = 128;
+constexpr int kKeyTileBytes = kTileTok * kIdxDim;   // 16 KB
+constexpr int kScaleTileBytes = kTileTok * 4;       // 512 B
+
+struct IdxTc {
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  const int32_t* tile_prefix;
+  const float* wq;
+  const uint8_t* key_pool;
+  float* scores;
+  int64_t score_stride;
+  int64_t key_page_stride;
+  int batch, n_q, max_pages, num_pages, stages, nacc, ncol, tmem_cols;
+  int* err;
+};
+
+struct TileWalk {
+  int b, j;        // request, tile within the request
+  long long t;     // global tile index
+  int end_b;       // global tile index where request b ends
+};
+
+__device__ __forceinline__ void walk_start(const IdxTc& a, long long t0, TileWalk& w) {
+  int lo = 0, hi = a.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a.tile_prefix[mid] > t0) hi = mid; else lo = mid + 1;
+  }
+  w.b = lo;
+  w.end_b = a.tile_prefix[lo];
+  w.t = t0;
+  w.j = int(t0 - (lo ? a.tile_prefix[lo - 1] : 0));
 }
 
-__global__ void __launch_bounds__(256) indexer_simt_kernel(
-    const uint8_t* __restrict__ q8, const float* __restrict__ wq, const uint8_t* __restrict__ key_pool,
-    int64_t key_page_stride, const int32_t* __restrict__ block_table, int max_pages,
-    const int32_t* __restrict__ ctx_lens, int num_pages, int n_q, float* __restrict__ scores,
-    int64_t score_stride, int* err) {
-  extern __shared__ float sm[];
-  float* kf = sm;                              // [64][129]
-  float* qf = kf + 64 * 129;                   // [n_q*32][128]
-  float* part = qf + n_q * kIdxHeads * kIdxDim;  // [4][64]
-  __shared__ float ssc[64];
+__device__ __forceinline__ void walk_next(const IdxTc& a, TileWalk& w) {
+  ++w.t;
+  ++w.j;
+  while (w.t >= w.end_b && w.b + 1 < a.batch) {
+    ++w.b;
+    w.j = 0;
+    w.end_b = a.tile_prefix[w.b];
+  }
+}
 
-  const int lp = blockIdx.x, b = blockIdx.y;
-  const int cap = max_pages * kPage;
-  const int ctx = ctx_lens[b];
-  if (ctx < n_q || ctx > cap) {
-    if (lp == 0 && threadIdx.x == 0) atomicOr(err, DSA_DEVERR_CTX);
-    return;
+__device__ __forceinline__ int checked_page(const IdxTc& a, int b, int lp) {
+  const int pg = a.block_table[size_t(b) * a.max_pages + lp];
+  if (pg < 0 || pg >= a.num_pages) {
+    atomicOr(a.err, DSA_DEVERR_BLOCK_TABLE);
+    return 0;
   }
-  if (lp * kPage >= ctx) return;
-  int page = block_table[size_t(b) * max_pages + lp];
-  if (page < 0 || page >= num_pages) {
-    if (threadIdx.x == 0) atomicOr(err, DSA_DEVERR_BLOCK_TABLE);
-    page = 0;
+  return pg;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                   const __grid_constant__ CUtensorMap qmap,
+                                                                   IdxTc a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.stages, NA = a.nacc;
+  const int qbytes = a.n_q * kIdxHeads * kIdxDim;
+  uint8_t* keys = smem;                                   // S x 16 KB
+  uint8_t* qbuf = keys + size_t(S) * kKeyTileBytes;       // 2 x qbytes
+  float* scl = reinterpret_cast<float*>(qbuf + 2 * qbytes);  // S x 128
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scl + size_t(S) * kTileTok);
+  uint64_t* full = bars;
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + NA;
+  uint64_t* qfull = tempty + NA;
+  uint64_t* qempty = qfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long T = a.tile_prefix[a.batch - 1];
+  const long long t_begin = T * blockIdx.x / gridDim.x;
+  const long long t_end = T * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) { ptx::mbar_init(full + i, 1); ptx::mbar_init(empty + i, 1 + 4); }
+    for (int i = 0; i < NA; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, 4); }
+    for (int i = 0; i < 2; ++i) { ptx::mbar_init(qfull + i, 1); ptx::mbar_init(qempty + i, 1); }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
   }
-  const uint8_t* pg = key_pool + size_t(page) * key_page_stride;
-  for (int i = threadIdx.x; i < 64 * 128; i += 256) kf[(i >> 7) * 129 + (i & 127)] = e4m3_to_float(pg[i]);
-  if (threadIdx.x < 64) ssc[threadIdx.x] = reinterpret_cast<const float*>(pg + 64 * 128)[threadIdx.x];
-  const uint8_t* qrow = q8 + size_t(b) * n_q * kIdxHeads * kIdxDim;
-  for (int i = threadIdx.x; i < n_q * kIdxHeads * kIdxDim; i += 256) qf[i] = e4m3_to_float(qrow[i]);
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, a.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
   __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  const int j = threadIdx.x & 63, g = threadIdx.x >> 6;
-  const float sc = ssc[j];
-  for (int t = 0; t < n_q; ++t) {
-    float acc = 0.f;
-    for (int hh = 0; hh < 8; ++hh) {
-      const int h = g * 8 + hh;
-      const float* qv = qf + (t * kIdxHeads + h) * kIdxDim;
-      const float* kv = kf + j * 129;
-      float d = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < kIdxDim; ++i) d = fmaf(qv[i], kv[i], d);
-      acc += wq[(size_t(b) * n_q + t) * kIdxHeads + h] * fmaxf(sc * d, 0.f);
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(a.err, DSA_DEVERR_TIMEOUT);
+  };
+
+  if (t_begin < t_end) {
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        ptx::prefetch_tmap(&kmap);
+        ptx::prefetch_tmap(&qmap);
+        TileWalk w;
+        walk_start(a, t_begin, w);
+        int cur_b = -1, nq = -1, npages = 0;
+        for (long long k = 0; w.t < t_end; ++k, walk_next(a, w)) {
+          if (*abort_flag) break;
+          const int s = int(k % S);
+          const uint32_t ph = uint32_t(k / S) & 1u;
+          if (w.b != cur_b) {
+            ++nq;
+            const int slot = nq & 1;
+            if (!ptx::mbar_wait(qempty + slot, (uint32_t(nq >> 1) & 1u) ^ 1u)) { fail(); break; }
+            ptx::mbar_arrive_expect_tx(qfull + slot, qbytes);
+            ptx::tma_load_2d(qbuf + slot * qbytes, &qmap, qfull + slot, 0, w.b * a.n_q * kIdxHeads);
+            cur_b = w.b;
+            npages = (a.ctx_lens[w.b] + kPage - 1) / kPage;
+          }
+          if (!ptx::mbar_wait(empty + s, ph ^ 1u)) { fail(); break; }
+          const int lp0 = 2 * w.j;
+          const bool two = lp0 + 1 < npages;
+          ptx::mbar_arrive_expect_tx(full + s, (two ? 2u : 1u) * (kPage * kIdxDim + kPage * 4));
+          const int pg0 = checked_page(a, w.b, lp0);
+          ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes, &kmap, full + s, 0, 0, pg0);
+          ptx::bulk_load(scl + size_t(s) * kTileTok, a.key_pool + size_t(pg0) * a.key_page_stride + kPage * kIdxDim,
+                         kPage * 4, full + s);
+          if (two) {
+            const int pg1 = checked_page(a, w.b, lp0 + 1);
+            ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes + kPage * kIdxDim, &kmap, full + s, 0, 0, pg1);
+            ptx::bulk_load(scl + size_t(s) * kTileTok + kPage,
+                           a.key_pool + size_t(pg1) * a.key_page_stride + kPage * kIdxDim, kPage * 4, full + s);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        const uint32_t id = ptx::idesc(0, 0, kTileTok, uint32_t(a.n_q * kIdxHeads));
+        TileWalk w;
+        walk_start(a, t_begin, w);
+        int cur_b = -1, nq = -1;
+        for (long long k = 0; w.t < t_end; ++k, walk_next(a, w)) {
+          if (*abort_flag) break;
+          const int s = int(k % S);
+          const uint32_t ph = uint32_t(k / S) & 1u;
+          const int acc = int(k % NA);
+          const uint32_t aph = uint32_t(k / NA) & 1u;
+          if (w.b != cur_b) {
+            if (cur_b >= 0) ptx::mma_commit(qempty + (nq & 1));
+            ++nq;
+            if (!ptx::mbar_wait(qfull + (nq & 1), uint32_t(nq >> 1) & 1u)) { fail(); break; }
+            cur_b = w.b;
+          }
+          if (!ptx::mbar_wait(tempty + acc, aph ^ 1u)) { fail(); break; }
+          if (!ptx::mbar_wait(full + s, ph)) { fail(); break; }
+          ptx::tc_fence_after();
+          const uint32_t a_base = ptx::smem_u32(keys + size_t(s) * kKeyTileBytes);
+          const uint32_t b_base = ptx::smem_u32(qbuf + (nq & 1) * qbytes);
+          const uint32_t d = tmem + uint32_t(acc * a.ncol);
+#pragma unroll
+          for (int kk = 0; kk < kIdxDim / 32; ++kk)
+            ptx::mma_f8f6f4(d, ptx::sdesc_sw128(a_base + kk * 32), ptx::sdesc_sw128(b_base + kk * 32), id,
+                            kk > 0 ? 1u : 0u);
+          ptx::mma_commit(empty + s);
+          ptx::mma_commit(tfull + acc);
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue
+      const int quad = warp & 3;
+      const int rowt = quad * 32 + lane;
+      TileWalk w;
+      walk_start(a, t_begin, w);
+      int cur_b = -1, ctx = 0;
+      for (long long k = 0; w.t < t_end; ++k, walk_next(a, w)) {
+        if (*abort_flag) break;
+        const int s = int(k % S);
+        const int acc = int(k % NA);
+        const uint32_t aph = uint32_t(k / NA) & 1u;
+        if (w.b != cur_b) {
+          cur_b = w.b;
+          ctx = a.ctx_lens[w.b];
+        }
+        if (!ptx::mbar_wait(tfull + acc, aph)) { fail(); break; }
+        ptx::tc_fence_after();
+        const float sc = scl[size_t(s) * kTileTok + rowt];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty + s);
+        const int tok = w.j * kTileTok + rowt;
+        for (int t = 0; t < a.n_q; ++t) {
+          float v[32];
+          ptx::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(acc * a.ncol + t * 32), v);
+          const float* wr = a.wq + (size_t(w.b) * a.n_q + t) * kIdxHeads;
+          float sum = 0.f;
+#pragma unroll
+          for (int h = 0; h < kIdxHeads; ++h) sum = fmaf(__ldg(wr + h), fmaxf(sc * v[h], 0.f), sum);
+          const int Lt = ctx - a.n_q + t + 1;
+          if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + t) * a.score_stride + tok] = sum;
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty + acc);
+      }
     }
-    part[g * 64 + j] = acc;
-    __syncthreads();
-    if (threadIdx.x < 64) {
-      const int s = lp * kPage + threadIdx.x;
-      const int L = ctx - n_q + t + 1;
-      const float v = (part[threadIdx.x] + part[64 + threadIdx.x]) + (part[128 + threadIdx.x] + part[192 + threadIdx.x]);
-      if (s < L && s < score_stride) scores[(size_t(b) * n_q + t) * score_stride + s] = v;
-    }
-    __syncthreads();
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, a.tmem_cols);
   }
 }
 
-cudaError_t launch_indexer(const dsa_params_t& p, const uint8_t* q8, const float* wq, const void* key_pool,
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+bool encode_u8_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                   const uint32_t* box, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, cuuint32_t(rank), const_cast<void*>(base),
+                  reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides),
+                  reinterpret_cast<const cuuint32_t*>(box), es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
                            const int32_t* block_table, const int32_t* ctx_lens, float* scores,
-                           int64_t score_stride, int* err, cudaStream_t st) {
-  const size_t smem = (64 * 129 + size_t(p.n_q) * kIdxHeads * kIdxDim + 4 * 64) * sizeof(float);
-  cudaFuncSetAttribute(indexer_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  dim3 grid(p.max_pages_per_req, p.batch);
-  indexer_simt_kernel<<<grid, 256, smem, st>>>(q8, wq, static_cast<const uint8_t*>(key_pool), p.key_page_stride,
-                                              block_table, p.max_pages_per_req, ctx_lens, p.num_pages, p.n_q,
-                                              scores, score_stride, err);
+                           int64_t score_stride, cudaStream_t st) {
+  const uint8_t* q8 = reinterpret_cast<const uint8_t*>(ws + L.q8);
+  const float* wq = reinterpret_cast<const float*>(ws + L.wq);
+  int* err = reinterpret_cast<int*>(ws + L.err);
+  CUtensorMap kmap, qmap;
+  {
+    const uint64_t dims[3] = {uint64_t(kIdxDim), uint64_t(kPage), uint64_t(p.num_pages)};
+    const uint64_t strides[2] = {uint64_t(kIdxDim), uint64_t(p.key_page_stride)};
+    const uint32_t box[3] = {uint32_t(kIdxDim), uint32_t(kPage), 1};
+    if (!encode_u8_map(&kmap, key_pool, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {uint64_t(kIdxDim), uint64_t(L.rows) * kIdxHeads};
+    const uint64_t strides[1] = {uint64_t(kIdxDim)};
+    const uint32_t box[2] = {uint32_t(kIdxDim), uint32_t(p.n_q * kIdxHeads)};
+    if (!encode_u8_map(&qmap, q8, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
+  }
+  IdxTc a;
+  a.block_table = block_table;
+  a.ctx_lens = ctx_lens;
+  a.tile_prefix = reinterpret_cast<const int32_t*>(ws + L.tiles);
+  a.wq = wq;
+  a.key_pool = static_cast<const uint8_t*>(key_pool);
+  a.scores = scores;
+  a.score_stride = score_stride;
+  a.key_page_stride = p.key_page_stride;
+  a.batch = p.batch;
+  a.n_q = p.n_q;
+  a.max_pages = p.max_pages_per_req;
+  a.num_pages = p.num_pages;
+  a.ncol = p.n_q * kIdxHeads;
+  a.nacc = a.ncol <= 64 ? 4 : (a.ncol <= 128 ? 4 : 2);
+  int cols = 32;
+  while (cols < a.nacc * a.ncol) cols <<= 1;
+  a.tmem_cols = cols;
+  a.stages = p.n_q <= 2 ? 8 : 6;
+  a.err = err;
+  const size_t smem = 1024 + size_t(a.stages) * (kKeyTileBytes + kScaleTileBytes) +
+                      2 * size_t(p.n_q) * kIdxHeads * kIdxDim + (2 * a.stages + 2 * a.nacc + 4) * 8 + 16;
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  // enough tiles for every SM is the common case; with fewer, one CTA per tile
+  const long long max_tiles = (long long)p.batch * ((L.cap + kTileTok - 1) / kTileTok);
+  const int grid = int(std::min<long long>(sm_count(), std::max<long long>(1, max_tiles)));
+  indexer_tc_kernel<<<grid, kTcThreads, smem, st>>>(kmap, qmap, a);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,7 @@ typedef enum { DSA_LAT_FP8_576 = 0, DSA_LAT_NVFP4_352 = 1 } dsa_lat_fmt_t;
 #define DSA_DEVERR_BLOCK_TABLE 0x1  /* a block-table entry outside [0, num_pages) */
 #define DSA_DEVERR_CTX 0x2          /* ctx_b outside [n_q, max_pages_per_req * page_size] */
 #define DSA_DEVERR_TOPK_INDEX 0x4   /* a top-k index outside [-1, L_{b,t}) */
+#define DSA_DEVERR_TIMEOUT 0x8      /* a bounded in-kernel wait gave up (results unspecified) */
 
 typedef struct {
   int32_t batch;              /* B >= 1 */
