@@ -5,8 +5,8 @@ module only turns tensors into device pointers and status codes into
 exceptions. There is no fallback: if libdsa.so is missing, ``load()`` raises.
 
 Entry points mirror include/dsa.h: ``workspace_size``, ``indexer_scores``,
-``topk``, ``sparse_mla_decode``, ``decode``, ``get_device_error``,
-``status_string``.
+``topk``, ``topk_noalloc``, ``sparse_mla_decode``, ``decode``,
+``get_device_error``, ``status_string``.
 """
 from __future__ import annotations
 
@@ -29,6 +29,7 @@ EXPORTS = (
     "dsa_workspace_size",
     "dsa_indexer_scores",
     "dsa_topk",
+    "dsa_topk_noalloc",
     "dsa_sparse_mla_decode",
     "dsa_decode",
     "dsa_get_device_error",
@@ -96,6 +97,7 @@ def load() -> ctypes.CDLL:
         "dsa_workspace_size": [P, ctypes.POINTER(sz)],
         "dsa_indexer_scores": [P, vp, vp, vp, vp, vp, vp, i64, vp, sz, vp],
         "dsa_topk": [P, vp, i64, vp, vp, vp, vp, vp, sz, vp],
+        "dsa_topk_noalloc": [P, vp, i64, vp, vp, vp, vp, vp],
         "dsa_sparse_mla_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_get_device_error": [vp, vp, ctypes.POINTER(ctypes.c_int32)],
@@ -156,6 +158,14 @@ def topk(params, scores, score_stride, ctx_lens, block_table, topk_idx, phys_row
     _check("dsa_topk", load().dsa_topk(
         ctypes.byref(params), _ptr(scores), int(score_stride), _ptr(ctx_lens), _ptr(block_table),
         _ptr(topk_idx), _ptr(phys_rows), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def topk_noalloc(params, scores, score_stride, ctx_lens, block_table, topk_idx, phys_rows, stream=None):
+    """dsa_topk without a workspace: for callers that cannot allocate device
+    memory; its scratch is a static array inside libdsa (limits in include/dsa.h)."""
+    _check("dsa_topk_noalloc", load().dsa_topk_noalloc(
+        ctypes.byref(params), _ptr(scores), int(score_stride), _ptr(ctx_lens), _ptr(block_table),
+        _ptr(topk_idx), _ptr(phys_rows), _stream(stream)))
 
 
 def sparse_mla_decode(params, q, lat_pool, block_table, ctx_lens, topk_idx, out, lse, ws, stream=None):

@@ -173,6 +173,29 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
                         float* lse, int32_t* topk_idx_out, void* ws, size_t ws_bytes,
                         cudaStream_t stream);
 
+/* Stage 2 without a workspace, for callers that cannot allocate device memory
+ * when they select tokens (a plugin whose host owns every device byte, a
+ * real-time loop that must not enter the allocator, a caller handed only input
+ * and output pointers). The paper has no counterpart: this is a deployment
+ * variant of dsa_topk, with the same arguments minus the workspace and the same
+ * results bit for bit.
+ * - Scratch: one static device array of about 1.6 MB inside libdsa, held by
+ *   every GPU that loads the library until the process exits. The call
+ *   allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * - Limits: batch * n_q <= 64 and max_pages_per_req * page_size <= 1,048,576;
+ *   larger problems return DSA_ERR_UNSUPPORTED and launch nothing.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, on the current device); make that first call before any stream
+ *   capture.
+ * - Every call shares the array: calls whose kernels overlap on the GPU (two
+ *   streams, two threads) race and give wrong results; order them. Each call
+ *   clears the parts that must start at zero itself.
+ * - Bad data found on the device is skipped as in dsa_topk, but there is no
+ *   workspace error word to report it through. */
+dsa_status_t dsa_topk_noalloc(const dsa_params_t* params, const float* scores, int64_t score_stride,
+                              const int32_t* ctx_lens, const int32_t* block_table, int32_t* topk_idx,
+                              int32_t* phys_rows, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the
  * workspace `ws` into *code (0 = no error; DSA_DEVERR_* bits otherwise). */
 dsa_status_t dsa_get_device_error(void* ws, cudaStream_t stream, int32_t* code);
