@@ -49,6 +49,22 @@ def indexer_bytes(ctx, n_q):
     return sum(KEY_B * int(c) for c in ctx) + len(ctx) * n_q * (32 * 128 * 2 + 32 * 4)
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest of each rank's value (the slowest rank sets the step time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(ms_per_step: float, world: int) -> float:
+    """Layer-steps/s of the whole job: every rank runs one replica step per ms_per_step."""
+    return world * 1e3 / ms_per_step
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -164,6 +180,50 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_stage(args):
+    """Time one stage entry point alone (for kernel profiles): `--stage indexer|topk|mla`."""
+    import torch
+
+    import dsa_sparse_mla_paged_gb300 as dsa
+    import gen
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from dsa_testlib import Dev
+
+    torch.cuda.set_device(0)
+    dsa.load()
+    inp = gen.make_workload(args.workload)
+    d = Dev(inp)
+    sc = torch.empty((d.rows, d.cap), dtype=torch.float32, device="cuda")
+    idx = torch.empty((d.rows, inp.topk), dtype=torch.int32, device="cuda")
+    out = torch.empty((d.rows, 96, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((d.rows, 96), dtype=torch.float32, device="cuda")
+    # inputs of the later stages come from the earlier ones, computed once untimed
+    dsa.indexer_scores(d.p, d.q_idx, d.w, d.key_pool, d.block_table, d.ctx, sc, d.cap, d.ws)
+    dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws)
+    calls = {
+        "indexer": lambda: dsa.indexer_scores(d.p, d.q_idx, d.w, d.key_pool, d.block_table, d.ctx, sc, d.cap, d.ws),
+        "topk": lambda: dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws),
+        "mla": lambda: dsa.sparse_mla_decode(d.p, d.q, d.lat_pool, d.block_table, d.ctx, idx, out, lse, d.ws),
+    }
+    f = calls[args.stage]
+    for _ in range(args.warmup):
+        f()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(args.steps):
+        f()
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    nbytes = {"indexer": indexer_bytes(inp.ctx, inp.n_q), "topk": 4 * sum(int(c) for c in inp.ctx) * inp.n_q,
+              "mla": step_bytes(inp.ctx, inp.n_q, inp.topk) - indexer_bytes(inp.ctx, inp.n_q)}[args.stage]
+    assert dsa.get_device_error(d.ws) == 0
+    print(json.dumps({"stage": args.stage, "workload": args.workload, "ms": ms, "bytes": nbytes,
+                      "gbs": nbytes / (ms * 1e-3) / 1e9}), flush=True)
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -225,11 +285,7 @@ def run_ours(args, rank, world):
                 graph.replay()
             ev1.record(stream)
         barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, "cuda")
 
     # per-stage times (the three stage entry points, events on the launching stream)
     stage_ms = {"indexer": 0.0, "topk": 0.0, "sparse_mla": 0.0}
@@ -270,11 +326,7 @@ def run_ours(args, rank, world):
             h_out[1].copy_(lse, non_blocking=True)
         ev[1].record(stream)
     barrier()
-    e2e_ms = ev[0].elapsed_time(ev[1]) / ke2e
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(ev[0].elapsed_time(ev[1]) / ke2e, dist, "cuda")
 
     if rank == 0:
         peak, peak_kind = peaks()
@@ -283,7 +335,7 @@ def run_ours(args, rank, world):
         gbs = sbytes / (ms * 1e-3) / 1e9
         idx_gbs = ibytes / (stage_ms["indexer"] * 1e-3) / 1e9
         line = {
-            "metric": METRIC, "value": world * 1e3 / ms, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": replica_throughput(ms, world), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8+bf16", "data": "synthetic",
             "config": {"workload": args.workload, "batch": inp.batch, "n_q": inp.n_q,
@@ -296,7 +348,7 @@ def run_ours(args, rank, world):
             "roofline": {"bound": "hbm", "kernel": "indexer (dsa_indexer_scores)", "achieved": idx_gbs,
                          "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
                          "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": ibytes},
-            "e2e": {"value": world * 1e3 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": replica_throughput(e2e_ms, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * dsa.KERNELS_PER_DECODE,
             "clocks": clk.summary(),
@@ -316,12 +368,16 @@ def main():
     ap.add_argument("--workload", default="b4_ctx1m")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage", default="all", choices=["all", "indexer", "topk", "mla"],
+                    help="time one stage entry point alone (kernel profiling)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
         run_reference(args, rank)
+    elif args.stage != "all":
+        run_stage(args)
     else:
         run_ours(args, rank, world)
 

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libdsa translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,8 +28,11 @@ constexpr int kHist1Bins = 2048;  // bits 20..10
 constexpr int kHist2Bins = 1024;  // bits 9..0
 constexpr int kRowState = 16;     // int32 words of per-row selection state
 
-// sparse attention: at most this many KV splits per row.
-constexpr int kMaxSplits = 16;
+// sparse attention: the K selected slots of a row are cut into splits of this
+// many tokens, one CTA pair each. The split size depends on nothing but K, so a
+// request's result does not depend on the batch it is in.
+constexpr int kSplitTok = 256;
+constexpr int kMaxSplits = (kMaxTopK + kSplitTok - 1) / kSplitTok;
 
 // Byte offsets of the workspace regions (all 256-B aligned).
 struct WsLayout {
@@ -51,18 +55,15 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// KV splits of the attention for `rows` rows (same function for sizing and launch).
-inline int attention_splits(int rows) {
-  int s = (512 + rows - 1) / rows;
-  return s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
-}
+// KV splits of the attention for top-k size `topk` (same function for sizing and launch).
+inline int attention_splits(int topk) { return (topk + kSplitTok - 1) / kSplitTok; }
 
 inline WsLayout ws_layout(const dsa_params_t& p) {
   WsLayout L{};
   L.rows = p.batch * p.n_q;
   L.cap = p.max_pages_per_req * p.page_size;
   L.max_chunks = (L.cap + kTopkChunk - 1) / kTopkChunk;
-  L.splits = attention_splits(L.rows);
+  L.splits = attention_splits(p.topk);
   size_t o = 0;
   L.err = o; o = align256(o + 256);
   L.q8 = o; o = align256(o + size_t(L.rows) * kIdxHeads * kIdxDim);
@@ -91,6 +92,12 @@ __device__ __forceinline__ int row_visible_len(const int32_t* ctx_lens, int b, i
   }
   return c - n_q + t + 1;
 }
+
+// Number of SMs of the current device.
+int sm_count();
+// Tiled TMA tensor map (cuTensorMapEncodeTiled through the runtime's driver entry point).
+bool encode_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, bool swizzle128);
 
 // ---------------------------------------------------------------- launchers
 // (each returns cudaGetLastError() of its launches)

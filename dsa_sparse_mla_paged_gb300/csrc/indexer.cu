@@ -157,6 +157,41 @@ __device__ __forceinline__ int checked_page(const IdxTc& a, int b, int lp) {
   return pg;
 }
 
+// Physical pages of one tile (pg1 = -1 when the tile holds a single page).
+struct TilePages {
+  int b, pg0, pg1;
+};
+
+// Move the walk `n` tiles forward; `np` tracks the pages of the walk's request.
+__device__ __forceinline__ void advance_walk(const IdxTc& a, TileWalk& w, int& np, int n) {
+  w.t += n;
+  w.j += n;
+  if (w.t >= w.end_b) {
+    const int b0 = w.b;
+    while (w.t >= w.end_b && w.b + 1 < a.batch) {
+      ++w.b;
+      w.end_b = a.tile_prefix[w.b];
+    }
+    w.j = int(w.t - (w.b ? a.tile_prefix[w.b - 1] : 0));
+    if (w.b != b0) np = (a.ctx_lens[w.b] + kPage - 1) / kPage;
+  }
+}
+
+// Lane `lane` of the producer warp: the pages of tile (w.t + lane).
+__device__ __forceinline__ TilePages tile_pages(const IdxTc& a, const TileWalk& w, int np, long long t_end,
+                                                int lane) {
+  TilePages tp{w.b, 0, -1};
+  if (w.t + lane >= t_end) return tp;
+  TileWalk x = w;
+  int xnp = np;
+  if (lane) advance_walk(a, x, xnp, lane);
+  tp.b = x.b;
+  const int lp0 = 2 * x.j;
+  tp.pg0 = checked_page(a, x.b, lp0);
+  if (lp0 + 1 < xnp) tp.pg1 = checked_page(a, x.b, lp0 + 1);
+  return tp;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap qmap,
                                                                    IdxTc a) {
@@ -206,40 +241,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
   if (t_begin < t_end) {
     if (warp == 0) {
       // ------------------------------------------------------------ producer
+      // The whole warp looks 32 tiles ahead: lane i loads the block-table
+      // entries of tile (chunk + i) one chunk before lane 0 issues its copies,
+      // so no copy waits on a dependent global load.
       if (lane == 0) {
         ptx::prefetch_tmap(&kmap);
         ptx::prefetch_tmap(&qmap);
-        TileWalk w;
-        walk_start(a, t_begin, w);
-        int cur_b = -1, nq = -1, npages = 0;
-        for (long long k = 0; w.t < t_end; ++k, walk_next(a, w)) {
-          if (*abort_flag) break;
-          const int s = int(k % S);
-          const uint32_t ph = uint32_t(k / S) & 1u;
-          if (w.b != cur_b) {
-            ++nq;
-            const int slot = nq & 1;
-            if (!ptx::mbar_wait(qempty + slot, (uint32_t(nq >> 1) & 1u) ^ 1u)) { fail(); break; }
-            ptx::mbar_arrive_expect_tx(qfull + slot, qbytes);
-            ptx::tma_load_2d(qbuf + slot * qbytes, &qmap, qfull + slot, 0, w.b * a.n_q * kIdxHeads);
-            cur_b = w.b;
-            npages = (a.ctx_lens[w.b] + kPage - 1) / kPage;
+      }
+      TileWalk base;
+      walk_start(a, t_begin, base);
+      int base_np = (a.ctx_lens[base.b] + kPage - 1) / kPage;
+      TilePages cur = tile_pages(a, base, base_np, t_end, lane);
+      int cur_b = -1, nq = -1;
+      long long k = 0;
+      for (long long tc = t_begin; tc < t_end; tc += 32) {
+        // advance the base walk by 32 tiles and prefetch that chunk
+        TileWalk nb = base;
+        int nb_np = base_np;
+        advance_walk(a, nb, nb_np, 32);
+        const TilePages nxt = tile_pages(a, nb, nb_np, t_end, lane);
+        const int n = int(t_end - tc < 32 ? t_end - tc : 32);
+        bool ok = true;
+        for (int i = 0; i < n; ++i, ++k) {
+          const int b = __shfl_sync(0xffffffffu, cur.b, i);
+          const int pg0 = __shfl_sync(0xffffffffu, cur.pg0, i);
+          const int pg1 = __shfl_sync(0xffffffffu, cur.pg1, i);
+          if (lane == 0 && ok) {
+            if (*abort_flag) ok = false;
+            const int s = int(k % S);
+            const uint32_t ph = uint32_t(k / S) & 1u;
+            if (ok && b != cur_b) {
+              ++nq;
+              const int slot = nq & 1;
+              if (!ptx::mbar_wait(qempty + slot, (uint32_t(nq >> 1) & 1u) ^ 1u)) { fail(); ok = false; }
+              if (ok) {
+                ptx::mbar_arrive_expect_tx(qfull + slot, qbytes);
+                ptx::tma_load_2d(qbuf + slot * qbytes, &qmap, qfull + slot, 0, b * a.n_q * kIdxHeads);
+                cur_b = b;
+              }
+            }
+            if (ok && !ptx::mbar_wait(empty + s, ph ^ 1u)) { fail(); ok = false; }
+            if (ok) {
+              const bool two = pg1 >= 0;
+              ptx::mbar_arrive_expect_tx(full + s, (two ? 2u : 1u) * (kPage * kIdxDim + kPage * 4));
+              ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes, &kmap, full + s, 0, 0, pg0);
+              ptx::bulk_load(scl + size_t(s) * kTileTok, a.key_pool + size_t(pg0) * a.key_page_stride + kPage * kIdxDim,
+                             kPage * 4, full + s);
+              if (two) {
+                ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes + kPage * kIdxDim, &kmap, full + s, 0, 0, pg1);
+                ptx::bulk_load(scl + size_t(s) * kTileTok + kPage,
+                               a.key_pool + size_t(pg1) * a.key_page_stride + kPage * kIdxDim, kPage * 4, full + s);
+              }
+            }
           }
-          if (!ptx::mbar_wait(empty + s, ph ^ 1u)) { fail(); break; }
-          const int lp0 = 2 * w.j;
-          const bool two = lp0 + 1 < npages;
-          ptx::mbar_arrive_expect_tx(full + s, (two ? 2u : 1u) * (kPage * kIdxDim + kPage * 4));
-          const int pg0 = checked_page(a, w.b, lp0);
-          ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes, &kmap, full + s, 0, 0, pg0);
-          ptx::bulk_load(scl + size_t(s) * kTileTok, a.key_pool + size_t(pg0) * a.key_page_stride + kPage * kIdxDim,
-                         kPage * 4, full + s);
-          if (two) {
-            const int pg1 = checked_page(a, w.b, lp0 + 1);
-            ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes + kPage * kIdxDim, &kmap, full + s, 0, 0, pg1);
-            ptx::bulk_load(scl + size_t(s) * kTileTok + kPage,
-                           a.key_pool + size_t(pg1) * a.key_page_stride + kPage * kIdxDim, kPage * 4, full + s);
-          }
+          __syncwarp();
         }
+        if (!__shfl_sync(0xffffffffu, int(ok), 0)) break;
+        base = nb;
+        base_np = nb_np;
+        cur = nxt;
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
@@ -281,6 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
       TileWalk w;
       walk_start(a, t_begin, w);
       int cur_b = -1, ctx = 0;
+      float wl[kMaxNQ];  // lane h holds w'_h of each query row of the current request
       for (long long k = 0; w.t < t_end; ++k, walk_next(a, w)) {
         if (*abort_flag) break;
         const int s = int(k % S);
@@ -289,6 +350,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
         if (w.b != cur_b) {
           cur_b = w.b;
           ctx = a.ctx_lens[w.b];
+#pragma unroll
+          for (int t = 0; t < kMaxNQ; ++t)
+            wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
         }
         if (!ptx::mbar_wait(tfull + acc, aph)) { fail(); break; }
         ptx::tc_fence_after();
@@ -296,13 +360,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty + s);
         const int tok = w.j * kTileTok + rowt;
-        for (int t = 0; t < a.n_q; ++t) {
+#pragma unroll
+        for (int t = 0; t < kMaxNQ; ++t) {
+          if (t >= a.n_q) break;
           float v[32];
           ptx::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(acc * a.ncol + t * 32), v);
-          const float* wr = a.wq + (size_t(w.b) * a.n_q + t) * kIdxHeads;
           float sum = 0.f;
 #pragma unroll
-          for (int h = 0; h < kIdxHeads; ++h) sum = fmaf(__ldg(wr + h), fmaxf(sc * v[h], 0.f), sum);
+          for (int h = 0; h < kIdxHeads; ++h)
+            sum = fmaf(__shfl_sync(0xffffffffu, wl[t], h), fmaxf(sc * v[h], 0.f), sum);
           const int Lt = ctx - a.n_q + t + 1;
           if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + t) * a.score_stride + tok] = sum;
         }
@@ -346,12 +412,12 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-bool encode_u8_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                   const uint32_t* box, bool swizzle128) {
+bool encode_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, cuuint32_t(rank), const_cast<void*>(base),
+  CUresult r = fn(m, dtype, cuuint32_t(rank), const_cast<void*>(base),
                   reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides),
                   reinterpret_cast<const cuuint32_t*>(box), es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -370,13 +436,13 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
     const uint64_t dims[3] = {uint64_t(kIdxDim), uint64_t(kPage), uint64_t(p.num_pages)};
     const uint64_t strides[2] = {uint64_t(kIdxDim), uint64_t(p.key_page_stride)};
     const uint32_t box[3] = {uint32_t(kIdxDim), uint32_t(kPage), 1};
-    if (!encode_u8_map(&kmap, key_pool, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
+    if (!encode_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, key_pool, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   {
     const uint64_t dims[2] = {uint64_t(kIdxDim), uint64_t(L.rows) * kIdxHeads};
     const uint64_t strides[1] = {uint64_t(kIdxDim)};
     const uint32_t box[2] = {uint32_t(kIdxDim), uint32_t(p.n_q * kIdxHeads)};
-    if (!encode_u8_map(&qmap, q8, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
+    if (!encode_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q8, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   IdxTc a;
   a.block_table = block_table;

@@ -115,6 +115,28 @@ __device__ __forceinline__ RowInfo row_info(const TopkArgs& a) {
   return ri;
 }
 
+// The chunk's scores for this thread: 4 float4 loads (all issued before any
+// use), element i*1024 + 4*tid + e of the chunk; `n[i]` valid lanes per load.
+struct ChunkVals {
+  float v[4][4];
+  int n[4];
+};
+
+__device__ __forceinline__ void load_chunk(const float* row, int s0, int s1, ChunkVals& c) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = s0 + i * kThreads * 4 + threadIdx.x * 4;
+    c.n[i] = min(4, max(0, s1 - s));
+    if (c.n[i] == 4) {
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(row + s));
+      c.v[i][0] = f.x; c.v[i][1] = f.y; c.v[i][2] = f.z; c.v[i][3] = f.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c.v[i][e] = e < c.n[i] ? row[s + e] : 0.f;
+    }
+  }
+}
+
 // Histogram pass `pass` (0, 1, 2) of one chunk.
 template <int PASS>
 __global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
@@ -134,23 +156,18 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
   const float* row = a.scores + size_t(ri.r) * a.stride;
   const int s0 = ri.c * kTopkChunk;
   const int s1 = min(ri.L, s0 + kTopkChunk);
-  for (int s = s0 + threadIdx.x * 4; s < s1; s += kThreads * 4) {
-    float v[4];
-    int n = 4;
-    if (s + 4 <= s1) {
-      const float4 f = *reinterpret_cast<const float4*>(row + s);
-      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-    } else {
-      n = s1 - s;
-      for (int i = 0; i < n; ++i) v[i] = row[s + i];
-    }
-    for (int i = 0; i < n; ++i) {
-      const uint32_t u = order_key(v[i]);
+  ChunkVals cv;
+  load_chunk(row, s0, s1, cv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (e >= cv.n[i]) break;
+      const uint32_t u = order_key(cv.v[i][e]);
       if (PASS == 0) atomicAdd(&sh[u >> 21], 1);
       if (PASS == 1 && (u >> 21) == prefix) atomicAdd(&sh[(u >> 10) & 2047u], 1);
       if (PASS == 2 && (u >> 10) == prefix) atomicAdd(&sh[u & 1023u], 1);
     }
-  }
   __syncthreads();
   int* gh = a.hist + size_t(ri.r) * (kHist0Bins + kHist1Bins + kHist2Bins) +
             (PASS == 0 ? 0 : PASS == 1 ? kHist0Bins : kHist0Bins + kHist1Bins);
@@ -187,11 +204,17 @@ __global__ void __launch_bounds__(kThreads) topk_count_kernel(TopkArgs a) {
   const int s0 = ri.c * kTopkChunk;
   const int s1 = min(ri.L, s0 + kTopkChunk);
   int gt = 0, eq = 0;
-  for (int s = s0 + threadIdx.x; s < s1; s += kThreads) {
-    const uint32_t u = order_key(row[s]);
-    gt += u > tau;
-    eq += u == tau;
-  }
+  ChunkVals cv;
+  load_chunk(row, s0, s1, cv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (e >= cv.n[i]) break;
+      const uint32_t u = order_key(cv.v[i][e]);
+      gt += u > tau;
+      eq += u == tau;
+    }
   int tg, te;
   block_excl_scan(gt, &tg, sm8);
   block_excl_scan(eq, &te, sm8);
@@ -260,39 +283,38 @@ __global__ void __launch_bounds__(kThreads) topk_write_kernel(TopkArgs a) {
   const float* row = a.scores + size_t(ri.r) * a.stride;
   const int s0 = ri.c * kTopkChunk;
   const int s1 = min(ri.L, s0 + kTopkChunk);
-  for (int base = s0; base < s1; base += kThreads * 4) {
-    const int s = base + threadIdx.x * 4;
+  ChunkVals cv;
+  load_chunk(row, s0, s1, cv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = s0 + i * kThreads * 4 + threadIdx.x * 4;
+    const int n = cv.n[i];
     uint32_t u[4];
-    int n = 0;
-    if (s + 4 <= s1) {
-      const float4 f = *reinterpret_cast<const float4*>(row + s);
-      u[0] = order_key(f.x); u[1] = order_key(f.y); u[2] = order_key(f.z); u[3] = order_key(f.w);
-      n = 4;
-    } else {
-      for (int i = 0; i < 4; ++i)
-        if (s + i < s1) { u[i] = order_key(row[s + i]); n = i + 1; }
-    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) u[e] = order_key(cv.v[i][e]);
     int ne = 0;
-    for (int i = 0; i < n; ++i) ne += u[i] == tau;
+    for (int e = 0; e < n; ++e) ne += u[e] == tau;
     int te;
     int eq_pre = block_excl_scan(ne, &te, sm8) + eq_run;
     bool sel[4];
     int ns = 0;
-    for (int i = 0; i < 4; ++i) {
-      sel[i] = false;
-      if (i < n) {
-        if (u[i] > tau) sel[i] = true;
-        else if (u[i] == tau) sel[i] = (eq_pre++) < need;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sel[e] = false;
+      if (e < n) {
+        if (u[e] > tau) sel[e] = true;
+        else if (u[e] == tau) sel[e] = (eq_pre++) < need;
       }
-      ns += sel[i];
+      ns += sel[e];
     }
     int ts;
     int p = block_excl_scan(ns, &ts, sm8) + pos;
-    for (int i = 0; i < n; ++i)
-      if (sel[i]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (sel[e]) {
         if (p < a.K) {
-          out[p] = s + i;
-          if (phys) phys[p] = phys_row(a, ri.b, s + i);
+          out[p] = s + e;
+          if (phys) phys[p] = phys_row(a, ri.b, s + e);
         }
         ++p;
       }

@@ -343,6 +343,9 @@ WORKLOADS = {
     "b4_ctx1m": dict(batch=4, n_q=1, ctx=1 << 20, seed=3, bt_mode="permuted"),
     "b32x6_ctx256k_fp4": dict(batch=32, n_q=6, ctx=1 << 18, seed=4, bt_mode="permuted",
                               key_fmt="mxfp4", lat_fmt="nvfp4"),
+    # small cases for kernel profiles: each kernel's own inputs still exceed the 129 MB L2
+    "b4_ctx256k": dict(batch=4, n_q=1, ctx=1 << 18, seed=5, bt_mode="permuted"),
+    "b64_ctx16k": dict(batch=64, n_q=1, ctx=1 << 14, seed=6, bt_mode="permuted"),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
