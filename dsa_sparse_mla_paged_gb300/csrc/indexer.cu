@@ -116,7 +116,7 @@ struct IdxTc {
   float* scores;
   int64_t score_stride;
   int64_t key_page_stride;
-  int batch, n_q, max_pages, num_pages, stages, nacc, ncol, tmem_cols;
+  int batch, n_q, max_pages, num_pages, stages, nacc, group, ncol, tmem_cols;
   int* err;
 };
 
@@ -197,12 +197,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
                                                                    IdxTc a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = a.stages, NA = a.nacc;
+  const int S = a.stages, NA = a.nacc, G = a.group;
   const int qbytes = a.n_q * kIdxHeads * kIdxDim;
-  uint8_t* keys = smem;                                   // S x 16 KB
-  uint8_t* qbuf = keys + size_t(S) * kKeyTileBytes;       // 2 x qbytes
-  float* scl = reinterpret_cast<float*>(qbuf + 2 * qbytes);  // S x 128
-  uint64_t* bars = reinterpret_cast<uint64_t*>(scl + size_t(S) * kTileTok);
+  uint8_t* keys = smem;                                           // S x G x 16 KB
+  uint8_t* qbuf = keys + size_t(S) * G * kKeyTileBytes;           // 2 x qbytes
+  float* scl = reinterpret_cast<float*>(qbuf + 2 * qbytes);       // S x G x 128
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scl + size_t(S) * G * kTileTok);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
@@ -238,6 +238,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
     atomicOr(a.err, DSA_DEVERR_TIMEOUT);
   };
 
+  // Tiles are consumed in order; every G consecutive tiles of the CTA's range
+  // share one pipeline stage (one barrier round trip per G x 16.5 KB).
   if (t_begin < t_end) {
     if (warp == 0) {
       // ------------------------------------------------------------ producer
@@ -253,24 +255,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
       int base_np = (a.ctx_lens[base.b] + kPage - 1) / kPage;
       TilePages cur = tile_pages(a, base, base_np, t_end, lane);
       int cur_b = -1, nq = -1;
-      long long k = 0;
-      for (long long tc = t_begin; tc < t_end; tc += 32) {
-        // advance the base walk by 32 tiles and prefetch that chunk
+      int s = 0;          // ring stage
+      uint32_t ph = 0;    // its phase bit
+      bool ok = true;
+      for (long long tc = t_begin; tc < t_end && ok; tc += 32) {
         TileWalk nb = base;
         int nb_np = base_np;
         advance_walk(a, nb, nb_np, 32);
         const TilePages nxt = tile_pages(a, nb, nb_np, t_end, lane);
         const int n = int(t_end - tc < 32 ? t_end - tc : 32);
-        bool ok = true;
-        for (int i = 0; i < n; ++i, ++k) {
-          const int b = __shfl_sync(0xffffffffu, cur.b, i);
-          const int pg0 = __shfl_sync(0xffffffffu, cur.pg0, i);
-          const int pg1 = __shfl_sync(0xffffffffu, cur.pg1, i);
-          if (lane == 0 && ok) {
+        for (int i0 = 0; i0 < n; i0 += G) {
+          const int ng = min(G, n - i0);
+          uint32_t bytes = 0;
+          for (int g = 0; g < ng; ++g)
+            bytes += (__shfl_sync(0xffffffffu, cur.pg1, i0 + g) >= 0 ? 2u : 1u) * (kPage * kIdxDim + kPage * 4);
+          if (lane == 0) {
             if (*abort_flag) ok = false;
-            const int s = int(k % S);
-            const uint32_t ph = uint32_t(k / S) & 1u;
-            if (ok && b != cur_b) {
+            if (ok && !ptx::mbar_wait(empty + s, ph ^ 1u)) { fail(); ok = false; }
+            if (ok) ptx::mbar_arrive_expect_tx(full + s, bytes);
+          }
+          // all key copies of the stage first, then its query loads: a query
+          // slot is released by the MMA warp only once it has this stage in hand
+          for (int g = 0; g < ng; ++g) {
+            const int pg0 = __shfl_sync(0xffffffffu, cur.pg0, i0 + g);
+            const int pg1 = __shfl_sync(0xffffffffu, cur.pg1, i0 + g);
+            if (lane == 0 && ok) {
+              uint8_t* kdst = keys + (size_t(s) * G + g) * kKeyTileBytes;
+              float* sdst = scl + (size_t(s) * G + g) * kTileTok;
+              ptx::tma_load_3d(kdst, &kmap, full + s, 0, 0, pg0);
+              ptx::bulk_load(sdst, a.key_pool + size_t(pg0) * a.key_page_stride + kPage * kIdxDim, kPage * 4,
+                             full + s);
+              if (pg1 >= 0) {
+                ptx::tma_load_3d(kdst + kPage * kIdxDim, &kmap, full + s, 0, 0, pg1);
+                ptx::bulk_load(sdst + kPage, a.key_pool + size_t(pg1) * a.key_page_stride + kPage * kIdxDim,
+                               kPage * 4, full + s);
+              }
+            }
+          }
+          for (int g = 0; g < ng; ++g) {
+            const int b = __shfl_sync(0xffffffffu, cur.b, i0 + g);
+            if (lane == 0 && ok && b != cur_b) {
               ++nq;
               const int slot = nq & 1;
               if (!ptx::mbar_wait(qempty + slot, (uint32_t(nq >> 1) & 1u) ^ 1u)) { fail(); ok = false; }
@@ -280,23 +304,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
                 cur_b = b;
               }
             }
-            if (ok && !ptx::mbar_wait(empty + s, ph ^ 1u)) { fail(); ok = false; }
-            if (ok) {
-              const bool two = pg1 >= 0;
-              ptx::mbar_arrive_expect_tx(full + s, (two ? 2u : 1u) * (kPage * kIdxDim + kPage * 4));
-              ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes, &kmap, full + s, 0, 0, pg0);
-              ptx::bulk_load(scl + size_t(s) * kTileTok, a.key_pool + size_t(pg0) * a.key_page_stride + kPage * kIdxDim,
-                             kPage * 4, full + s);
-              if (two) {
-                ptx::tma_load_3d(keys + size_t(s) * kKeyTileBytes + kPage * kIdxDim, &kmap, full + s, 0, 0, pg1);
-                ptx::bulk_load(scl + size_t(s) * kTileTok + kPage,
-                               a.key_pool + size_t(pg1) * a.key_page_stride + kPage * kIdxDim, kPage * 4, full + s);
-              }
-            }
           }
-          __syncwarp();
+          if (++s == S) { s = 0; ph ^= 1u; }
+          ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+          if (!ok) break;
         }
-        if (!__shfl_sync(0xffffffffu, int(ok), 0)) break;
         base = nb;
         base_np = nb_np;
         cur = nxt;
@@ -308,30 +320,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
         TileWalk w;
         walk_start(a, t_begin, w);
         int cur_b = -1, nq = -1;
-        for (long long k = 0; w.t < t_end; ++k, walk_next(a, w)) {
-          if (*abort_flag) break;
-          const int s = int(k % S);
-          const uint32_t ph = uint32_t(k / S) & 1u;
-          const int acc = int(k % NA);
-          const uint32_t aph = uint32_t(k / NA) & 1u;
-          if (w.b != cur_b) {
-            if (cur_b >= 0) ptx::mma_commit(qempty + (nq & 1));
-            ++nq;
-            if (!ptx::mbar_wait(qfull + (nq & 1), uint32_t(nq >> 1) & 1u)) { fail(); break; }
-            cur_b = w.b;
+        int s = 0, acc = 0;
+        uint32_t ph = 0, aph = 0;
+        bool ok = true;
+        for (long long t0 = t_begin; t0 < t_end && ok; t0 += G) {
+          const int ng = int(t_end - t0 < G ? t_end - t0 : G);
+          if (*abort_flag || !ptx::mbar_wait(tempty + acc, aph ^ 1u) || !ptx::mbar_wait(full + s, ph)) {
+            fail();
+            break;
           }
-          if (!ptx::mbar_wait(tempty + acc, aph ^ 1u)) { fail(); break; }
-          if (!ptx::mbar_wait(full + s, ph)) { fail(); break; }
           ptx::tc_fence_after();
-          const uint32_t a_base = ptx::smem_u32(keys + size_t(s) * kKeyTileBytes);
-          const uint32_t b_base = ptx::smem_u32(qbuf + (nq & 1) * qbytes);
-          const uint32_t d = tmem + uint32_t(acc * a.ncol);
+          for (int g = 0; g < ng; ++g, walk_next(a, w)) {
+            if (w.b != cur_b) {
+              if (cur_b >= 0) ptx::mma_commit(qempty + (nq & 1));
+              ++nq;
+              if (!ptx::mbar_wait(qfull + (nq & 1), uint32_t(nq >> 1) & 1u)) { fail(); ok = false; break; }
+              ptx::tc_fence_after();
+              cur_b = w.b;
+            }
+            const uint32_t a_base = ptx::smem_u32(keys + (size_t(s) * G + g) * kKeyTileBytes);
+            const uint32_t b_base = ptx::smem_u32(qbuf + (nq & 1) * qbytes);
+            const uint32_t d = tmem + uint32_t((acc * G + g) * a.ncol);
 #pragma unroll
-          for (int kk = 0; kk < kIdxDim / 32; ++kk)
-            ptx::mma_f8f6f4(d, ptx::sdesc_sw128(a_base + kk * 32), ptx::sdesc_sw128(b_base + kk * 32), id,
-                            kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kIdxDim / 32; ++kk)
+              ptx::mma_f8f6f4(d, ptx::sdesc_sw128(a_base + kk * 32), ptx::sdesc_sw128(b_base + kk * 32), id,
+                              kk > 0 ? 1u : 0u);
+          }
+          if (!ok) break;
           ptx::mma_commit(empty + s);
           ptx::mma_commit(tfull + acc);
+          if (++s == S) { s = 0; ph ^= 1u; }
+          if (++acc == NA) { acc = 0; aph ^= 1u; }
         }
       }
     } else {
@@ -342,39 +361,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
       walk_start(a, t_begin, w);
       int cur_b = -1, ctx = 0;
       float wl[kMaxNQ];  // lane h holds w'_h of each query row of the current request
-      for (long long k = 0; w.t < t_end; ++k, walk_next(a, w)) {
+      int s = 0, acc = 0;
+      uint32_t aph = 0;
+      for (long long t0 = t_begin; t0 < t_end; t0 += G) {
+        const int ng = int(t_end - t0 < G ? t_end - t0 : G);
         if (*abort_flag) break;
-        const int s = int(k % S);
-        const int acc = int(k % NA);
-        const uint32_t aph = uint32_t(k / NA) & 1u;
-        if (w.b != cur_b) {
-          cur_b = w.b;
-          ctx = a.ctx_lens[w.b];
-#pragma unroll
-          for (int t = 0; t < kMaxNQ; ++t)
-            wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
-        }
         if (!ptx::mbar_wait(tfull + acc, aph)) { fail(); break; }
         ptx::tc_fence_after();
-        const float sc = scl[size_t(s) * kTileTok + rowt];
+        float sc[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) sc[g] = g < ng ? scl[(size_t(s) * G + g) * kTileTok + rowt] : 0.f;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty + s);
-        const int tok = w.j * kTileTok + rowt;
+#pragma unroll 1
+        for (int g = 0; g < ng; ++g, walk_next(a, w)) {
+          if (w.b != cur_b) {
+            cur_b = w.b;
+            ctx = a.ctx_lens[w.b];
 #pragma unroll
-        for (int t = 0; t < kMaxNQ; ++t) {
-          if (t >= a.n_q) break;
-          float v[32];
-          ptx::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(acc * a.ncol + t * 32), v);
-          float sum = 0.f;
+            for (int t = 0; t < kMaxNQ; ++t)
+              wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
+          }
+          const float scale = g == 0 ? sc[0] : g == 1 ? sc[1] : g == 2 ? sc[2] : sc[3];
+          const int tok = w.j * kTileTok + rowt;
 #pragma unroll
-          for (int h = 0; h < kIdxHeads; ++h)
-            sum = fmaf(__shfl_sync(0xffffffffu, wl[t], h), fmaxf(sc * v[h], 0.f), sum);
-          const int Lt = ctx - a.n_q + t + 1;
-          if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + t) * a.score_stride + tok] = sum;
+          for (int t = 0; t < kMaxNQ; ++t) {
+            if (t >= a.n_q) break;
+            float v[32];
+            ptx::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t((acc * G + g) * a.ncol + t * 32), v);
+            float sum = 0.f;
+#pragma unroll
+            for (int h = 0; h < kIdxHeads; ++h)
+              sum = fmaf(__shfl_sync(0xffffffffu, wl[t], h), fmaxf(scale * v[h], 0.f), sum);
+            const int Lt = ctx - a.n_q + t + 1;
+            if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + t) * a.score_stride + tok] = sum;
+          }
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tempty + acc);
+        if (++s == S) s = 0;
+        if (++acc == NA) { acc = 0; aph ^= 1u; }
       }
     }
   }
@@ -458,14 +485,18 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   a.max_pages = p.max_pages_per_req;
   a.num_pages = p.num_pages;
   a.ncol = p.n_q * kIdxHeads;
-  a.nacc = a.ncol <= 64 ? 4 : (a.ncol <= 128 ? 4 : 2);
+  // tiles per stage: as many as fit 256 accumulator columns (at most 4)
+  a.group = std::max(1, std::min(4, 256 / a.ncol));
+  const int slot_cols = a.group * a.ncol;
+  a.nacc = std::max(1, std::min(4, 512 / slot_cols));
   int cols = 32;
-  while (cols < a.nacc * a.ncol) cols <<= 1;
+  while (cols < a.nacc * slot_cols) cols <<= 1;
   a.tmem_cols = cols;
-  a.stages = p.n_q <= 2 ? 8 : 6;
+  const size_t stage_bytes = size_t(a.group) * (kKeyTileBytes + kScaleTileBytes);
+  const size_t fixed = 1024 + 2 * size_t(p.n_q) * kIdxHeads * kIdxDim + 256;
+  a.stages = int(std::min<size_t>(8, (227 * 1024 - fixed) / stage_bytes));
   a.err = err;
-  const size_t smem = 1024 + size_t(a.stages) * (kKeyTileBytes + kScaleTileBytes) +
-                      2 * size_t(p.n_q) * kIdxHeads * kIdxDim + (2 * a.stages + 2 * a.nacc + 4) * 8 + 16;
+  const size_t smem = fixed + size_t(a.stages) * stage_bytes;
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   // enough tiles for every SM is the common case; with fewer, one CTA per tile
