@@ -21,11 +21,10 @@ constexpr int kLatRowFp8 = kDQK;                         // 576
 constexpr int kMaxNQ = 8;
 constexpr int kMaxTopK = 2048;
 
-// top-k: a row of scores is cut into chunks of this many tokens, one CTA each.
+// top-k: a row of scores is cut into chunks of this many tokens, one CTA each;
+// each row keeps at most kCandCap candidates for its exact selection.
 constexpr int kTopkChunk = 4096;
-constexpr int kHist0Bins = 2048;  // bits 31..21 of the order-preserving key
-constexpr int kHist1Bins = 2048;  // bits 20..10
-constexpr int kHist2Bins = 1024;  // bits 9..0
+constexpr int kCandCap = 8192;
 constexpr int kRowState = 16;     // int32 words of per-row selection state
 
 // sparse attention: the K selected slots of a row are cut into splits of this
@@ -40,11 +39,9 @@ struct WsLayout {
   size_t q8;        // uint8 [rows][32][128] quantised indexer query
   size_t wq;        // float [rows][32] folded head weights
   size_t tiles;     // int32 [batch] inclusive prefix of 128-token tiles per request
-  size_t hist;      // int32 [rows][2048 + 2048 + 1024]
   size_t state;     // int32 [rows][kRowState]
-  size_t ticket;    // int32 [rows][4] last-CTA tickets (zero between calls)
-  size_t chunkcnt;  // int32 [rows][max_chunks][2]
-  size_t chunkoff;  // int32 [rows][max_chunks][2]
+  size_t chunkinfo; // int32 [rows][max_chunks][2] (offset, count) of each chunk's candidates
+  size_t cand;      // uint64 [rows][kCandCap] top-k candidates (key << 32 | token)
   size_t opart;     // float [rows][splits][96][512]
   size_t lpart;     // float [rows][splits][96]
   size_t topk;      // int32 [rows][topk] (dsa_decode without topk_idx_out)
@@ -69,11 +66,9 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.q8 = o; o = align256(o + size_t(L.rows) * kIdxHeads * kIdxDim);
   L.wq = o; o = align256(o + size_t(L.rows) * kIdxHeads * 4);
   L.tiles = o; o = align256(o + size_t(p.batch) * 4);
-  L.hist = o; o = align256(o + size_t(L.rows) * (kHist0Bins + kHist1Bins + kHist2Bins) * 4);
   L.state = o; o = align256(o + size_t(L.rows) * kRowState * 4);
-  L.ticket = o; o = align256(o + size_t(L.rows) * 4 * 4);
-  L.chunkcnt = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
-  L.chunkoff = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
+  L.chunkinfo = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
+  L.cand = o; o = align256(o + size_t(L.rows) * kCandCap * 8);
   L.opart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * kDNope * 4);
   L.lpart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * 4);
   L.topk = o; o = align256(o + size_t(L.rows) * p.topk * 4);

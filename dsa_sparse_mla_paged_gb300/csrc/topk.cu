@@ -5,25 +5,31 @@
 // descending, token index ascending) and writes the kept tokens in ascending
 // index order.
 //
-// Method: radix select on the order-preserving 32-bit image of each score
-// (11 + 11 + 10 bits), split over the context in chunks of kTopkChunk tokens.
-//   pass 0..2  every chunk CTA histograms its tokens' next digit (among the
-//              tokens that still match the prefix) into smem, then adds the
-//              non-zero bins to the row's global histogram; the last CTA of the
-//              row to finish (atomic ticket, no waiting) walks the histogram and
-//              fixes the next digit of the threshold tau.
-//   count      every chunk counts tokens above tau and equal to tau; the last
-//              CTA turns the counts into per-chunk output offsets.
-//   write      every chunk writes its selected tokens in index order (block
-//              scans), ties at tau taken lowest index first.
-// Counts do not depend on the order of atomics, so the result is deterministic.
+// Scores are compared through an order-preserving 32-bit key (larger score ->
+// larger key; -0 and +0 share one key). Three kernels:
+//   sample  one CTA per row: from <= 8,192 evenly spaced scores, pick a key g
+//           that about 2K tokens of the row are expected to reach
+//   filter  one CTA per 4,096-token chunk: compact the chunk's tokens with
+//           key >= g, in index order, into the row's candidate buffer (a
+//           region reserved with one atomic; its place recorded per chunk)
+//   select  one CTA per row: gather the candidates chunk by chunk (so they are
+//           in index order again), radix-select the exact K-th largest key tau
+//           among them and write the winners in order, ties at tau lowest
+//           index first.
+// Whenever at least K tokens reach g, the candidates contain every token with
+// key >= tau, so the selection is exact. Otherwise (g too high, or more
+// candidates than the buffer holds, e.g. a row of equal scores) the select CTA
+// runs an exact radix select over the whole row by itself. No CTA ever waits
+// on another; the result does not depend on the order of the atomics.
 #include "dsa_internal.cuh"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kFiltThreads = 256;
+constexpr int kSelThreads = 1024;
+constexpr int kSampleMax = 8192;
 
 struct TopkArgs {
   const float* scores;
@@ -31,11 +37,9 @@ struct TopkArgs {
   const int32_t* ctx_lens;
   const int32_t* block_table;
   int n_q, cap, K, max_pages, num_pages, max_chunks;
-  int* hist;      // [rows][5120]
-  int* state;     // [rows][kRowState]
-  int* ticket;    // [rows][4]
-  int* chunkcnt;  // [rows][max_chunks][2]
-  int* chunkoff;  // [rows][max_chunks][2]
+  int* state;      // [rows][kRowState]: 0 g, 1 cursor, 2 overflow
+  int* chunkinfo;  // [rows][max_chunks][2]: (offset, count) in the candidate buffer
+  uint64_t* cand;  // [rows][kCandCap]: key << 32 | token
   int* err;
   int32_t* topk_idx;
   int32_t* phys_rows;
@@ -47,8 +51,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block scan (256 threads) of one int per thread; *total gets the sum.
-__device__ __forceinline__ int block_excl_scan(int v, int* total, int* sm8) {
+// Exclusive block scan of one int per thread (NT threads); *total gets the sum.
+template <int NT>
+__device__ __forceinline__ int block_excl_scan(int v, int* total, int* smw) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -56,195 +62,37 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int* sm8) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) sm8[warp] = x;
+  if (lane == 31) smw[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = lane < 8 ? sm8[lane] : 0;
+    int s = lane < NW ? smw[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
+    for (int o = 1; o < NW; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    if (lane < 8) sm8[lane] = s;
+    if (lane < NW) smw[lane] = s;
   }
   __syncthreads();
-  const int pre = (warp ? sm8[warp - 1] : 0) + x - v;
-  *total = sm8[7];
+  const int pre = (warp ? smw[warp - 1] : 0) + x - v;
+  *total = smw[NW - 1];
   __syncthreads();
   return pre;
 }
 
-// Find bin d (scanning from the top) holding the k-th largest (1-based) entry.
-// Writes d and the count strictly above it to out[0], out[1] (shared memory).
-__device__ void resolve_bin(const int* hist, int nbins, int k, int* out, int* sm8) {
-  const int per = nbins / kThreads;
-  const int hi = nbins - 1 - threadIdx.x * per;
-  int s = 0;
-  for (int j = 0; j < per; ++j) s += __ldcg(hist + hi - j);
-  int tot;
-  const int pre = block_excl_scan(s, &tot, sm8);
-  if (pre < k && k <= pre + s) {
-    int c = pre;
-    for (int j = 0; j < per; ++j) {
-      const int h = __ldcg(hist + hi - j);
-      if (k <= c + h) {
-        out[0] = hi - j;
-        out[1] = c;
-        break;
-      }
-      c += h;
-    }
-  }
-  __syncthreads();
-}
-
-struct RowInfo {
-  int r, b, L, nch, c;
+struct Row {
+  int r, b, L;
 };
 
-__device__ __forceinline__ RowInfo row_info(const TopkArgs& a) {
-  RowInfo ri;
-  ri.r = blockIdx.y;
-  ri.b = ri.r / a.n_q;
-  const int t = ri.r - ri.b * a.n_q;
-  const int ctx = a.ctx_lens[ri.b];
-  ri.L = (ctx < a.n_q || ctx > a.cap) ? -1 : ctx - a.n_q + t + 1;
-  if (ri.L > a.stride) ri.L = -1;
-  ri.nch = ri.L > 0 ? (ri.L + kTopkChunk - 1) / kTopkChunk : 0;
-  ri.c = blockIdx.x;
-  return ri;
-}
-
-// The chunk's scores for this thread: 4 float4 loads (all issued before any
-// use), element i*1024 + 4*tid + e of the chunk; `n[i]` valid lanes per load.
-struct ChunkVals {
-  float v[4][4];
-  int n[4];
-};
-
-__device__ __forceinline__ void load_chunk(const float* row, int s0, int s1, ChunkVals& c) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int s = s0 + i * kThreads * 4 + threadIdx.x * 4;
-    c.n[i] = min(4, max(0, s1 - s));
-    if (c.n[i] == 4) {
-      const float4 f = __ldcg(reinterpret_cast<const float4*>(row + s));
-      c.v[i][0] = f.x; c.v[i][1] = f.y; c.v[i][2] = f.z; c.v[i][3] = f.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c.v[i][e] = e < c.n[i] ? row[s + e] : 0.f;
-    }
-  }
-}
-
-// Histogram pass `pass` (0, 1, 2) of one chunk.
-template <int PASS>
-__global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
-  constexpr int NB = PASS == 2 ? kHist2Bins : 2048;
-  __shared__ int sh[NB];
-  __shared__ int sm8[8];
-  __shared__ int res[2];
-  __shared__ int last;
-  const RowInfo ri = row_info(a);
-  if (ri.L <= a.K || ri.c >= ri.nch) return;
-  int* st = a.state + size_t(ri.r) * kRowState;
-  uint32_t prefix = 0;
-  if (PASS == 1) prefix = uint32_t(st[0]);
-  if (PASS == 2) prefix = (uint32_t(st[0]) << 11) | uint32_t(st[2]);
-  for (int i = threadIdx.x; i < NB; i += kThreads) sh[i] = 0;
-  __syncthreads();
-  const float* row = a.scores + size_t(ri.r) * a.stride;
-  const int s0 = ri.c * kTopkChunk;
-  const int s1 = min(ri.L, s0 + kTopkChunk);
-  ChunkVals cv;
-  load_chunk(row, s0, s1, cv);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (e >= cv.n[i]) break;
-      const uint32_t u = order_key(cv.v[i][e]);
-      if (PASS == 0) atomicAdd(&sh[u >> 21], 1);
-      if (PASS == 1 && (u >> 21) == prefix) atomicAdd(&sh[(u >> 10) & 2047u], 1);
-      if (PASS == 2 && (u >> 10) == prefix) atomicAdd(&sh[u & 1023u], 1);
-    }
-  __syncthreads();
-  int* gh = a.hist + size_t(ri.r) * (kHist0Bins + kHist1Bins + kHist2Bins) +
-            (PASS == 0 ? 0 : PASS == 1 ? kHist0Bins : kHist0Bins + kHist1Bins);
-  for (int i = threadIdx.x; i < NB; i += kThreads)
-    if (sh[i]) atomicAdd(gh + i, sh[i]);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(a.ticket + ri.r * 4 + PASS, 1) == ri.nch - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  const int k = PASS == 0 ? a.K : PASS == 1 ? st[1] : st[3];
-  resolve_bin(gh, NB, k, res, sm8);
-  if (threadIdx.x == 0) {
-    if (PASS == 0) { st[0] = res[0]; st[1] = k - res[1]; }
-    if (PASS == 1) { st[2] = res[0]; st[3] = k - res[1]; }
-    if (PASS == 2) {
-      st[4] = int((prefix << 10) | uint32_t(res[0]));  // tau (order key)
-      st[5] = k - res[1];                               // ties at tau to take
-    }
-    a.ticket[ri.r * 4 + PASS] = 0;
-  }
-}
-
-// Count tokens above / equal to tau per chunk; the last CTA scans the counts.
-__global__ void __launch_bounds__(kThreads) topk_count_kernel(TopkArgs a) {
-  __shared__ int sm8[8];
-  __shared__ int last;
-  const RowInfo ri = row_info(a);
-  if (ri.L <= a.K || ri.c >= ri.nch) return;
-  int* st = a.state + size_t(ri.r) * kRowState;
-  const uint32_t tau = uint32_t(st[4]);
-  const float* row = a.scores + size_t(ri.r) * a.stride;
-  const int s0 = ri.c * kTopkChunk;
-  const int s1 = min(ri.L, s0 + kTopkChunk);
-  int gt = 0, eq = 0;
-  ChunkVals cv;
-  load_chunk(row, s0, s1, cv);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (e >= cv.n[i]) break;
-      const uint32_t u = order_key(cv.v[i][e]);
-      gt += u > tau;
-      eq += u == tau;
-    }
-  int tg, te;
-  block_excl_scan(gt, &tg, sm8);
-  block_excl_scan(eq, &te, sm8);
-  int* cc = a.chunkcnt + (size_t(ri.r) * a.max_chunks + ri.c) * 2;
-  if (threadIdx.x == 0) { cc[0] = tg; cc[1] = te; }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(a.ticket + ri.r * 4 + 3, 1) == ri.nch - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  const int need = st[5];
-  int run_gt = 0, run_eq = 0;
-  const int* ccr = a.chunkcnt + size_t(ri.r) * a.max_chunks * 2;
-  int* cor = a.chunkoff + size_t(ri.r) * a.max_chunks * 2;
-  for (int c0 = 0; c0 < ri.nch; c0 += kThreads) {
-    const int c = c0 + threadIdx.x;
-    const int g = c < ri.nch ? __ldcg(ccr + 2 * c) : 0;
-    const int e = c < ri.nch ? __ldcg(ccr + 2 * c + 1) : 0;
-    int sg, se;
-    const int pg = block_excl_scan(g, &sg, sm8) + run_gt;
-    const int pe = block_excl_scan(e, &se, sm8) + run_eq;
-    if (c < ri.nch) {
-      cor[2 * c] = pg + min(pe, need);  // selected tokens before chunk c
-      cor[2 * c + 1] = pe;              // ties before chunk c
-    }
-    run_gt += sg;
-    run_eq += se;
-  }
-  if (threadIdx.x == 0) a.ticket[ri.r * 4 + 3] = 0;
+__device__ __forceinline__ Row row_of(const TopkArgs& a, int r) {
+  Row w;
+  w.r = r;
+  w.b = r / a.n_q;
+  const int t = r - w.b * a.n_q;
+  const int ctx = a.ctx_lens[w.b];
+  w.L = (ctx < a.n_q || ctx > a.cap) ? -1 : ctx - a.n_q + t + 1;
+  if (w.L > a.stride) w.L = -1;
+  return w;
 }
 
 __device__ __forceinline__ int phys_row(const TopkArgs& a, int b, int s) {
@@ -256,70 +104,298 @@ __device__ __forceinline__ int phys_row(const TopkArgs& a, int b, int s) {
   return pg * kPage + (s % kPage);
 }
 
-// Write the selected tokens of one chunk in index order.
-__global__ void __launch_bounds__(kThreads) topk_write_kernel(TopkArgs a) {
-  __shared__ int sm8[8];
-  const RowInfo ri = row_info(a);
-  int32_t* out = a.topk_idx + size_t(ri.r) * a.K;
-  int32_t* phys = a.phys_rows ? a.phys_rows + size_t(ri.r) * a.K : nullptr;
-  if (ri.L <= a.K) {
+// Radix select over n keys in shared memory (NT threads, 8 bits per pass): the
+// k-th largest key (1-based) and how many keys equal to it are among the k largest.
+template <int NT>
+__device__ void smem_kth_key(const uint32_t* keys, int n, int k, int* hist, uint32_t* out_key, int* out_need) {
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_k;
+  if (threadIdx.x == 0) { s_prefix = 0; s_k = k; }
+  __syncthreads();
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();
+    const uint32_t pre = s_prefix;
+    const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (32 - 8 * pass));
+    for (int i = threadIdx.x; i < n; i += NT) {
+      const uint32_t u = keys[i];
+      if ((u & hmask) == pre) atomicAdd(&hist[(u >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // walk the 256 bins from the top: lane l owns bins 255-8l .. 248-8l
+      const int lane = threadIdx.x;
+      int c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { c[j] = hist[255 - lane * 8 - j]; sum += c[j]; }
+      int x = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const int before = x - sum;
+      const int kk = s_k;
+      if (before < kk && kk <= x) {
+        int cum = before;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (kk <= cum + c[j]) {
+            s_prefix = pre | (uint32_t(255 - lane * 8 - j) << shift);
+            s_k = kk - cum;
+            break;
+          }
+          cum += c[j];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  *out_key = s_prefix;
+  *out_need = s_k;
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- sample
+__global__ void __launch_bounds__(512) topk_sample_kernel(TopkArgs a) {
+  __shared__ uint32_t keys[kSampleMax];
+  __shared__ int hist[256];
+  const Row w = row_of(a, blockIdx.x);
+  int* st = a.state + size_t(w.r) * kRowState;
+  if (w.L <= a.K) return;
+  const int ns = min(w.L, kSampleMax);
+  const float* row = a.scores + size_t(w.r) * a.stride;
+  for (int i = threadIdx.x; i < ns; i += 512) keys[i] = order_key(__ldcg(row + int((int64_t(i) * w.L) / ns)));
+  __syncthreads();
+  // the r-th largest sample: about 2K tokens of the row are expected at or above it
+  const int r = int((int64_t(2) * a.K * ns + w.L - 1) / w.L);
+  uint32_t g = 0u;
+  if (r < ns) {
+    int need;
+    smem_kth_key<512>(keys, ns, r, hist, &g, &need);
+  }
+  if (threadIdx.x == 0) {
+    st[0] = int(g);
+    st[1] = 0;  // candidate cursor
+    st[2] = 0;  // overflow
+  }
+}
+
+// ---------------------------------------------------------------- filter
+__global__ void __launch_bounds__(kFiltThreads) topk_filter_kernel(TopkArgs a) {
+  __shared__ int smw[8];
+  __shared__ int s_base;
+  const Row w = row_of(a, blockIdx.y);
+  if (w.L <= a.K) return;
+  const int nch = (w.L + kTopkChunk - 1) / kTopkChunk;
+  const int c = blockIdx.x;
+  if (c >= nch) return;
+  int* st = a.state + size_t(w.r) * kRowState;
+  const uint32_t g = uint32_t(st[0]);
+  const float* row = a.scores + size_t(w.r) * a.stride;
+  const int s0 = c * kTopkChunk;
+  const int s1 = min(w.L, s0 + kTopkChunk);
+  // element i*1024 + 4*tid + e of the chunk; all loads issued before any use
+  float v[4][4];
+  int n[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = s0 + i * kFiltThreads * 4 + threadIdx.x * 4;
+    n[i] = min(4, max(0, s1 - s));
+    if (n[i] == 4) {
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(row + s));
+      v[i][0] = f.x; v[i][1] = f.y; v[i][2] = f.z; v[i][3] = f.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[i][e] = e < n[i] ? row[s + e] : 0.f;
+    }
+  }
+  int pre[4], run = 0;
+  uint32_t keep[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int m = 0;
+    keep[i] = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < n[i] && order_key(v[i][e]) >= g) { keep[i] |= 1u << e; ++m; }
+    int tot;
+    pre[i] = block_excl_scan<kFiltThreads>(m, &tot, smw) + run;
+    run += tot;
+  }
+  if (threadIdx.x == 0) {
+    const int base = atomicAdd(st + 1, run);
+    if (base + run > kCandCap) atomicOr(st + 2, 1);
+    s_base = base;
+    int* ci = a.chunkinfo + (size_t(w.r) * a.max_chunks + c) * 2;
+    ci[0] = base;
+    ci[1] = run;
+  }
+  __syncthreads();
+  const int base = s_base;
+  if (base + run > kCandCap) return;
+  uint64_t* out = a.cand + size_t(w.r) * kCandCap + base;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = s0 + i * kFiltThreads * 4 + threadIdx.x * 4;
+    int p = pre[i];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (keep[i] & (1u << e)) out[p++] = (uint64_t(order_key(v[i][e])) << 32) | uint32_t(s + e);
+  }
+}
+
+// ---------------------------------------------------------------- select
+// Exact radix select over the whole row by this CTA alone (the rare path):
+// 11 + 11 + 10 key bits, then an ordered write in tiles of kSelThreads tokens.
+__device__ void select_whole_row(const TopkArgs& a, const Row& w, int* hist, int* smw, int32_t* out,
+                                 int32_t* phys) {
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_k;
+  const float* row = a.scores + size_t(w.r) * a.stride;
+  if (threadIdx.x == 0) { s_prefix = 0; s_k = a.K; }
+  __syncthreads();
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+    const int width = pass == 2 ? 10 : 11;
+    const int nb = 1 << width;
+    for (int i = threadIdx.x; i < nb; i += kSelThreads) hist[i] = 0;
+    __syncthreads();
+    const uint32_t pre = s_prefix;
+    const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (sh + width));
+    for (int s = threadIdx.x; s < w.L; s += kSelThreads) {
+      const uint32_t u = order_key(__ldcg(row + s));
+      if ((u & hmask) == pre) atomicAdd(&hist[(u >> sh) & uint32_t(nb - 1)], 1);
+    }
+    __syncthreads();
+    // bins from the top; thread t owns bins nb-1-t*per .. nb-per-t*per
+    const int per = nb / kSelThreads;
+    int cnt = 0;
+    for (int j = 0; j < per; ++j) cnt += hist[nb - 1 - threadIdx.x * per - j];
+    int tot;
+    const int before = block_excl_scan<kSelThreads>(cnt, &tot, smw);
+    const int kk = s_k;
+    __syncthreads();
+    if (before < kk && kk <= before + cnt) {
+      int cum = before;
+      for (int j = 0; j < per; ++j) {
+        const int bin = nb - 1 - threadIdx.x * per - j;
+        if (kk <= cum + hist[bin]) {
+          s_prefix = pre | (uint32_t(bin) << sh);
+          s_k = kk - cum;
+          break;
+        }
+        cum += hist[bin];
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t tau = s_prefix;
+  const int need = s_k;
+  int pos = 0, eq_run = 0;
+  for (int base = 0; base < w.L; base += kSelThreads) {
+    const int s = base + threadIdx.x;
+    const uint32_t u = s < w.L ? order_key(__ldcg(row + s)) : 0u;
+    const int is_eq = (s < w.L && u == tau) ? 1 : 0;
+    int te;
+    const int eq_pre = block_excl_scan<kSelThreads>(is_eq, &te, smw) + eq_run;
+    const int sel = (s < w.L && (u > tau || (is_eq && eq_pre < need))) ? 1 : 0;
+    int ts;
+    const int p = block_excl_scan<kSelThreads>(sel, &ts, smw) + pos;
+    if (sel && p < a.K) {
+      out[p] = s;
+      if (phys) phys[p] = phys_row(a, w.b, s);
+    }
+    pos += ts;
+    eq_run += te;
+  }
+}
+
+constexpr size_t kSelSmem = size_t(kCandCap) * 8 + 2048 * 4;
+
+__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(TopkArgs a) {
+  extern __shared__ uint32_t sel_smem[];
+  uint32_t* ckey = sel_smem;                                  // [kCandCap]
+  int* cidx = reinterpret_cast<int*>(sel_smem + kCandCap);    // [kCandCap]
+  int* hist = cidx + kCandCap;                                // [2048]
+  __shared__ int smw[32];
+  __shared__ int s_total;
+  const Row w = row_of(a, blockIdx.x);
+  int32_t* out = a.topk_idx + size_t(w.r) * a.K;
+  int32_t* phys = a.phys_rows ? a.phys_rows + size_t(w.r) * a.K : nullptr;
+  if (w.L <= a.K) {
     // every visible token is kept (an invalid row keeps none)
-    if (ri.c != 0) return;
-    if (ri.L < 0 && threadIdx.x == 0) atomicOr(a.err, DSA_DEVERR_CTX);
-    for (int i = threadIdx.x; i < a.K; i += kThreads) {
-      const bool keep = i < ri.L;
+    if (w.L < 0 && threadIdx.x == 0) atomicOr(a.err, DSA_DEVERR_CTX);
+    for (int i = threadIdx.x; i < a.K; i += kSelThreads) {
+      const bool keep = i < w.L;
       out[i] = keep ? i : -1;
-      if (phys) phys[i] = keep ? phys_row(a, ri.b, i) : -1;
+      if (phys) phys[i] = keep ? phys_row(a, w.b, i) : -1;
     }
     return;
   }
-  if (ri.c >= ri.nch) return;
-  const int* st = a.state + size_t(ri.r) * kRowState;
-  const uint32_t tau = uint32_t(st[4]);
-  const int need = st[5];
-  const int* co = a.chunkoff + (size_t(ri.r) * a.max_chunks + ri.c) * 2;
-  int pos = co[0];
-  int eq_run = co[1];
-  const float* row = a.scores + size_t(ri.r) * a.stride;
-  const int s0 = ri.c * kTopkChunk;
-  const int s1 = min(ri.L, s0 + kTopkChunk);
-  ChunkVals cv;
-  load_chunk(row, s0, s1, cv);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int s = s0 + i * kThreads * 4 + threadIdx.x * 4;
-    const int n = cv.n[i];
-    uint32_t u[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) u[e] = order_key(cv.v[i][e]);
-    int ne = 0;
-    for (int e = 0; e < n; ++e) ne += u[e] == tau;
-    int te;
-    int eq_pre = block_excl_scan(ne, &te, sm8) + eq_run;
-    bool sel[4];
-    int ns = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sel[e] = false;
-      if (e < n) {
-        if (u[e] > tau) sel[e] = true;
-        else if (u[e] == tau) sel[e] = (eq_pre++) < need;
+  const int* st = a.state + size_t(w.r) * kRowState;
+  const int total = st[1];
+  if (st[2] != 0 || total < a.K) {
+    select_whole_row(a, w, hist, smw, out, phys);
+    return;
+  }
+  // gather the candidates chunk by chunk: index order again
+  const int nch = (w.L + kTopkChunk - 1) / kTopkChunk;
+  const int* ci = a.chunkinfo + size_t(w.r) * a.max_chunks * 2;
+  const uint64_t* cand = a.cand + size_t(w.r) * kCandCap;
+  if (threadIdx.x == 0) s_total = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < nch; c0 += kSelThreads) {
+    const int c = c0 + threadIdx.x;
+    const int cnt = c < nch ? ci[2 * c + 1] : 0;
+    const int run0 = s_total;
+    int tot;
+    const int pre = block_excl_scan<kSelThreads>(cnt, &tot, smw) + run0;
+    if (c < nch) {
+      const int src = ci[2 * c];
+      for (int j = 0; j < cnt; ++j) {
+        const uint64_t v = cand[src + j];
+        ckey[pre + j] = uint32_t(v >> 32);
+        cidx[pre + j] = int(uint32_t(v));
       }
-      ns += sel[e];
     }
-    int ts;
-    int p = block_excl_scan(ns, &ts, sm8) + pos;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (sel[e]) {
-        if (p < a.K) {
-          out[p] = s + e;
-          if (phys) phys[p] = phys_row(a, ri.b, s + e);
-        }
-        ++p;
+    __syncthreads();
+    if (threadIdx.x == 0) s_total = run0 + tot;
+    __syncthreads();
+  }
+  uint32_t tau;
+  int need;
+  smem_kth_key<kSelThreads>(ckey, total, a.K, hist, &tau, &need);
+  // ordered write: thread t takes a contiguous run of the candidates
+  const int per = (total + kSelThreads - 1) / kSelThreads;
+  const int i0 = min(total, int(threadIdx.x) * per), i1 = min(total, i0 + per);
+  int ne = 0;
+  for (int i = i0; i < i1; ++i) ne += ckey[i] == tau;
+  int te;
+  int eq = block_excl_scan<kSelThreads>(ne, &te, smw);
+  int ns = 0;
+  for (int i = i0, e = eq; i < i1; ++i) {
+    const uint32_t u = ckey[i];
+    if (u > tau) ++ns;
+    else if (u == tau && e++ < need) ++ns;
+  }
+  int ts;
+  int p = block_excl_scan<kSelThreads>(ns, &ts, smw);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t u = ckey[i];
+    bool sel = false;
+    if (u > tau) sel = true;
+    else if (u == tau) sel = eq++ < need;
+    if (sel) {
+      if (p < a.K) {
+        out[p] = cidx[i];
+        if (phys) phys[p] = phys_row(a, w.b, cidx[i]);
       }
-    pos += ts;
-    eq_run += te;
+      ++p;
+    }
   }
 }
 
@@ -339,23 +415,17 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   a.max_pages = p.max_pages_per_req;
   a.num_pages = p.num_pages;
   a.max_chunks = L.max_chunks;
-  a.hist = reinterpret_cast<int*>(ws + L.hist);
   a.state = reinterpret_cast<int*>(ws + L.state);
-  a.ticket = reinterpret_cast<int*>(ws + L.ticket);
-  a.chunkcnt = reinterpret_cast<int*>(ws + L.chunkcnt);
-  a.chunkoff = reinterpret_cast<int*>(ws + L.chunkoff);
+  a.chunkinfo = reinterpret_cast<int*>(ws + L.chunkinfo);
+  a.cand = reinterpret_cast<uint64_t*>(ws + L.cand);
   a.err = reinterpret_cast<int*>(ws + L.err);
   a.topk_idx = topk_idx;
   a.phys_rows = phys_rows;
-  // histograms and tickets start at zero for every call
-  cudaError_t e = cudaMemsetAsync(ws + L.hist, 0, L.ticket + size_t(L.rows) * 16 - L.hist, st);
+  topk_sample_kernel<<<L.rows, 512, 0, st>>>(a);
+  topk_filter_kernel<<<dim3(L.max_chunks, L.rows), kFiltThreads, 0, st>>>(a);
+  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSelSmem));
   if (e != cudaSuccess) return e;
-  dim3 grid(L.max_chunks, L.rows);
-  topk_hist_kernel<0><<<grid, kThreads, 0, st>>>(a);
-  topk_hist_kernel<1><<<grid, kThreads, 0, st>>>(a);
-  topk_hist_kernel<2><<<grid, kThreads, 0, st>>>(a);
-  topk_count_kernel<<<grid, kThreads, 0, st>>>(a);
-  topk_write_kernel<<<grid, kThreads, 0, st>>>(a);
+  topk_select_kernel<<<L.rows, kSelThreads, kSelSmem, st>>>(a);
   return cudaGetLastError();
 }
 

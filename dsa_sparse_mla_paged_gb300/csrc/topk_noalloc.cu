@@ -5,8 +5,8 @@
 // device byte, code running in a real-time decode loop that must not call
 // into the allocator (cudaMalloc can synchronise the device), or a C caller
 // that is handed only input and output pointers. For them this entry point
-// keeps the top-k scratch (histograms, per-row selection state, per-chunk
-// counts and offsets) in one file-scope device array that every GPU loading
+// keeps the top-k scratch (per-row selection state, per-chunk candidate
+// offsets, the candidate buffer) in one file-scope device array that every GPU loading
 // the library holds until the process exits.
 #include <mutex>
 
@@ -20,12 +20,11 @@ constexpr int kNoAllocMaxCtx = 1 << 20;             // max_pages_per_req * page_
 constexpr int kNoAllocMaxChunks = kNoAllocMaxCtx / kTopkChunk;
 constexpr size_t kNoAllocBytes =
     256 +                                                                        // error word
-    size_t(kNoAllocMaxRows) * (kHist0Bins + kHist1Bins + kHist2Bins) * 4 +       // histograms
     size_t(kNoAllocMaxRows) * kRowState * 4 +                                    // row state
-    size_t(kNoAllocMaxRows) * 4 * 4 +                                            // tickets
-    2 * size_t(kNoAllocMaxRows) * kNoAllocMaxChunks * 2 * 4;                     // chunk counts, offsets
+    size_t(kNoAllocMaxRows) * kNoAllocMaxChunks * 2 * 4 +                        // chunk (offset, count)
+    size_t(kNoAllocMaxRows) * kCandCap * 8;                                      // candidates
 
-// The scratch itself (about 1.6 MB). Only host code below takes its address.
+// The scratch itself (about 4.3 MB). Only host code below takes its address.
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
@@ -49,8 +48,8 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-// The top-k regions of a workspace, packed into the static array (hist, state
-// and ticket stay contiguous: the launch clears them with one memset).
+// The top-k regions of a workspace, packed into the static array. Every call
+// rewrites the per-row state before anything reads it, so nothing needs clearing.
 WsLayout noalloc_layout(const dsa_params_t& p) {
   WsLayout L{};
   L.rows = p.batch * p.n_q;
@@ -59,11 +58,9 @@ WsLayout noalloc_layout(const dsa_params_t& p) {
   L.splits = 1;
   size_t o = 0;
   L.err = o; o += 256;
-  L.hist = o; o += size_t(L.rows) * (kHist0Bins + kHist1Bins + kHist2Bins) * 4;
   L.state = o; o += size_t(L.rows) * kRowState * 4;
-  L.ticket = o; o += size_t(L.rows) * 4 * 4;
-  L.chunkcnt = o; o += size_t(L.rows) * L.max_chunks * 2 * 4;
-  L.chunkoff = o; o += size_t(L.rows) * L.max_chunks * 2 * 4;
+  L.chunkinfo = o; o += size_t(L.rows) * L.max_chunks * 2 * 4;
+  L.cand = o; o += size_t(L.rows) * kCandCap * 8;
   L.total = o;
   return L;
 }

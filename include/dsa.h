@@ -110,7 +110,7 @@ typedef struct {
 } dsa_params_t;
 
 /* Bytes of workspace the calls below need for `params`. The workspace holds
- * the device error word, the quantised indexer query, the top-k histograms,
+ * the device error word, the quantised indexer query, the top-k candidates,
  * the split-KV partial outputs and (for dsa_decode) the fp32 scores of every
  * row over max_pages_per_req * page_size tokens. */
 dsa_status_t dsa_workspace_size(const dsa_params_t* params, size_t* bytes);
@@ -179,7 +179,7 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
  * and output pointers). The paper has no counterpart: this is a deployment
  * variant of dsa_topk, with the same arguments minus the workspace and the same
  * results bit for bit.
- * - Scratch: one static device array of about 1.6 MB inside libdsa, held by
+ * - Scratch: one static device array of about 4.3 MB inside libdsa, held by
  *   every GPU that loads the library until the process exits. The call
  *   allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  * - Limits: batch * n_q <= 64 and max_pages_per_req * page_size <= 1,048,576;
