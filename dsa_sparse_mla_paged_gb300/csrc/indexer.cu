@@ -58,12 +58,18 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
     }
     return;
   }
+  // all eight heads' loads first (independent), then the per-head reductions
+  uint2 raw[8];
+#pragma unroll
+  for (int hh = 0; hh < 8; ++hh)
+    raw[hh] = *reinterpret_cast<const uint2*>(q_idx + (size_t(row) * kIdxHeads + warp * 8 + hh) * kIdxDim + lane * 4);
+  const float wl = lane < 8 ? w[size_t(row) * kIdxHeads + warp * 8 + lane] : 0.f;
+#pragma unroll
   for (int hh = 0; hh < 8; ++hh) {
     const int h = warp * 8 + hh;
     const size_t base = (size_t(row) * kIdxHeads + h) * kIdxDim + lane * 4;
-    const uint2 raw = *reinterpret_cast<const uint2*>(q_idx + base);
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw[hh].x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw[hh].y);
     float v[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
     float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
@@ -76,7 +82,8 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
       packed |= uint32_t(c) << (8 * i);
     }
     *reinterpret_cast<uint32_t*>(q8 + base) = packed;
-    if (lane == 0) wq[size_t(row) * kIdxHeads + h] = __fmul_rn(w[size_t(row) * kIdxHeads + h], __fdiv_rn(m, 448.0f));
+    const float wh = __shfl_sync(0xffffffffu, wl, hh);
+    if (lane == 0) wq[size_t(row) * kIdxHeads + h] = __fmul_rn(wh, __fdiv_rn(m, 448.0f));
   }
 }
 

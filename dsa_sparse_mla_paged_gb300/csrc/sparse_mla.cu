@@ -16,34 +16,40 @@ namespace dsa {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Tensor-core split-KV attention (sm_103a).
+// Tensor-core split-KV attention (sm_103a), one 2-CTA cluster per (row, split).
 //
-// A 96-head x 512-dim fp32 output needs all 512 TMEM columns, so each (row,
-// split) runs as two CTAs: CTA half hv accumulates output dims [256hv,
-// 256hv+256) in TMEM columns [0, 256) and keeps the 64-token score tile in
-// columns [256, 320). Both halves compute the same scores (QK^T over all 576
-// dims), hence the same softmax; the 96 heads are the M=128 rows (rows 96..127
-// are padding that is never read back).
-//   warps 0..2  softmax / epilogue: one head row per thread (thread-local
-//               online softmax in base 2, lazy rescale of O by more than 2^8)
+// A 96-head x 512-dim fp32 output needs all 512 TMEM columns, so the pair
+// splits the work by latent dims: CTA c owns nope dims [256c, 256c+256) (its
+// half of the output, TMEM columns [0, 256)) and CTA 0 also the 64 rope dims.
+// Each CTA multiplies only its own dims, S_c = Q[:, own] . C[:, own]^T, and
+// the two partial score tiles are exchanged through distributed shared memory;
+// both CTAs add them (a + b, the same IEEE result on either side), so both run
+// the identical softmax and each finishes its half of O = P . V.
+// The 96 heads are the M = 128 rows (rows 96..127 are padding, never read).
+//   warps 0..2  softmax / epilogue: one head row per thread, online softmax in
+//               base 2 with lazy rescale of O (when the max grows by > 2^8)
+//   warp  3     TMEM owner, Q by TMA, MMA issuer (QK^T of tile k+1 is issued
+//               before PV of tile k, so it overlaps the softmax)
 //   warps 4..7  converters: gather the split's selected latent rows (paged,
-//               16-B loads, one tile ahead in registers) and expand E4M3 ->
-//               bf16 exactly into the 128-B swizzled K-major tile
-//   warp  3     (its TMEM lanes are padding rows) TMEM owner, Q by TMA, MMA issuer:
-//               S[128 x 64]  = Q[128 x 576] . C^T           (36 x K=16)
-//               O[128 x 256] += P[128 x 64] . V[64 x 256]    (4 x K=16, V MN-major)
+//               16-B loads one tile ahead) and expand this CTA's dims E4M3 ->
+//               bf16 exactly into a 128-B swizzled K-major tile (2 buffers)
 // ---------------------------------------------------------------------------
-constexpr int kNT = 64;                    // tokens per tile
-constexpr int kKB = kDQK / 64;             // 9 K-blocks of 64 dims (128 B of bf16)
-constexpr int kQBlk = kHeads * 128;        // 12,288 B per Q K-block (96 rows)
-constexpr int kLBlk = kNT * 128;           // 8,192 B per latent K-block (64 rows)
-constexpr int kQBytes = kKB * kQBlk;       // 110,592
-constexpr int kLatBytes = kKB * kLBlk;     // 73,728
-constexpr int kPBytes = 128 * 128;         // 16,384
+constexpr int kNT = 64;                     // tokens per tile
+constexpr int kQBlk = kHeads * 128;         // 12,288 B per Q K-block (96 rows of 64 bf16)
+constexpr int kLBlk = kNT * 128;            // 8,192 B per latent K-block (64 rows)
+constexpr int kOwnKB = 5;                   // K-blocks of CTA 0 (4 nope + rope); CTA 1 owns 4
+constexpr int kQBytes = kOwnKB * kQBlk;     // 61,440
+constexpr int kLatBuf = kOwnKB * kLBlk;     // 40,960 per buffer
+constexpr int kPBytes = 128 * 128;          // 16,384
+constexpr int kXRow = 64 * 4 + 16;          // one row of a partial score tile (+16 B against bank conflicts)
+constexpr int kXBuf = kHeads * kXRow;       // 26,112
+constexpr uint32_t kXBytes = kHeads * 64 * 4;  // score bytes the peer sends per tile
 constexpr int kTcMlaThreads = 256;
-constexpr uint32_t kSCol = 256;
-constexpr int kSplitTiles = kSplitTok / kNT;  // tiles per split
-constexpr size_t kTcMlaSmem = 1024 + kQBytes + kLatBytes + kPBytes + kSplitTok * 8 + kSplitTiles * 8 + 8 * 8 + 16;
+constexpr uint32_t kSCol = 256;             // score tiles at TMEM columns [256, 384)
+constexpr int kSplitTiles = kSplitTok / kNT;
+constexpr int kNumBars = 16;
+constexpr size_t kTcMlaSmem =
+    1024 + kQBytes + 2 * kLatBuf + kPBytes + 2 * kXBuf + kSplitTok * 8 + kSplitTiles * 8 + kNumBars * 8 + 16;
 
 struct MlaTc {
   const int32_t* block_table;
@@ -85,35 +91,106 @@ __device__ __forceinline__ void expand_e4m3x16(const uint4 w, float scale, uint4
   }
 }
 
-__global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qmap,
-                                                                         MlaTc a) {
+// Byte offset inside a 576-B latent row of this CTA's 16-B piece q, for
+// NPC = 20 (CTA 0: nope [0, 256) then rope) or NPC = 16 (CTA 1: nope [256, 512)).
+template <int NPC>
+__device__ __forceinline__ int piece_offset(int q) {
+  return NPC == 20 ? (q < 16 ? 16 * q : 512 + 16 * (q - 16)) : 256 + 16 * q;
+}
+
+// Gather this CTA's pieces of tile k's selected rows into registers (zeros for
+// unused slots). Piece pc = ct + 128u: token pc / NPC, piece pc % NPC of its row.
+template <int NPC>
+__device__ __forceinline__ void conv_load(uint4 (&buf)[NPC / 2], const uint8_t* const* rowptr, int ct, int k) {
+  const uint8_t* const* rp = rowptr + k * kNT;
+#pragma unroll
+  for (int u = 0; u < NPC / 2; ++u) {
+    const int pc = ct + 128 * u;
+    const int jj = pc / NPC, q = pc - jj * NPC;
+    const uint8_t* p = rp[jj];
+    buf[u] = p ? __ldg(reinterpret_cast<const uint4*>(p + piece_offset<NPC>(q))) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Expand tile k into LAT[k & 1] once the tile that last used that buffer is done.
+template <int NPC>
+__device__ __forceinline__ bool conv_store(const uint4 (&buf)[NPC / 2], const MlaTc& a, int ct, int lane, int k,
+                                           uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free) {
+  const int bk = k & 1;
+  bool ok = true;
+  if (k >= 2 && !ptx::mbar_wait(lat_free + bk, uint32_t((k >> 1) - 1) & 1u)) ok = false;
+  if (ok) {
+    uint8_t* lat = LAT + bk * kLatBuf;
+#pragma unroll
+    for (int u = 0; u < NPC / 2; ++u) {
+      const int pc = ct + 128 * u;
+      const int jj = pc / NPC, q = pc - jj * NPC;
+      const int kl = q >> 2, c = (q & 3) * 2;
+      uint4 lo, hi;
+      expand_e4m3x16(buf[u], a.lat_scale, lo, hi);
+      uint8_t* rowb = lat + kl * kLBlk + jj * 128;
+      *reinterpret_cast<uint4*>(rowb + ((c ^ (jj & 7)) << 4)) = lo;
+      *reinterpret_cast<uint4*>(rowb + (((c + 1) ^ (jj & 7)) << 4)) = hi;
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(lat_full + bk);
+  return ok;
+}
+
+// Converter warps (128 threads): tiles 0..nt-1 into LAT[k & 1], the loads of
+// tile k+1 in flight while tile k waits for its buffer and is expanded.
+template <int NPC>
+__device__ void converter_role(const MlaTc& a, int ct, int lane, int nt, const uint8_t* const* rowptr,
+                               uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free, bool& ok) {
+  uint4 bufa[NPC / 2], bufb[NPC / 2];
+  conv_load<NPC>(bufa, rowptr, ct, 0);
+  for (int k = 0; k < nt; k += 2) {
+    if (k + 1 < nt) conv_load<NPC>(bufb, rowptr, ct, k + 1);
+    if (!conv_store<NPC>(bufa, a, ct, lane, k, LAT, lat_full, lat_free)) { ok = false; return; }
+    if (k + 1 >= nt) break;
+    if (k + 2 < nt) conv_load<NPC>(bufa, rowptr, ct, k + 2);
+    if (!conv_store<NPC>(bufb, a, ct, lane, k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
+    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, MlaTc a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = sm;
-  uint8_t* LAT = Qs + kQBytes;
-  uint8_t* Ps = LAT + kLatBytes;
-  const uint8_t** rowptr = reinterpret_cast<const uint8_t**>(Ps + kPBytes);            // [kSplitTok]
+  uint8_t* LAT = Qs + kQBytes;                     // 2 buffers
+  uint8_t* Ps = LAT + 2 * kLatBuf;
+  uint8_t* X = Ps + kPBytes;                       // 2 buffers: the peer's partial scores
+  const uint8_t** rowptr = reinterpret_cast<const uint8_t**>(X + 2 * kXBuf);          // [kSplitTok]
   unsigned long long* vmask = reinterpret_cast<unsigned long long*>(rowptr + kSplitTok);  // [kSplitTiles]
   uint64_t* bars = reinterpret_cast<uint64_t*>(vmask + kSplitTiles);
   uint64_t* q_full = bars + 0;
-  uint64_t* lat_full = bars + 1;
-  uint64_t* lat_free = bars + 2;
-  uint64_t* s_full = bars + 3;
-  uint64_t* p_full = bars + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* lat_full = bars + 1;   // [2]
+  uint64_t* lat_free = bars + 3;   // [2]  (PV of the buffer's last tile done)
+  uint64_t* s_full = bars + 5;     // [2]
+  uint64_t* s_free = bars + 7;     // [2]
+  uint64_t* p_full = bars + 9;
+  uint64_t* x_full = bars + 10;    // [2]  the peer's partial scores have landed in X
+  uint64_t* x_free = bars + 12;    // [2]  the peer has read what this CTA wrote into its X
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
 
-  const int half = blockIdx.x & 1, split = blockIdx.x >> 1, r = blockIdx.y;
+  const int half = int(ptx::cluster_ctarank());
+  const int peer = half ^ 1;
+  const int split = blockIdx.x >> 1, r = blockIdx.y;
   const int b = r / a.n_q, t = r - b * a.n_q;
   const int ctx = a.ctx_lens[b];
   const int L = (ctx < a.n_q || ctx > a.cap) ? 0 : ctx - a.n_q + t + 1;
   const int j0 = split * a.per_split;
   const int j1 = min(a.K, j0 + a.per_split);
   const int nt = j1 > j0 ? (j1 - j0 + kNT - 1) / kNT : 0;
+  const int nkb = half == 0 ? 5 : 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* op = a.opart + (size_t(r) * a.splits + split) * kHeads * kDNope + half * 256;
   float* lp = a.lpart + (size_t(r) * a.splits + split) * kHeads;
 
-  if (nt == 0) {  // a split past the top-k list: empty partial
+  if (nt == 0) {  // a split past the top-k list (both CTAs of the pair return here)
     for (int i = threadIdx.x; i < kHeads * 256; i += blockDim.x) op[(i >> 8) * kDNope + (i & 255)] = 0.f;
     if (half == 0)
       for (int i = threadIdx.x; i < kHeads; i += blockDim.x) lp[i] = -INFINITY;
@@ -122,10 +199,18 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    ptx::mbar_init(lat_full, 4);
-    ptx::mbar_init(lat_free, 1);
-    ptx::mbar_init(s_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(lat_full + i, 4);
+      ptx::mbar_init(lat_free + i, 1);
+      ptx::mbar_init(s_full + i, 1);
+      ptx::mbar_init(s_free + i, 3);
+      ptx::mbar_init(x_full + i, 1);
+      ptx::mbar_init(x_free + i, 3);
+    }
     ptx::mbar_init(p_full, 3);
+    // the peer's first two score tiles may arrive as soon as the pair has synced
+    ptx::mbar_arrive_expect_tx(x_full + 0, kXBytes);
+    ptx::mbar_arrive_expect_tx(x_full + 1, kXBytes);
     ptx::fence_mbar_init();
   }
   if (warp == 3) {
@@ -134,38 +219,49 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  bool ok = true;
 
   if (warp == 3) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = true;
-      ptx::mbar_arrive_expect_tx(q_full, kQBytes);
-      for (int kb = 0; kb < kKB; ++kb) ptx::tma_load_2d(Qs + kb * kQBlk, &qmap, q_full, kb * 64, r * kHeads);
+      ptx::mbar_arrive_expect_tx(q_full, nkb * kQBlk);
+      for (int kl = 0; kl < nkb; ++kl) {
+        const int kbg = half == 0 ? (kl < 4 ? kl : 8) : 4 + kl;
+        ptx::tma_load_2d(Qs + kl * kQBlk, &qmap, q_full, kbg * 64, r * kHeads);
+      }
       if (!ptx::mbar_wait(q_full, 0)) ok = false;
       const uint32_t id_qk = ptx::idesc(1, 1, 128, kNT);
       const uint32_t id_pv = ptx::idesc(1, 1, 128, 256, 0, 1);
       const uint32_t q0 = ptx::smem_u32(Qs), l0 = ptx::smem_u32(LAT), p0 = ptx::smem_u32(Ps);
-      for (int k = 0; k < nt && ok; ++k) {
-        if (!ptx::mbar_wait(lat_full, uint32_t(k) & 1u)) { ok = false; break; }
+      auto pv = [&](int j) {
+        if (!ok || !ptx::mbar_wait(p_full, uint32_t(j) & 1u)) { ok = false; return; }
         ptx::tc_fence_after();
-        for (int kb = 0; kb < kKB; ++kb)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_f16(tmem + kSCol, ptx::sdesc_sw128(q0 + kb * kQBlk + kk * 32),
-                         ptx::sdesc_sw128(l0 + kb * kLBlk + kk * 32), id_qk, (kb | kk) ? 1u : 0u);
-        ptx::mma_commit(s_full);
-        if (!ptx::mbar_wait(p_full, uint32_t(k) & 1u)) { ok = false; break; }
-        ptx::tc_fence_after();
+        const uint32_t lat = l0 + (j & 1) * kLatBuf;
 #pragma unroll
         for (int kk = 0; kk < kNT / 16; ++kk)
-          ptx::mma_f16(tmem, ptx::sdesc_sw128(p0 + kk * 32),
-                       ptx::sdesc_sw128_mn(l0 + 4 * half * kLBlk + kk * 16 * 128, kLBlk, 1024), id_pv,
-                       (k > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(lat_free);
+          ptx::mma_f16(tmem, ptx::sdesc_sw128(p0 + kk * 32), ptx::sdesc_sw128_mn(lat + kk * 16 * 128, kLBlk, 1024),
+                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(lat_free + (j & 1));
+      };
+      for (int k = 0; k < nt && ok; ++k) {
+        const int bk = k & 1;
+        const uint32_t kph = uint32_t(k >> 1) & 1u;
+        if (!ptx::mbar_wait(lat_full + bk, kph)) { ok = false; break; }
+        if (k >= 2 && !ptx::mbar_wait(s_free + bk, kph ^ 1u)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t lat = l0 + bk * kLatBuf;
+        for (int kl = 0; kl < nkb; ++kl)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_f16(tmem + kSCol + bk * kNT, ptx::sdesc_sw128(q0 + kl * kQBlk + kk * 32),
+                         ptx::sdesc_sw128(lat + kl * kLBlk + kk * 32), id_qk, (kl | kk) ? 1u : 0u);
+        ptx::mma_commit(s_full + bk);
+        if (k >= 1) pv(k - 1);
       }
-      if (!ok) atomicOr(a.err, DSA_DEVERR_TIMEOUT);
+      if (ok) pv(nt - 1);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ converters
@@ -181,9 +277,9 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
           const int pg = a.block_table[size_t(b) * a.max_pages + sidx / kPage];
           if (pg >= 0 && pg < a.num_pages)
             rp = a.lat_pool + size_t(pg) * a.lat_stride + size_t(sidx % kPage) * kLatRowFp8;
-          else
+          else if (half == 0)
             atomicOr(a.err, DSA_DEVERR_BLOCK_TABLE);
-        } else if (sidx != -1) {
+        } else if (sidx != -1 && half == 0) {
           atomicOr(a.err, DSA_DEVERR_TOPK_INDEX);
         }
       }
@@ -192,56 +288,53 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
       if (lane == 0) reinterpret_cast<uint32_t*>(vmask)[jj >> 5] = m;
     }
     ptx::named_bar_sync(1, 128);
-    uint4 buf[18];
-    bool ok = true;
-    for (int k = -1; k < nt; ++k) {
-      if (k >= 0) {
-        if (k > 0 && !ptx::mbar_wait(lat_free, uint32_t(k - 1) & 1u)) ok = false;
-        if (ok) {
-#pragma unroll
-          for (int u = 0; u < 18; ++u) {
-            const int pc = ct + 128 * u;
-            const int jj = pc / 36, c16 = pc % 36;
-            const int kb = c16 >> 2, c = (c16 & 3) * 2;
-            uint4 lo, hi;
-            expand_e4m3x16(buf[u], a.lat_scale, lo, hi);
-            uint8_t* rowb = LAT + kb * kLBlk + jj * 128;
-            *reinterpret_cast<uint4*>(rowb + ((c ^ (jj & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(rowb + (((c + 1) ^ (jj & 7)) << 4)) = hi;
-          }
-          ptx::fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(lat_full);
-        if (!ok) break;
-      }
-      if (k + 1 < nt) {
-        // start tile k+1's loads; they land while tile k is multiplied
-        const uint8_t* const* rp = rowptr + (k + 1) * kNT;
-#pragma unroll
-        for (int u = 0; u < 18; ++u) {
-          const int pc = ct + 128 * u;
-          const uint8_t* p = rp[pc / 36];
-          buf[u] = p ? __ldg(reinterpret_cast<const uint4*>(p + (pc % 36) * 16)) : make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
-    if (!ok) atomicOr(a.err, DSA_DEVERR_TIMEOUT);
+    if (half == 0)
+      converter_role<20>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
+    else
+      converter_role<16>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
   } else if (warp < 3) {
     // ------------------------------------------------------------ softmax / epilogue
     const int h = warp * 32 + lane;
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     float m_use = -INFINITY, l = 0.f;
-    bool ok = true;
+    const uint32_t x_mine = ptx::smem_u32(X) + h * kXRow;
+    const uint32_t x_peer = ptx::mapa_shared(x_mine, peer);
     for (int k = 0; k < nt; ++k) {
-      // lat_full orders the converters' validity mask before this read (they
-      // cannot refill the tile before this row's P has been consumed)
-      if (!ptx::mbar_wait(lat_full, uint32_t(k) & 1u)) { ok = false; break; }
-      if (!ptx::mbar_wait(s_full, uint32_t(k) & 1u)) { ok = false; break; }
+      const int bk = k & 1;
+      const uint32_t kph = uint32_t(k >> 1) & 1u;
+      // lat_full orders the converters' validity mask before this read
+      if (!ptx::mbar_wait(lat_full + bk, kph) || !ptx::mbar_wait(s_full + bk, kph)) { ok = false; break; }
       ptx::tc_fence_after();
       float sv[64];
-      ptx::tmem_ld32(tmem + lane_base + kSCol, *reinterpret_cast<float(*)[32]>(&sv[0]));
-      ptx::tmem_ld32(tmem + lane_base + kSCol + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+      ptx::tmem_ld32(tmem + lane_base + kSCol + bk * kNT, *reinterpret_cast<float(*)[32]>(&sv[0]));
+      ptx::tmem_ld32(tmem + lane_base + kSCol + bk * kNT + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(s_free + bk);
+      // exchange partial scores with the peer CTA: asynchronous remote stores
+      // whose bytes complete on the peer's x_full[bk]
+      if (k >= 2 && !ptx::mbar_wait_cluster(x_free + bk, kph ^ 1u)) { ok = false; break; }
+      {
+        const uint32_t dst = x_peer + bk * kXBuf;
+        const uint32_t rbar = ptx::mapa_shared(ptx::smem_u32(x_full + bk), peer);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          ptx::st_async_f4(dst + i * 16, make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), rbar);
+      }
+      if (!ptx::mbar_wait_cluster(x_full + bk, kph)) { ok = false; break; }
+      const float4* xr = reinterpret_cast<const float4*>(X + bk * kXBuf + h * kXRow);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 x = xr[i];
+        sv[4 * i] += x.x; sv[4 * i + 1] += x.y; sv[4 * i + 2] += x.z; sv[4 * i + 3] += x.w;
+      }
+      // each warp tells the peer it has read its rows; warp 0 first re-arms
+      // x_full[bk] for tile k+2 (the peer sends only after all three arrivals)
+      __syncwarp();
+      if (lane == 0) {
+        if (warp == 0 && k + 2 < nt) ptx::mbar_arrive_expect_tx(x_full + bk, kXBytes);
+        ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(x_free + bk), peer));
+      }
       const unsigned long long vm = vmask[k];
       float tmax = -INFINITY;
 #pragma unroll
@@ -249,18 +342,19 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
         sv[i] = ((vm >> i) & 1ull) ? sv[i] * a.sm_scale_log2 : -INFINITY;
         tmax = fmaxf(tmax, sv[i]);
       }
+      // P and O are free once the previous tile's PV has completed
+      if (k >= 1 && !ptx::mbar_wait(lat_free + ((k - 1) & 1), uint32_t((k - 1) >> 1) & 1u)) { ok = false; break; }
+      ptx::tc_fence_after();
       bool need = false;
       float alpha = 1.f;
       if (m_use == -INFINITY) {
         m_use = tmax;
       } else if (tmax > m_use + 8.f) {
         need = true;
-        alpha = exp2f(m_use - tmax);
+        alpha = ptx::ex2_approx(m_use - tmax);
         m_use = tmax;
       }
       if (__any_sync(0xffffffffu, need)) {
-        // O (this warp's 32 rows, 256 columns) *= alpha; the previous PV is complete
-        // because this tile's latents were written only after it finished.
         l *= alpha;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -279,8 +373,8 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 8 * c + 2 * e;
-          const float p0 = m_use == -INFINITY ? 0.f : exp2f(sv[i] - m_use);
-          const float p1 = m_use == -INFINITY ? 0.f : exp2f(sv[i + 1] - m_use);
+          const float p0 = m_use == -INFINITY ? 0.f : ptx::ex2_approx(sv[i] - m_use);
+          const float p1 = m_use == -INFINITY ? 0.f : ptx::ex2_approx(sv[i + 1] - m_use);
           psum += p0 + p1;
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
           pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
@@ -293,10 +387,8 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(p_full);
     }
-    if (ok && !ptx::mbar_wait(lat_free, uint32_t(nt - 1) & 1u)) ok = false;
-    if (!ok) {
-      if (lane == 0) atomicOr(a.err, DSA_DEVERR_TIMEOUT);
-    } else {
+    if (ok && !ptx::mbar_wait(lat_free + ((nt - 1) & 1), uint32_t((nt - 1) >> 1) & 1u)) ok = false;
+    if (ok) {
       ptx::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float* orow = op + size_t(h) * kDNope;
@@ -311,8 +403,10 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
       if (half == 0) lp[h] = l > 0.f ? (m_use + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
   }
+  if (!ok) atomicOr(a.err, DSA_DEVERR_TIMEOUT);
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // no remote access to a CTA that has exited
   if (warp == 3) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
@@ -320,32 +414,52 @@ __global__ void __launch_bounds__(kTcMlaThreads, 1) sparse_mla_tc_kernel(const _
 }
 
 // LSE merge of the splits of one row: out = sum_i e^{lse_i - lse} O_i, lse = ln sum_i e^{lse_i}.
+// One CTA per (row, 8 heads): warp w merges head 8*blockIdx.y + w; lane i < splits
+// holds split i's lse, so the weights come from two shuffle reductions.
 __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ opart,
                                                           const float* __restrict__ lpart, int splits,
                                                           __nv_bfloat16* __restrict__ out,
                                                           float* __restrict__ lse) {
   const int r = blockIdx.x;
-  const int h = blockIdx.y;
-  __shared__ float wts[kMaxSplits];
-  __shared__ float s_lse;
-  if (threadIdx.x == 0) {
-    float m = -INFINITY;
-    for (int i = 0; i < splits; ++i) m = fmaxf(m, lpart[(size_t(r) * splits + i) * kHeads + h]);
-    float tot = 0.f;
-    if (m != -INFINITY)
-      for (int i = 0; i < splits; ++i) tot += expf(lpart[(size_t(r) * splits + i) * kHeads + h] - m);
-    const float L = m == -INFINITY ? -INFINITY : m + logf(tot);
-    for (int i = 0; i < splits; ++i)
-      wts[i] = m == -INFINITY ? 0.f : expf(lpart[(size_t(r) * splits + i) * kHeads + h] - L);
-    s_lse = L;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + warp;
+  const float li = lane < splits ? __ldg(lpart + (size_t(r) * splits + lane) * kHeads + h) : -INFINITY;
+  float m = li;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float e = m == -INFINITY ? 0.f : expf(li - m);
+  float tot = e;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const float L = m == -INFINITY ? -INFINITY : m + logf(tot);
+  const float wgt = m == -INFINITY ? 0.f : expf(li - L);
+  // each lane merges 16 of the head's 512 dims (4 float4 per split)
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kMaxSplits; ++i) {
+    if (i >= splits) break;
+    const float wi = __shfl_sync(0xffffffffu, wgt, i);
+    const float4* src = reinterpret_cast<const float4*>(opart + ((size_t(r) * splits + i) * kHeads + h) * kDNope);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 v = __ldg(src + lane + 32 * j);
+      acc[j].x = fmaf(wi, v.x, acc[j].x); acc[j].y = fmaf(wi, v.y, acc[j].y);
+      acc[j].z = fmaf(wi, v.z, acc[j].z); acc[j].w = fmaf(wi, v.w, acc[j].w);
+    }
   }
-  __syncthreads();
-  for (int d = threadIdx.x; d < kDNope; d += 256) {
-    float acc = 0.f;
-    for (int i = 0; i < splits; ++i) acc = fmaf(wts[i], opart[((size_t(r) * splits + i) * kHeads + h) * kDNope + d], acc);
-    out[(size_t(r) * kHeads + h) * kDNope + d] = __float2bfloat16_rn(acc);
+  __nv_bfloat16* dst = out + (size_t(r) * kHeads + h) * kDNope;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x, acc[j].y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z, acc[j].w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst + 4 * (lane + 32 * j)) = pk;
   }
-  if (lse && threadIdx.x == 0) lse[size_t(r) * kHeads + h] = s_lse;
+  if (lse && lane == 0) lse[size_t(r) * kHeads + h] = L;
 }
 
 }  // namespace
@@ -384,7 +498,7 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   if (e != cudaSuccess) return e;
   dim3 grid(2 * L.splits, L.rows);
   sparse_mla_tc_kernel<<<grid, kTcMlaThreads, kTcMlaSmem, st>>>(qmap, t);
-  dim3 g2(L.rows, kHeads);
+  dim3 g2(L.rows, kHeads / 8);
   mla_combine_kernel<<<g2, 256, 0, st>>>(t.opart, t.lpart, L.splits, static_cast<__nv_bfloat16*>(out), lse);
   return cudaGetLastError();
 }

@@ -104,78 +104,113 @@ __device__ __forceinline__ int phys_row(const TopkArgs& a, int b, int s) {
   return pg * kPage + (s % kPage);
 }
 
-// Radix select over n keys in shared memory (NT threads, 8 bits per pass): the
-// k-th largest key (1-based) and how many keys equal to it are among the k largest.
+// Sum of one int over the CTA (NT threads); every thread gets the total.
 template <int NT>
-__device__ void smem_kth_key(const uint32_t* keys, int n, int k, int* hist, uint32_t* out_key, int* out_need) {
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_k;
-  if (threadIdx.x == 0) { s_prefix = 0; s_k = k; }
+__device__ __forceinline__ int block_sum(int v, int* smw) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ws = __reduce_add_sync(0xffffffffu, v);
+  if (lane == 0) smw[warp] = ws;
   __syncthreads();
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
+  int t = lane < NW ? smw[lane] : 0;
+  t = __reduce_add_sync(0xffffffffu, t);
+  __syncthreads();
+  return t;
+}
+
+// The k-th largest (1-based) of the keys held by the CTA (PER per thread; key
+// 0 marks an empty slot and is never counted; 1 <= k <= number of keys).
+// The bits all keys share (from the block's min and max key) are skipped; the
+// rest are radix-selected 11 bits per pass with a shared histogram of 2048 bins,
+// so bins stay spread out even when the values crowd into a narrow range.
+template <int NT, int PER>
+__device__ uint32_t block_kth_key(const uint32_t (&keys)[PER], int k, int* hist, int* smw) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (keys[i]) { mn = min(mn, keys[i]); mx = max(mx, keys[i]); }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) { smw[warp] = int(mn); smw[NW + warp] = int(mx); }
+  __syncthreads();
+  mn = lane < NW ? uint32_t(smw[lane]) : 0xFFFFFFFFu;
+  mx = lane < NW ? uint32_t(smw[NW + lane]) : 0u;
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  __syncthreads();
+  const uint32_t diff = mn ^ mx;
+  if (diff == 0) return mx;
+  int lo_bit = 32 - __clz(diff);                  // bits [lo_bit, 32) are common to all keys
+  uint32_t prefix = lo_bit >= 32 ? 0u : (mx >> lo_bit) << lo_bit;
+  int kk = k;
+  __shared__ int s_sel[2];
+  while (lo_bit > 0) {
+    const int width = min(11, lo_bit);
+    const int sh = lo_bit - width;
+    const int nb = 1 << width;
+    for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
     __syncthreads();
-    const uint32_t pre = s_prefix;
-    const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (32 - 8 * pass));
-    for (int i = threadIdx.x; i < n; i += NT) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
       const uint32_t u = keys[i];
-      if ((u & hmask) == pre) atomicAdd(&hist[(u >> shift) & 255u], 1);
+      const bool match = u != 0u && (lo_bit >= 32 || (u >> lo_bit) == (prefix >> lo_bit));
+      if (match) atomicAdd(&hist[(u >> sh) & uint32_t(nb - 1)], 1);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // walk the 256 bins from the top: lane l owns bins 255-8l .. 248-8l
-      const int lane = threadIdx.x;
-      int c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) { c[j] = hist[255 - lane * 8 - j]; sum += c[j]; }
-      int x = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      const int before = x - sum;
-      const int kk = s_k;
-      if (before < kk && kk <= x) {
-        int cum = before;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (kk <= cum + c[j]) {
-            s_prefix = pre | (uint32_t(255 - lane * 8 - j) << shift);
-            s_k = kk - cum;
-            break;
-          }
-          cum += c[j];
+    // bins from the top: thread t owns bins nb-1-t*per .. (per >= 1 when nb >= NT, else one or none)
+    const int per = (nb + NT - 1) / NT;
+    int cnt = 0;
+    for (int j = 0; j < per; ++j) {
+      const int bin = nb - 1 - int(threadIdx.x) * per - j;
+      if (bin >= 0) cnt += hist[bin];
+    }
+    int tot;
+    const int before = block_excl_scan<NT>(cnt, &tot, smw);
+    if (before < kk && kk <= before + cnt) {
+      int cum = before;
+      for (int j = 0; j < per; ++j) {
+        const int bin = nb - 1 - int(threadIdx.x) * per - j;
+        if (bin < 0) break;
+        if (kk <= cum + hist[bin]) {
+          s_sel[0] = bin;
+          s_sel[1] = kk - cum;
+          break;
         }
+        cum += hist[bin];
       }
     }
+    __syncthreads();
+    prefix |= uint32_t(s_sel[0]) << sh;
+    kk = s_sel[1];
+    lo_bit = sh;
     __syncthreads();
   }
-  *out_key = s_prefix;
-  *out_need = s_k;
-  __syncthreads();
+  return prefix;
 }
 
 // ---------------------------------------------------------------- sample
-__global__ void __launch_bounds__(512) topk_sample_kernel(TopkArgs a) {
-  __shared__ uint32_t keys[kSampleMax];
-  __shared__ int hist[256];
+constexpr int kSampleThreads = 1024;
+constexpr int kSamplePer = kSampleMax / kSampleThreads;  // 8
+
+__global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(TopkArgs a) {
+  __shared__ int smw[64];
+  __shared__ int hist[2048];
   const Row w = row_of(a, blockIdx.x);
   int* st = a.state + size_t(w.r) * kRowState;
   if (w.L <= a.K) return;
   const int ns = min(w.L, kSampleMax);
   const float* row = a.scores + size_t(w.r) * a.stride;
-  for (int i = threadIdx.x; i < ns; i += 512) keys[i] = order_key(__ldcg(row + int((int64_t(i) * w.L) / ns)));
-  __syncthreads();
+  uint32_t keys[kSamplePer];
+#pragma unroll
+  for (int u = 0; u < kSamplePer; ++u) {
+    const int i = threadIdx.x + u * kSampleThreads;
+    keys[u] = i < ns ? order_key(__ldcg(row + int((int64_t(i) * w.L) / ns))) : 0u;
+  }
   // the r-th largest sample: about 2K tokens of the row are expected at or above it
   const int r = int((int64_t(2) * a.K * ns + w.L - 1) / w.L);
-  uint32_t g = 0u;
-  if (r < ns) {
-    int need;
-    smem_kth_key<512>(keys, ns, r, hist, &g, &need);
-  }
+  const uint32_t g = r < ns ? block_kth_key<kSampleThreads, kSamplePer>(keys, r, hist, smw) : 0u;
   if (threadIdx.x == 0) {
     st[0] = int(g);
     st[1] = 0;  // candidate cursor
@@ -195,36 +230,27 @@ __global__ void __launch_bounds__(kFiltThreads) topk_filter_kernel(TopkArgs a) {
   int* st = a.state + size_t(w.r) * kRowState;
   const uint32_t g = uint32_t(st[0]);
   const float* row = a.scores + size_t(w.r) * a.stride;
-  const int s0 = c * kTopkChunk;
-  const int s1 = min(w.L, s0 + kTopkChunk);
-  // element i*1024 + 4*tid + e of the chunk; all loads issued before any use
-  float v[4][4];
-  int n[4];
+  // thread t holds tokens s0 + 16t .. s0 + 16t + 15 (all loads issued first)
+  const int s = c * kTopkChunk + threadIdx.x * 16;
+  const int n = min(16, max(0, w.L - s));
+  float v[16];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int s = s0 + i * kFiltThreads * 4 + threadIdx.x * 4;
-    n[i] = min(4, max(0, s1 - s));
-    if (n[i] == 4) {
-      const float4 f = __ldcg(reinterpret_cast<const float4*>(row + s));
-      v[i][0] = f.x; v[i][1] = f.y; v[i][2] = f.z; v[i][3] = f.w;
+    if (4 * i + 4 <= n) {
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(row + s + 4 * i));
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[i][e] = e < n[i] ? row[s + e] : 0.f;
+      for (int e = 0; e < 4; ++e) v[4 * i + e] = 4 * i + e < n ? row[s + 4 * i + e] : 0.f;
     }
   }
-  int pre[4], run = 0;
-  uint32_t keep[4];
+  uint32_t keep = 0;
+  int m = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int m = 0;
-    keep[i] = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (e < n[i] && order_key(v[i][e]) >= g) { keep[i] |= 1u << e; ++m; }
-    int tot;
-    pre[i] = block_excl_scan<kFiltThreads>(m, &tot, smw) + run;
-    run += tot;
-  }
+  for (int e = 0; e < 16; ++e)
+    if (e < n && order_key(v[e]) >= g) { keep |= 1u << e; ++m; }
+  int run;
+  const int pre = block_excl_scan<kFiltThreads>(m, &run, smw);
   if (threadIdx.x == 0) {
     const int base = atomicAdd(st + 1, run);
     if (base + run > kCandCap) atomicOr(st + 2, 1);
@@ -236,15 +262,11 @@ __global__ void __launch_bounds__(kFiltThreads) topk_filter_kernel(TopkArgs a) {
   __syncthreads();
   const int base = s_base;
   if (base + run > kCandCap) return;
-  uint64_t* out = a.cand + size_t(w.r) * kCandCap + base;
+  uint64_t* out = a.cand + size_t(w.r) * kCandCap + base + pre;
+  int p = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int s = s0 + i * kFiltThreads * 4 + threadIdx.x * 4;
-    int p = pre[i];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (keep[i] & (1u << e)) out[p++] = (uint64_t(order_key(v[i][e])) << 32) | uint32_t(s + e);
-  }
+  for (int e = 0; e < 16; ++e)
+    if (keep & (1u << e)) out[p++] = (uint64_t(order_key(v[e])) << 32) | uint32_t(s + e);
 }
 
 // ---------------------------------------------------------------- select
@@ -321,8 +343,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(TopkArgs a) {
   uint32_t* ckey = sel_smem;                                  // [kCandCap]
   int* cidx = reinterpret_cast<int*>(sel_smem + kCandCap);    // [kCandCap]
   int* hist = cidx + kCandCap;                                // [2048]
-  __shared__ int smw[32];
-  __shared__ int s_total;
+  __shared__ int smw[64];
   const Row w = row_of(a, blockIdx.x);
   int32_t* out = a.topk_idx + size_t(w.r) * a.K;
   int32_t* phys = a.phys_rows ? a.phys_rows + size_t(w.r) * a.K : nullptr;
@@ -342,53 +363,74 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(TopkArgs a) {
     select_whole_row(a, w, hist, smw, out, phys);
     return;
   }
-  // gather the candidates chunk by chunk: index order again
+  // gather the candidates chunk by chunk (index order again): chunks in
+  // windows of 1024; positions spread over all threads, each finds its chunk
+  // by binary search over the window's offsets
   const int nch = (w.L + kTopkChunk - 1) / kTopkChunk;
   const int* ci = a.chunkinfo + size_t(w.r) * a.max_chunks * 2;
   const uint64_t* cand = a.cand + size_t(w.r) * kCandCap;
-  if (threadIdx.x == 0) s_total = 0;
-  __syncthreads();
+  int* wpre = hist;          // [1024] window prefix of counts
+  int* wsrc = hist + 1024;   // [1024] source offsets
+  int done = 0;
   for (int c0 = 0; c0 < nch; c0 += kSelThreads) {
     const int c = c0 + threadIdx.x;
     const int cnt = c < nch ? ci[2 * c + 1] : 0;
-    const int run0 = s_total;
     int tot;
-    const int pre = block_excl_scan<kSelThreads>(cnt, &tot, smw) + run0;
-    if (c < nch) {
-      const int src = ci[2 * c];
-      for (int j = 0; j < cnt; ++j) {
-        const uint64_t v = cand[src + j];
-        ckey[pre + j] = uint32_t(v >> 32);
-        cidx[pre + j] = int(uint32_t(v));
-      }
-    }
+    const int pre = block_excl_scan<kSelThreads>(cnt, &tot, smw);
+    wpre[threadIdx.x] = pre;
+    wsrc[threadIdx.x] = c < nch ? ci[2 * c] : 0;
     __syncthreads();
-    if (threadIdx.x == 0) s_total = run0 + tot;
+    const int nw = min(kSelThreads, nch - c0);
+    for (int pos = threadIdx.x; pos < tot; pos += kSelThreads) {
+      int lo = 0, hi = nw - 1;  // last chunk with wpre <= pos
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (wpre[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      const uint64_t v = cand[wsrc[lo] + (pos - wpre[lo])];
+      ckey[done + pos] = uint32_t(v >> 32);
+      cidx[done + pos] = int(uint32_t(v));
+    }
+    done += tot;
     __syncthreads();
   }
-  uint32_t tau;
-  int need;
-  smem_kth_key<kSelThreads>(ckey, total, a.K, hist, &tau, &need);
-  // ordered write: thread t takes a contiguous run of the candidates
-  const int per = (total + kSelThreads - 1) / kSelThreads;
-  const int i0 = min(total, int(threadIdx.x) * per), i1 = min(total, i0 + per);
-  int ne = 0;
-  for (int i = i0; i < i1; ++i) ne += ckey[i] == tau;
+  // exact K-th largest candidate key and the ties at it to take
+  constexpr int kSelPer = kCandCap / kSelThreads;  // 8
+  uint32_t mk[kSelPer];
+#pragma unroll
+  for (int u = 0; u < kSelPer; ++u) {
+    const int i = threadIdx.x * kSelPer + u;
+    mk[u] = i < total ? ckey[i] : 0u;
+  }
+  const uint32_t tau = block_kth_key<kSelThreads, kSelPer>(mk, a.K, hist, smw);
+  int gt = 0;
+#pragma unroll
+  for (int u = 0; u < kSelPer; ++u) gt += mk[u] > tau;
+  const int need = a.K - block_sum<kSelThreads>(gt, smw);
+  // ordered write: thread t takes candidates t*8 .. t*8+7
+  int ne = 0, ns = 0;
+#pragma unroll
+  for (int u = 0; u < kSelPer; ++u) ne += (threadIdx.x * kSelPer + u < total) && mk[u] == tau;
   int te;
   int eq = block_excl_scan<kSelThreads>(ne, &te, smw);
-  int ns = 0;
-  for (int i = i0, e = eq; i < i1; ++i) {
-    const uint32_t u = ckey[i];
-    if (u > tau) ++ns;
-    else if (u == tau && e++ < need) ++ns;
+  {
+    int e = eq;
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) {
+      if (threadIdx.x * kSelPer + u >= total) break;
+      if (mk[u] > tau) ++ns;
+      else if (mk[u] == tau && e++ < need) ++ns;
+    }
   }
   int ts;
   int p = block_excl_scan<kSelThreads>(ns, &ts, smw);
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t u = ckey[i];
+#pragma unroll
+  for (int u = 0; u < kSelPer; ++u) {
+    const int i = threadIdx.x * kSelPer + u;
+    if (i >= total) break;
     bool sel = false;
-    if (u > tau) sel = true;
-    else if (u == tau) sel = eq++ < need;
+    if (mk[u] > tau) sel = true;
+    else if (mk[u] == tau) sel = eq++ < need;
     if (sel) {
       if (p < a.K) {
         out[p] = cidx[i];
@@ -421,7 +463,7 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   a.err = reinterpret_cast<int*>(ws + L.err);
   a.topk_idx = topk_idx;
   a.phys_rows = phys_rows;
-  topk_sample_kernel<<<L.rows, 512, 0, st>>>(a);
+  topk_sample_kernel<<<L.rows, kSampleThreads, 0, st>>>(a);
   topk_filter_kernel<<<dim3(L.max_chunks, L.rows), kFiltThreads, 0, st>>>(a);
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSelSmem));
   if (e != cudaSuccess) return e;
