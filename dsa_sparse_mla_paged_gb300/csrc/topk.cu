@@ -202,11 +202,14 @@ __global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(TopkArgs a)
   if (w.L <= a.K) return;
   const int ns = min(w.L, kSampleMax);
   const float* row = a.scores + size_t(w.r) * a.stride;
+  // evenly spaced positions (any fixed spread serves: g only has to be a good guess)
+  const float step = float(w.L) / float(ns);
   uint32_t keys[kSamplePer];
 #pragma unroll
   for (int u = 0; u < kSamplePer; ++u) {
     const int i = threadIdx.x + u * kSampleThreads;
-    keys[u] = i < ns ? order_key(__ldcg(row + int((int64_t(i) * w.L) / ns))) : 0u;
+    const int pos = min(w.L - 1, int(float(i) * step));
+    keys[u] = i < ns ? order_key(__ldcg(row + pos)) : 0u;
   }
   // the r-th largest sample: about 2K tokens of the row are expected at or above it
   const int r = int((int64_t(2) * a.K * ns + w.L - 1) / w.L);
