@@ -100,8 +100,9 @@ cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* w
 // Tensor-core scorer (sm_103a): a persistent CTA per SM walks a contiguous
 // range of the batch's 128-token tiles (two pages each), so every CTA streams
 // the same number of keys whatever the context lengths ("key-balanced").
-//   warp 0     : TMA producer -- key pages (128-B swizzled), their scales,
-//                and the request's FP8 query when the request changes
+//   warp 0     : TMA producer -- key pages (128-B swizzled) and their scales,
+//                lane g issuing tile g of a stage, and the request's FP8
+//                query when the request changes
 //   warp 1     : TMEM owner and MMA issuer -- D[128 tok x 32*n_q] =
 //                keys[128 x 128] * q8^T, four K=32 FP8 MMAs per tile
 //   warps 2..5 : epilogue -- one token row per thread out of TMEM,
@@ -155,19 +156,19 @@ __device__ __forceinline__ void walk_next(const IdxTc& a, TileWalk& w) {
   }
 }
 
-__device__ __forceinline__ int checked_page(const IdxTc& a, int b, int lp) {
-  const int pg = a.block_table[size_t(b) * a.max_pages + lp];
+// Block-table entries of one tile as loaded: range-checked only where they
+// are used, so the loads of a look-ahead stay in flight.
+struct TilePages {
+  int b, pg0, pg1, two;  // two: the tile holds a second page
+};
+
+__device__ __forceinline__ int page_or_zero(const IdxTc& a, int pg) {
   if (pg < 0 || pg >= a.num_pages) {
     atomicOr(a.err, DSA_DEVERR_BLOCK_TABLE);
     return 0;
   }
   return pg;
 }
-
-// Physical pages of one tile (pg1 = -1 when the tile holds a single page).
-struct TilePages {
-  int b, pg0, pg1;
-};
 
 // Move the walk `n` tiles forward; `np` tracks the pages of the walk's request.
 __device__ __forceinline__ void advance_walk(const IdxTc& a, TileWalk& w, int& np, int n) {
@@ -187,16 +188,54 @@ __device__ __forceinline__ void advance_walk(const IdxTc& a, TileWalk& w, int& n
 // Lane `lane` of the producer warp: the pages of tile (w.t + lane).
 __device__ __forceinline__ TilePages tile_pages(const IdxTc& a, const TileWalk& w, int np, long long t_end,
                                                 int lane) {
-  TilePages tp{w.b, 0, -1};
+  TilePages tp{w.b, 0, 0, 0};
   if (w.t + lane >= t_end) return tp;
   TileWalk x = w;
   int xnp = np;
   if (lane) advance_walk(a, x, xnp, lane);
   tp.b = x.b;
   const int lp0 = 2 * x.j;
-  tp.pg0 = checked_page(a, x.b, lp0);
-  if (lp0 + 1 < xnp) tp.pg1 = checked_page(a, x.b, lp0 + 1);
+  const int32_t* row = a.block_table + size_t(x.b) * a.max_pages;
+  tp.pg0 = row[lp0];
+  tp.two = lp0 + 1 < xnp;
+  if (tp.two) tp.pg1 = row[lp0 + 1];
   return tp;
+}
+
+// Epilogue position inside a stage: tile g, query row t.
+struct EpiState {
+  int g, t;
+};
+
+// Reduce one 32-column accumulator block (tile e.g, query row e.t) of this
+// thread's token row and store the score, then step to the next block.
+__device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
+                                          int lane, TileWalk& w, EpiState& e, int& cur_b, int& ctx,
+                                          float (&wl)[kMaxNQ]) {
+  if (e.t == 0 && w.b != cur_b) {
+    cur_b = w.b;
+    ctx = a.ctx_lens[w.b];
+#pragma unroll
+    for (int t = 0; t < kMaxNQ; ++t) wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
+  }
+  float scale = sc[0], wt = wl[0];
+#pragma unroll
+  for (int g = 1; g < 4; ++g)
+    if (e.g == g) scale = sc[g];
+#pragma unroll
+  for (int t = 1; t < kMaxNQ; ++t)
+    if (e.t == t) wt = wl[t];
+  float sum = 0.f;
+#pragma unroll
+  for (int h = 0; h < kIdxHeads; ++h) sum = fmaf(__shfl_sync(0xffffffffu, wt, h), fmaxf(scale * v[h], 0.f), sum);
+  const int tok = w.j * kTileTok + rowt;
+  const int Lt = ctx - a.n_q + e.t + 1;
+  if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + e.t) * a.score_stride + tok] = sum;
+  if (++e.t == a.n_q) {
+    e.t = 0;
+    ++e.g;
+    walk_next(a, w);
+  }
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -251,7 +290,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       // The whole warp looks 32 tiles ahead: lane i loads the block-table
-      // entries of tile (chunk + i) one chunk before lane 0 issues its copies,
+      // entries of tile (chunk + i) one chunk before their copies are issued,
       // so no copy waits on a dependent global load.
       if (lane == 0) {
         ptx::prefetch_tmap(&kmap);
@@ -275,33 +314,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
           const int ng = min(G, n - i0);
           uint32_t bytes = 0;
           for (int g = 0; g < ng; ++g)
-            bytes += (__shfl_sync(0xffffffffu, cur.pg1, i0 + g) >= 0 ? 2u : 1u) * (kPage * kIdxDim + kPage * 4);
+            bytes += (__shfl_sync(0xffffffffu, cur.two, i0 + g) ? 2u : 1u) * (kPage * kIdxDim + kPage * 4);
           if (lane == 0) {
             if (*abort_flag) ok = false;
             if (ok && !ptx::mbar_wait(empty + s, ph ^ 1u)) { fail(); ok = false; }
-            if (ok) ptx::mbar_arrive_expect_tx(full + s, bytes);
           }
-          // all key copies of the stage first, then its query loads: a query
-          // slot is released by the MMA warp only once it has this stage in hand
-          for (int g = 0; g < ng; ++g) {
-            const int pg0 = __shfl_sync(0xffffffffu, cur.pg0, i0 + g);
-            const int pg1 = __shfl_sync(0xffffffffu, cur.pg1, i0 + g);
-            if (lane == 0 && ok) {
-              uint8_t* kdst = keys + (size_t(s) * G + g) * kKeyTileBytes;
-              float* sdst = scl + (size_t(s) * G + g) * kTileTok;
-              ptx::tma_load_3d(kdst, &kmap, full + s, 0, 0, pg0);
-              ptx::bulk_load(sdst, a.key_pool + size_t(pg0) * a.key_page_stride + kPage * kIdxDim, kPage * 4,
+          ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+          if (!ok) break;
+          if (lane == 0) ptx::mbar_arrive_expect_tx(full + s, bytes);
+          // lane g issues the copies of tile g (keys and scales of its pages);
+          // all key copies of the stage go out before its query loads, since a
+          // query slot is released by the MMA warp only once it has this stage
+          // in hand
+          {
+            const int src = i0 + min(lane, ng - 1);
+            const int pg0 = __shfl_sync(0xffffffffu, cur.pg0, src);
+            const int pg1 = __shfl_sync(0xffffffffu, cur.pg1, src);
+            const int two = __shfl_sync(0xffffffffu, cur.two, src);
+            if (lane < ng) {
+              uint8_t* kdst = keys + (size_t(s) * G + lane) * kKeyTileBytes;
+              float* sdst = scl + (size_t(s) * G + lane) * kTileTok;
+              const int p0 = page_or_zero(a, pg0);
+              ptx::tma_load_3d(kdst, &kmap, full + s, 0, 0, p0);
+              ptx::bulk_load(sdst, a.key_pool + size_t(p0) * a.key_page_stride + kPage * kIdxDim, kPage * 4,
                              full + s);
-              if (pg1 >= 0) {
-                ptx::tma_load_3d(kdst + kPage * kIdxDim, &kmap, full + s, 0, 0, pg1);
-                ptx::bulk_load(sdst + kPage, a.key_pool + size_t(pg1) * a.key_page_stride + kPage * kIdxDim,
+              if (two) {
+                const int p1 = page_or_zero(a, pg1);
+                ptx::tma_load_3d(kdst + kPage * kIdxDim, &kmap, full + s, 0, 0, p1);
+                ptx::bulk_load(sdst + kPage, a.key_pool + size_t(p1) * a.key_page_stride + kPage * kIdxDim,
                                kPage * 4, full + s);
               }
             }
           }
           for (int g = 0; g < ng; ++g) {
             const int b = __shfl_sync(0xffffffffu, cur.b, i0 + g);
-            if (lane == 0 && ok && b != cur_b) {
+            if (lane == 0 && b != cur_b) {
               ++nq;
               const int slot = nq & 1;
               if (!ptx::mbar_wait(qempty + slot, (uint32_t(nq >> 1) & 1u) ^ 1u)) { fail(); ok = false; }
@@ -348,6 +395,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
             const uint32_t a_base = ptx::smem_u32(keys + (size_t(s) * G + g) * kKeyTileBytes);
             const uint32_t b_base = ptx::smem_u32(qbuf + (nq & 1) * qbytes);
             const uint32_t d = tmem + uint32_t((acc * G + g) * a.ncol);
+            // tile-major order: the four K steps of a tile back to back (measured
+            // faster than interleaving the tiles of a stage)
 #pragma unroll
             for (int kk = 0; kk < kIdxDim / 32; ++kk)
               ptx::mma_f8f6f4(d, ptx::sdesc_sw128(a_base + kk * 32), ptx::sdesc_sw128(b_base + kk * 32), id,
@@ -380,28 +429,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
         for (int g = 0; g < 4; ++g) sc[g] = g < ng ? scl[(size_t(s) * G + g) * kTileTok + rowt] : 0.f;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty + s);
+        // the stage's accumulators are nb = ng * n_q blocks of 32 columns,
+        // block (g, t) = tile g, query row t; the load of block c + 1 is in
+        // flight while block c is reduced
+        const uint32_t col0 = tmem + (uint32_t(quad * 32) << 16) + uint32_t(acc * G * a.ncol);
+        const int nb = ng * a.n_q;
+        EpiState e{0, 0};
+        float va[32], vb[32];
+        ptx::tmem_ld32_nowait(col0, va);
+        ptx::tmem_ld_wait(va);
 #pragma unroll 1
-        for (int g = 0; g < ng; ++g, walk_next(a, w)) {
-          if (w.b != cur_b) {
-            cur_b = w.b;
-            ctx = a.ctx_lens[w.b];
-#pragma unroll
-            for (int t = 0; t < kMaxNQ; ++t)
-              wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
-          }
-          const float scale = g == 0 ? sc[0] : g == 1 ? sc[1] : g == 2 ? sc[2] : sc[3];
-          const int tok = w.j * kTileTok + rowt;
-#pragma unroll
-          for (int t = 0; t < kMaxNQ; ++t) {
-            if (t >= a.n_q) break;
-            float v[32];
-            ptx::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t((acc * G + g) * a.ncol + t * 32), v);
-            float sum = 0.f;
-#pragma unroll
-            for (int h = 0; h < kIdxHeads; ++h)
-              sum = fmaf(__shfl_sync(0xffffffffu, wl[t], h), fmaxf(scale * v[h], 0.f), sum);
-            const int Lt = ctx - a.n_q + t + 1;
-            if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + t) * a.score_stride + tok] = sum;
+        for (int c = 0; c < nb; c += 2) {
+          if (c + 1 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 1) * 32), vb);
+          epi_block(a, va, sc, rowt, lane, w, e, cur_b, ctx, wl);
+          if (c + 1 < nb) {
+            ptx::tmem_ld_wait(vb);
+            if (c + 2 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 2) * 32), va);
+            epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ctx, wl);
+            if (c + 2 < nb) ptx::tmem_ld_wait(va);
           }
         }
         ptx::tc_fence_before();
