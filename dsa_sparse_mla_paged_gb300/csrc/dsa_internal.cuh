@@ -30,7 +30,7 @@ constexpr int kRowState = 16;     // int32 words of per-row selection state
 // sparse attention: the K selected slots of a row are cut into splits of this
 // many tokens, one CTA pair each. The split size depends on nothing but K, so a
 // request's result does not depend on the batch it is in.
-constexpr int kSplitTok = 256;
+constexpr int kSplitTok = 128;
 constexpr int kMaxSplits = (kMaxTopK + kSplitTok - 1) / kSplitTok;
 
 // Byte offsets of the workspace regions (all 256-B aligned).

@@ -90,6 +90,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 
 // ------------------------------------------------------------------ clusters
+// Untiled bulk copy shared -> global (both 16-B aligned, bytes a multiple of
+// 16), tracked by this thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+// Close this thread's bulk group and wait until its stores have completed.
+__device__ __forceinline__ void bulk_store_commit_wait() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -48,6 +48,8 @@ constexpr int kTcMlaThreads = 256;
 constexpr uint32_t kSCol = 256;             // score tiles at TMEM columns [256, 384)
 constexpr int kSplitTiles = kSplitTok / kNT;
 constexpr int kNumBars = 16;
+constexpr int kORow = 256 * 4 + 16;         // staged output row (+16 B against bank conflicts)
+static_assert(kHeads * kORow <= 2 * kLatBuf + kPBytes + 2 * kXBuf, "output staging overlaps the tile buffers");
 constexpr size_t kTcMlaSmem =
     1024 + kQBytes + 2 * kLatBuf + kPBytes + 2 * kXBuf + kSplitTok * 8 + kSplitTiles * 8 + kNumBars * 8 + 16;
 
@@ -389,17 +391,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
     }
     if (ok && !ptx::mbar_wait(lat_free + ((nt - 1) & 1), uint32_t((nt - 1) >> 1) & 1u)) ok = false;
     if (ok) {
+      // O / l of this head row: TMEM -> the free tile buffers (one padded row
+      // per head) -> one 1-KB bulk store per row
       ptx::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* orow = op + size_t(h) * kDNope;
+      uint8_t* orow_s = LAT + size_t(h) * kORow;
 #pragma unroll 1
       for (int c = 0; c < 256; c += 32) {
         float o[32];
         ptx::tmem_ld32(tmem + lane_base + c, o);
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(orow + c + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+          *reinterpret_cast<float4*>(orow_s + (c + i) * 4) =
+              make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
       }
+      ptx::fence_proxy_async_smem();
+      ptx::bulk_store(op + size_t(h) * kDNope, orow_s, 256 * 4);
+      ptx::bulk_store_commit_wait();
       if (half == 0) lp[h] = l > 0.f ? (m_use + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
   }
@@ -414,52 +422,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
 }
 
 // LSE merge of the splits of one row: out = sum_i e^{lse_i - lse} O_i, lse = ln sum_i e^{lse_i}.
-// One CTA per (row, 8 heads): warp w merges head 8*blockIdx.y + w; lane i < splits
-// holds split i's lse, so the weights come from two shuffle reductions.
-__global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ opart,
-                                                          const float* __restrict__ lpart, int splits,
-                                                          __nv_bfloat16* __restrict__ out,
-                                                          float* __restrict__ lse) {
+// One CTA per (row, 2 heads): 128 threads per head, 4 dims each. In every warp
+// lane i < splits holds split i's lse, so the weights come from two shuffle
+// reductions; the partial rows are read 8 splits at a time.
+constexpr int kCombThreads = 256;
+constexpr int kCombHeads = kCombThreads / 128;
+
+__global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* __restrict__ opart,
+                                                                   const float* __restrict__ lpart, int splits,
+                                                                   __nv_bfloat16* __restrict__ out,
+                                                                   float* __restrict__ lse) {
   const int r = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * 8 + warp;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kCombHeads + (threadIdx.x >> 7);
+  const int d4 = threadIdx.x & 127;  // dims 4*d4 .. 4*d4+3
   const float li = lane < splits ? __ldg(lpart + (size_t(r) * splits + lane) * kHeads + h) : -INFINITY;
   float m = li;
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float e = m == -INFINITY ? 0.f : expf(li - m);
+  const float e = m == -INFINITY ? 0.f : expf(li - m);
   float tot = e;
 #pragma unroll
   for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const float L = m == -INFINITY ? -INFINITY : m + logf(tot);
   const float wgt = m == -INFINITY ? 0.f : expf(li - L);
-  // each lane merges 16 of the head's 512 dims (4 float4 per split)
-  float4 acc[4];
+  const float4* src = reinterpret_cast<const float4*>(opart + (size_t(r) * splits * kHeads + h) * kDNope) + d4;
+  const size_t split_stride = size_t(kHeads) * kDNope / 4;  // float4 per split
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < splits; i0 += 8) {
+    float4 v[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < 8; ++u) v[u] = i0 + u < splits ? __ldg(src + (i0 + u) * split_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < kMaxSplits; ++i) {
-    if (i >= splits) break;
-    const float wi = __shfl_sync(0xffffffffu, wgt, i);
-    const float4* src = reinterpret_cast<const float4*>(opart + ((size_t(r) * splits + i) * kHeads + h) * kDNope);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float4 v = __ldg(src + lane + 32 * j);
-      acc[j].x = fmaf(wi, v.x, acc[j].x); acc[j].y = fmaf(wi, v.y, acc[j].y);
-      acc[j].z = fmaf(wi, v.z, acc[j].z); acc[j].w = fmaf(wi, v.w, acc[j].w);
+    for (int u = 0; u < 8; ++u) {
+      const float wi = __shfl_sync(0xffffffffu, wgt, (i0 + u) & 31);
+      if (i0 + u < splits) {
+        acc.x = fmaf(wi, v[u].x, acc.x); acc.y = fmaf(wi, v[u].y, acc.y);
+        acc.z = fmaf(wi, v[u].z, acc.z); acc.w = fmaf(wi, v[u].w, acc.w);
+      }
     }
   }
-  __nv_bfloat16* dst = out + (size_t(r) * kHeads + h) * kDNope;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x, acc[j].y);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z, acc[j].w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dst + 4 * (lane + 32 * j)) = pk;
-  }
-  if (lse && lane == 0) lse[size_t(r) * kHeads + h] = L;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(out + (size_t(r) * kHeads + h) * kDNope + 4 * d4) = pk;
+  if (lse && d4 == 0) lse[size_t(r) * kHeads + h] = L;
 }
 
 }  // namespace
@@ -498,8 +507,8 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   if (e != cudaSuccess) return e;
   dim3 grid(2 * L.splits, L.rows);
   sparse_mla_tc_kernel<<<grid, kTcMlaThreads, kTcMlaSmem, st>>>(qmap, t);
-  dim3 g2(L.rows, kHeads / 8);
-  mla_combine_kernel<<<g2, 256, 0, st>>>(t.opart, t.lpart, L.splits, static_cast<__nv_bfloat16*>(out), lse);
+  dim3 g2(L.rows, kHeads / kCombHeads);
+  mla_combine_kernel<<<g2, kCombThreads, 0, st>>>(t.opart, t.lpart, L.splits, static_cast<__nv_bfloat16*>(out), lse);
   return cudaGetLastError();
 }
 
