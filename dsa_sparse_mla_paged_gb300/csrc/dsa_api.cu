@@ -29,7 +29,6 @@ dsa_status_t check_params(const dsa_params_t* p) {
   if (p->lat_page_stride < lat_page || (p->lat_page_stride & 15)) return DSA_ERR_INVALID;
   if (!(p->softmax_scale > 0.f) || !(p->latent_scale > 0.f)) return DSA_ERR_INVALID;
   if (p->flags & ~int32_t(DSA_EMIT_PHYS_ROWS)) return DSA_ERR_INVALID;
-  if (p->key_fmt != DSA_KEY_FP8_132 || p->lat_fmt != DSA_LAT_FP8_576) return DSA_ERR_UNSUPPORTED;
   // keep every index of the kernels inside int32 / the grid limits
   if (int64_t(p->max_pages_per_req) * p->page_size > (int64_t(1) << 28)) return DSA_ERR_UNSUPPORTED;
   if (int64_t(p->batch) * p->n_q > 65535) return DSA_ERR_UNSUPPORTED;

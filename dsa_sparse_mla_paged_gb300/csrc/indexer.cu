@@ -5,9 +5,12 @@
 // (vLLM, "vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持": sections "K3.1 Pro 中的稀疏注意力"
 // and "低延迟解码：融合的 DSA 解码路径").
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "dsa_internal.cuh"
 #include "sm103_ptx.cuh"
@@ -107,10 +110,19 @@ cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* w
 //                keys[128 x 128] * q8^T, four K=32 FP8 MMAs per tile
 //   warps 2..5 : epilogue -- one token row per thread out of TMEM,
 //                score = sum_h w'_h * max(scale * D_h, 0), coalesced store
+// MXFP4 keys (68 B: 128 E2M1 + one E8M0 exponent per 32) take the same MMA and
+// epilogue. The producer then bulk-copies raw page pairs into a ring of their
+// own, and warps 6..9 rewrite each token as E4M3 values k * 2^(e_b - e_max)
+// (block b's exponent relative to the token's largest) plus a per-token scale
+// 2^(e_max - 127): exact whenever the token's block exponents lie within 8 of
+// one another (E4M3 reaches 2^-9), the nearest E4M3 value otherwise.
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 192;    // FP8 keys
+constexpr int kMxThreads = 320;    // MXFP4 keys: + 4 converter warps
+constexpr int kMxPageBytes = kPage * (kIdxDim / 2 + kIdxDim / 32);  // 4,352
+constexpr int kMxRawTile = 2 * kMxPageBytes;
 constexpr int kTileTok = 128;
 constexpr int kKeyTileBytes = kTileTok * kIdxDim;   // 16 KB
 constexpr int kScaleTileBytes = kTileTok * 4;       // 512 B
@@ -125,6 +137,7 @@ struct IdxTc {
   int64_t score_stride;
   int64_t key_page_stride;
   int batch, n_q, max_pages, num_pages, stages, nacc, group, ncol, tmem_cols;
+  int raw_slots;  // MXFP4: raw page-pair slots
   int* err;
 };
 
@@ -238,9 +251,51 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
   }
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                   const __grid_constant__ CUtensorMap qmap,
-                                                                   IdxTc a) {
+// One MXFP4 token (64 B of E2M1 pairs, element 2i in the low nibble; 4 E8M0
+// exponents) -> 128 E4M3 values into its 128-B swizzled row, and its scale.
+__device__ __forceinline__ void mx_convert_row(const uint8_t* vals, uint32_t e4, uint8_t* row, int r, float* scale) {
+  const uint32_t e0 = e4 & 0xFFu, e1 = (e4 >> 8) & 0xFFu, e2 = (e4 >> 16) & 0xFFu, e3 = e4 >> 24;
+  const uint32_t emax = max(max(e0, e1), max(e2, e3));
+  *scale = emax == 0u ? __uint_as_float(0x00400000u) : emax == 255u ? __uint_as_float(0x7FC00000u)
+                                                                    : __uint_as_float(emax << 23);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t eb = (e4 >> (8 * b)) & 0xFFu;
+    const uint32_t d = emax - eb;  // 2^-d as f16 (exact down to 2^-24, zero below)
+    const unsigned short mbits = d <= 14u ? (unsigned short)((15u - d) << 10)
+                                 : d <= 24u ? (unsigned short)(1u << (24u - d)) : (unsigned short)0;
+    const __half2 m2 = __halves2half2(__ushort_as_half(mbits), __ushort_as_half(mbits));
+    const uint4 v = *reinterpret_cast<const uint4*>(vals + 16 * b);
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int j = 2 * jp; j < 2 * jp + 2; ++j) {
+          __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(
+              static_cast<__nv_fp4x2_storage_t>((words[i] >> (8 * j)) & 0xFFu), __NV_E2M1);
+          const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&h), m2);
+          const __nv_fp8x2_storage_t f8 =
+              __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&x), __NV_SATFINITE, __NV_E4M3);
+          packed |= uint32_t(f8) << (16 * (j & 1));
+        }
+        o[(i & 1) * 2 + jp] = packed;
+      }
+      if (i & 1) {
+        // words i-1, i: 16 E4M3 bytes = output chunk 2b + i/2
+        const int c = 2 * b + (i >> 1);
+        *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
+template <bool kMx>
+__global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, IdxTc a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages, NA = a.nacc, G = a.group;
@@ -248,14 +303,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
   uint8_t* keys = smem;                                           // S x G x 16 KB
   uint8_t* qbuf = keys + size_t(S) * G * kKeyTileBytes;           // 2 x qbytes
   float* scl = reinterpret_cast<float*>(qbuf + 2 * qbytes);       // S x G x 128
-  uint64_t* bars = reinterpret_cast<uint64_t*>(scl + size_t(S) * G * kTileTok);
+  uint8_t* raw = reinterpret_cast<uint8_t*>(scl + size_t(S) * G * kTileTok);  // MXFP4: R x 8,704 B
+  const int R = kMx ? a.raw_slots : 0;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + size_t(R) * kMxRawTile);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + NA;
   uint64_t* qfull = tempty + NA;
   uint64_t* qempty = qfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qempty + 2);
+  uint64_t* rfull = qempty + 2;   // MXFP4 raw slots: landed
+  uint64_t* rempty = rfull + R;   // MXFP4 raw slots: converted
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + R);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -264,7 +323,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
   const long long t_end = T * (blockIdx.x + 1) / gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) { ptx::mbar_init(full + i, 1); ptx::mbar_init(empty + i, 1 + 4); }
+    for (int i = 0; i < S; ++i) { ptx::mbar_init(full + i, kMx ? 4 : 1); ptx::mbar_init(empty + i, 1 + 4); }
+    for (int i = 0; i < R; ++i) { ptx::mbar_init(rfull + i, 1); ptx::mbar_init(rempty + i, 4); }
     for (int i = 0; i < NA; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, 4); }
     for (int i = 0; i < 2; ++i) { ptx::mbar_init(qfull + i, 1); ptx::mbar_init(qempty + i, 1); }
     *abort_flag = 0;
@@ -293,9 +353,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
       // entries of tile (chunk + i) one chunk before their copies are issued,
       // so no copy waits on a dependent global load.
       if (lane == 0) {
-        ptx::prefetch_tmap(&kmap);
+        if (!kMx) ptx::prefetch_tmap(&kmap);
         ptx::prefetch_tmap(&qmap);
       }
+      int rs = 0;         // MXFP4 raw slot
+      uint32_t rph = 0;   // its phase bit
       TileWalk base;
       walk_start(a, t_begin, base);
       int base_np = (a.ctx_lens[base.b] + kPage - 1) / kPage;
@@ -312,6 +374,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
         const int n = int(t_end - tc < 32 ? t_end - tc : 32);
         for (int i0 = 0; i0 < n; i0 += G) {
           const int ng = min(G, n - i0);
+          if constexpr (kMx) {
+            // raw page pairs, one slot per tile; lanes 0 / 1 copy page 0 / 1
+            for (int g = 0; g < ng; ++g) {
+              const int pg0 = __shfl_sync(0xffffffffu, cur.pg0, i0 + g);
+              const int pg1 = __shfl_sync(0xffffffffu, cur.pg1, i0 + g);
+              const int two = __shfl_sync(0xffffffffu, cur.two, i0 + g);
+              if (lane == 0) {
+                if (*abort_flag) ok = false;
+                if (ok && !ptx::mbar_wait(rempty + rs, rph ^ 1u)) { fail(); ok = false; }
+                if (ok) ptx::mbar_arrive_expect_tx(rfull + rs, (two ? 2u : 1u) * kMxPageBytes);
+              }
+              ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+              if (!ok) break;
+              if (lane < 1 + two) {
+                const int pg = page_or_zero(a, lane ? pg1 : pg0);
+                ptx::bulk_load(raw + size_t(rs) * kMxRawTile + lane * kMxPageBytes,
+                               a.key_pool + size_t(pg) * a.key_page_stride, kMxPageBytes, rfull + rs);
+              }
+              if (++rs == R) { rs = 0; rph ^= 1u; }
+            }
+            if (!ok) break;
+          } else {
           uint32_t bytes = 0;
           for (int g = 0; g < ng; ++g)
             bytes += (__shfl_sync(0xffffffffu, cur.two, i0 + g) ? 2u : 1u) * (kPage * kIdxDim + kPage * 4);
@@ -345,6 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
                                kPage * 4, full + s);
               }
             }
+          }
           }
           for (int g = 0; g < ng; ++g) {
             const int b = __shfl_sync(0xffffffffu, cur.b, i0 + g);
@@ -409,7 +494,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) indexer_tc_kernel(const __grid_
           if (++acc == NA) { acc = 0; aph ^= 1u; }
         }
       }
-    } else {
+    } else if (kMx && warp >= 6) {
+      // ------------------------------------------------------------ MXFP4 converters
+      // thread ct rewrites token row ct of every tile (page ct / 64, slot ct % 64)
+      const int ct = threadIdx.x - 192;
+      const int half = ct >> 6, slot = ct & 63;
+      int rs = 0, s = 0, g = 0;
+      uint32_t rph = 0, ph = 0;
+      for (long long t = t_begin; t < t_end; ++t) {
+        if (*abort_flag) break;
+        if (g == 0 && !ptx::mbar_wait(empty + s, ph ^ 1u)) { fail(); break; }
+        if (!ptx::mbar_wait(rfull + rs, rph)) { fail(); break; }
+        const uint8_t* page = raw + size_t(rs) * kMxRawTile + half * kMxPageBytes;
+        mx_convert_row(page + slot * (kIdxDim / 2),
+                       *reinterpret_cast<const uint32_t*>(page + kPage * (kIdxDim / 2) + 4 * slot),
+                       keys + (size_t(s) * G + g) * kKeyTileBytes + ct * kIdxDim, ct,
+                       scl + (size_t(s) * G + g) * kTileTok + ct);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(rempty + rs);
+        if (++rs == R) { rs = 0; rph ^= 1u; }
+        if (++g == G || t + 1 == t_end) {
+          ptx::fence_proxy_async_smem();  // the MMA reads the keys through the async proxy
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(full + s);
+          g = 0;
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+      }
+    } else if (warp >= 2 && warp < 6) {
       // ------------------------------------------------------------ epilogue
       const int quad = warp & 3;
       const int rowt = quad * 32 + lane;
@@ -510,8 +622,10 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   const uint8_t* q8 = reinterpret_cast<const uint8_t*>(ws + L.q8);
   const float* wq = reinterpret_cast<const float*>(ws + L.wq);
   int* err = reinterpret_cast<int*>(ws + L.err);
+  const bool mx = p.key_fmt == DSA_KEY_MXFP4_68;
   CUtensorMap kmap, qmap;
-  {
+  std::memset(&kmap, 0, sizeof(kmap));  // unused by the MXFP4 kernel (raw pages go by bulk copy)
+  if (!mx) {
     const uint64_t dims[3] = {uint64_t(kIdxDim), uint64_t(kPage), uint64_t(p.num_pages)};
     const uint64_t strides[2] = {uint64_t(kIdxDim), uint64_t(p.key_page_stride)};
     const uint32_t box[3] = {uint32_t(kIdxDim), uint32_t(kPage), 1};
@@ -537,24 +651,38 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   a.max_pages = p.max_pages_per_req;
   a.num_pages = p.num_pages;
   a.ncol = p.n_q * kIdxHeads;
-  // tiles per stage: as many as fit 256 accumulator columns (at most 4)
-  a.group = std::max(1, std::min(4, 256 / a.ncol));
+  // tiles per stage: as many as fit 256 accumulator columns (at most 4; at
+  // most 2 with MXFP4 keys, whose raw ring needs the room)
+  a.group = std::max(1, std::min(mx ? 2 : 4, 256 / a.ncol));
   const int slot_cols = a.group * a.ncol;
   a.nacc = std::max(1, std::min(4, 512 / slot_cols));
   int cols = 32;
   while (cols < a.nacc * slot_cols) cols <<= 1;
   a.tmem_cols = cols;
   const size_t stage_bytes = size_t(a.group) * (kKeyTileBytes + kScaleTileBytes);
-  const size_t fixed = 1024 + 2 * size_t(p.n_q) * kIdxHeads * kIdxDim + 256;
-  a.stages = int(std::min<size_t>(8, (227 * 1024 - fixed) / stage_bytes));
+  const size_t fixed = 1024 + 2 * size_t(p.n_q) * kIdxHeads * kIdxDim + 512;
+  const size_t budget = 227 * 1024 - fixed;
+  if (mx) {
+    // three key stages; the rest of shared memory holds raw page pairs in flight
+    a.stages = 3;
+    a.raw_slots = int(std::min<size_t>(16, (budget - 3 * stage_bytes) / kMxRawTile));
+  } else {
+    a.stages = int(std::min<size_t>(8, budget / stage_bytes));
+    a.raw_slots = 0;
+  }
   a.err = err;
-  const size_t smem = fixed + size_t(a.stages) * stage_bytes;
-  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  const size_t smem = fixed + size_t(a.stages) * stage_bytes + size_t(a.raw_slots) * kMxRawTile;
+  const void* fn = mx ? reinterpret_cast<const void*>(indexer_tc_kernel<true>)
+                      : reinterpret_cast<const void*>(indexer_tc_kernel<false>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   // enough tiles for every SM is the common case; with fewer, one CTA per tile
   const long long max_tiles = (long long)p.batch * ((L.cap + kTileTok - 1) / kTileTok);
   const int grid = int(std::min<long long>(sm_count(), std::max<long long>(1, max_tiles)));
-  indexer_tc_kernel<<<grid, kTcThreads, smem, st>>>(kmap, qmap, a);
+  if (mx)
+    indexer_tc_kernel<true><<<grid, kMxThreads, smem, st>>>(kmap, qmap, a);
+  else
+    indexer_tc_kernel<false><<<grid, kTcThreads, smem, st>>>(kmap, qmap, a);
   return cudaGetLastError();
 }
 

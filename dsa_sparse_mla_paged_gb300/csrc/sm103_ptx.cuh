@@ -98,9 +98,11 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
                : "memory");
 }
 
-// Close this thread's bulk group and wait until its stores have completed.
-__device__ __forceinline__ void bulk_store_commit_wait() {
-  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+// Close this thread's bulk group and wait until its sources have been read
+// (the shared memory may then be reused; the global writes finish on their own
+// and are visible once the grid has completed).
+__device__ __forceinline__ void bulk_store_commit_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

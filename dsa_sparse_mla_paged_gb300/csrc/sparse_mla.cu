@@ -6,6 +6,7 @@
 // heads; "长上下文：带稀疏 indexer 的 decode 上下文并行": partial outputs merge by
 // log-sum-exp.)
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "dsa_internal.cuh"
@@ -59,6 +60,7 @@ struct MlaTc {
   const int32_t* topk_idx;
   const uint8_t* lat_pool;
   int64_t lat_stride;
+  int lat_row, lat_nvfp4;  // bytes per latent row; 1 for the NVFP4 row format
   int max_pages, num_pages, n_q, cap, K, splits, per_split;
   float sm_scale_log2, lat_scale;
   float* opart;
@@ -154,6 +156,121 @@ __device__ void converter_role(const MlaTc& a, int ct, int lane, int nt, const u
     if (k + 1 >= nt) break;
     if (k + 2 < nt) conv_load<NPC>(bufa, rowptr, ct, k + 2);
     if (!conv_store<NPC>(bufb, a, ct, lane, k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 latent rows (352 B: [256 B E2M1, element 2i in the low nibble][32 B
+// E4M3 scales, one per 16 nope values][64 B E4M3 rope]). A unit is 16 bytes of
+// a row: an E2M1 unit holds 32 nope values (two scales), a rope unit 16 E4M3
+// values. CTA 0 takes E2M1 units 0..7 (nope [0, 256)) and rope units 8..11;
+// CTA 1 takes E2M1 units 8..15 (nope [256, 512)).
+// ---------------------------------------------------------------------------
+template <int HALF>
+struct NvUnits {
+  static constexpr int kPerTok = HALF == 0 ? 12 : 8;
+  static constexpr int kPerThread = kNT * kPerTok / 128;
+};
+
+struct NvUnit {
+  uint4 v;
+  uint32_t s;  // the unit's two E4M3 scales (E2M1 units)
+};
+
+template <int HALF>
+__device__ __forceinline__ void conv_load_nv(NvUnit (&buf)[NvUnits<HALF>::kPerThread], const uint8_t* const* rowptr,
+                                             int ct, int k) {
+  constexpr int NU = NvUnits<HALF>::kPerTok;
+  const uint8_t* const* rp = rowptr + k * kNT;
+#pragma unroll
+  for (int u = 0; u < NvUnits<HALF>::kPerThread; ++u) {
+    const int pc = ct + 128 * u;
+    const int jj = pc / NU, q = pc - jj * NU;
+    const uint8_t* p = rp[jj];
+    buf[u].v = make_uint4(0, 0, 0, 0);
+    buf[u].s = 0;
+    if (p) {
+      if (q < 8) {
+        const int e = HALF * 8 + q;  // E2M1 unit of the row
+        buf[u].v = __ldg(reinterpret_cast<const uint4*>(p + 16 * e));
+        buf[u].s = __ldg(reinterpret_cast<const uint16_t*>(p + 256 + 2 * e));
+      } else {
+        buf[u].v = __ldg(reinterpret_cast<const uint4*>(p + 288 + 16 * (q - 8)));
+      }
+    }
+  }
+}
+
+// 8 E2M1 values (one 32-bit word) times `scale` -> 8 bf16 (one 16-B chunk).
+__device__ __forceinline__ uint4 e2m1x8_scaled(uint32_t w, float scale) {
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>((w >> (8 * i)) & 0xFFu), __NV_E2M1);
+    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    o[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte & 0xFFu), __NV_E4M3);
+  return __half2float(*reinterpret_cast<const __half*>(&h));
+}
+
+template <int HALF>
+__device__ __forceinline__ bool conv_store_nv(const NvUnit (&buf)[NvUnits<HALF>::kPerThread], const MlaTc& a, int ct,
+                                              int lane, int k, uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free) {
+  constexpr int NU = NvUnits<HALF>::kPerTok;
+  const int bk = k & 1;
+  bool ok = true;
+  if (k >= 2 && !ptx::mbar_wait(lat_free + bk, uint32_t((k >> 1) - 1) & 1u)) ok = false;
+  if (ok) {
+    uint8_t* lat = LAT + bk * kLatBuf;
+#pragma unroll
+    for (int u = 0; u < NvUnits<HALF>::kPerThread; ++u) {
+      const int pc = ct + 128 * u;
+      const int jj = pc / NU, q = pc - jj * NU;
+      uint8_t* rowb;
+      if (q < 8) {
+        // nope dims [32q, 32q + 32) of this CTA: K-block q / 2, chunks 4 (q & 1) .. + 3
+        rowb = lat + (q >> 1) * kLBlk + jj * 128;
+        const float s0 = e4m3_to_float(buf[u].s) * a.lat_scale;
+        const float s1 = e4m3_to_float(buf[u].s >> 8) * a.lat_scale;
+        const int c0 = (q & 1) * 4;
+        *reinterpret_cast<uint4*>(rowb + (((c0 + 0) ^ (jj & 7)) << 4)) = e2m1x8_scaled(buf[u].v.x, s0);
+        *reinterpret_cast<uint4*>(rowb + (((c0 + 1) ^ (jj & 7)) << 4)) = e2m1x8_scaled(buf[u].v.y, s0);
+        *reinterpret_cast<uint4*>(rowb + (((c0 + 2) ^ (jj & 7)) << 4)) = e2m1x8_scaled(buf[u].v.z, s1);
+        *reinterpret_cast<uint4*>(rowb + (((c0 + 3) ^ (jj & 7)) << 4)) = e2m1x8_scaled(buf[u].v.w, s1);
+      } else {
+        // rope dims [16 (q - 8), + 16): K-block 4, chunks 2 (q - 8) and + 1
+        rowb = lat + 4 * kLBlk + jj * 128;
+        const int c = (q - 8) * 2;
+        uint4 lo, hi;
+        expand_e4m3x16(buf[u].v, a.lat_scale, lo, hi);
+        *reinterpret_cast<uint4*>(rowb + ((c ^ (jj & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(rowb + (((c + 1) ^ (jj & 7)) << 4)) = hi;
+      }
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(lat_full + bk);
+  return ok;
+}
+
+template <int HALF>
+__device__ void converter_role_nv(const MlaTc& a, int ct, int lane, int nt, const uint8_t* const* rowptr,
+                                  uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free, bool& ok) {
+  NvUnit bufa[NvUnits<HALF>::kPerThread], bufb[NvUnits<HALF>::kPerThread];
+  conv_load_nv<HALF>(bufa, rowptr, ct, 0);
+  for (int k = 0; k < nt; k += 2) {
+    if (k + 1 < nt) conv_load_nv<HALF>(bufb, rowptr, ct, k + 1);
+    if (!conv_store_nv<HALF>(bufa, a, ct, lane, k, LAT, lat_full, lat_free)) { ok = false; return; }
+    if (k + 1 >= nt) break;
+    if (k + 2 < nt) conv_load_nv<HALF>(bufa, rowptr, ct, k + 2);
+    if (!conv_store_nv<HALF>(bufb, a, ct, lane, k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
   }
 }
 
@@ -278,7 +395,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
         if (sidx >= 0 && sidx < L) {
           const int pg = a.block_table[size_t(b) * a.max_pages + sidx / kPage];
           if (pg >= 0 && pg < a.num_pages)
-            rp = a.lat_pool + size_t(pg) * a.lat_stride + size_t(sidx % kPage) * kLatRowFp8;
+            rp = a.lat_pool + size_t(pg) * a.lat_stride + size_t(sidx % kPage) * a.lat_row;
           else if (half == 0)
             atomicOr(a.err, DSA_DEVERR_BLOCK_TABLE);
         } else if (sidx != -1 && half == 0) {
@@ -290,10 +407,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
       if (lane == 0) reinterpret_cast<uint32_t*>(vmask)[jj >> 5] = m;
     }
     ptx::named_bar_sync(1, 128);
-    if (half == 0)
+    if (a.lat_nvfp4) {
+      if (half == 0)
+        converter_role_nv<0>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
+      else
+        converter_role_nv<1>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
+    } else if (half == 0) {
       converter_role<20>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
-    else
+    } else {
       converter_role<16>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
+    }
   } else if (warp < 3) {
     // ------------------------------------------------------------ softmax / epilogue
     const int h = warp * 32 + lane;
@@ -407,7 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
       }
       ptx::fence_proxy_async_smem();
       ptx::bulk_store(op + size_t(h) * kDNope, orow_s, 256 * 4);
-      ptx::bulk_store_commit_wait();
+      ptx::bulk_store_commit_wait_read();
       if (half == 0) lp[h] = l > 0.f ? (m_use + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
   }
@@ -490,6 +613,8 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   t.topk_idx = topk_idx;
   t.lat_pool = static_cast<const uint8_t*>(lat_pool);
   t.lat_stride = p.lat_page_stride;
+  t.lat_nvfp4 = p.lat_fmt == DSA_LAT_NVFP4_352;
+  t.lat_row = t.lat_nvfp4 ? kDNope / 2 + kDNope / 16 + kDRope : kLatRowFp8;
   t.max_pages = p.max_pages_per_req;
   t.num_pages = p.num_pages;
   t.n_q = p.n_q;

@@ -31,6 +31,12 @@ latent values, q, plants):
   at the cell's midpoint), so the code histogram is that of E4M3(N(0, 1)) to
   within 2**-16 in probability.
 * key scales: U(0.5, 2) in fp32.
+* MXFP4 keys and NVFP4 latents: N(0, 1) values quantised block by block (MXFP4
+  shared exponent floor(log2 amax) - 2, NVFP4 block scale E4M3(amax / 6), E2M1
+  round-half-even, saturating). These pools are drawn in chunks of pages, each
+  chunk from its own PCG64 stream seeded by (seed, 1 for keys / 2 for latents,
+  chunk index), so that they can be filled by several threads; the main stream
+  then skips them.
 """
 from __future__ import annotations
 
@@ -97,6 +103,37 @@ def encode_e2m1(x: np.ndarray) -> np.ndarray:
     code = np.where(pick_hi, hi, lo).astype(np.uint8)
     code = np.where(a == 0, 0, code).astype(np.uint8)
     return code | np.where(np.signbit(x) & (code != 0), 0x8, 0).astype(np.uint8)
+
+
+def encode_e2m1_fast(x: np.ndarray) -> np.ndarray:
+    """``encode_e2m1`` in float32 arithmetic, for the big pools: the E2M1 grid has
+    steps of 1/2 below 2, 1 below 4 and 2 up to 6, so the nearest point is a
+    round-half-even of the value on that segment's scale (ties go to the even code,
+    as in ``encode_e2m1``; the tests compare the two on every midpoint)."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.minimum(np.abs(x), np.float32(6.0))
+    k1 = np.rint(a * np.float32(2.0))
+    k2 = np.rint(a) + np.float32(2.0)
+    k3 = np.rint(a * np.float32(0.5)) + np.float32(4.0)
+    code = np.where(a < 2, k1, np.where(a < 4, k2, k3)).astype(np.uint8)
+    return code | np.where(np.signbit(x) & (code != 0), np.uint8(8), np.uint8(0))
+
+
+def _chunked(seed: int, tag: int, n: int, step: int, fill) -> None:
+    """Call ``fill(rng, lo, hi)`` for every chunk [lo, hi) of range(n), each with
+    its own PCG64 stream seeded by (seed, tag, chunk index), on a thread pool (the
+    result does not depend on the number of threads)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    starts = list(range(0, n, step))
+
+    def one(i):
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, i])))
+        fill(rng, starts[i], min(n, starts[i] + step))
+
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(one, range(len(starts))))
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -202,7 +239,7 @@ def _quantise_mxfp4_keys(x: np.ndarray) -> np.ndarray:
     amax = np.abs(blk).max(axis=2)
     e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, -127)
     e = np.clip(e, -127, 127)
-    codes = encode_e2m1(blk / (2.0 ** e)[:, :, None]).reshape(n, 128)
+    codes = encode_e2m1_fast((blk / (2.0 ** e)[:, :, None]).astype(np.float32)).reshape(n, 128)
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
     scales = (e + 127).astype(np.uint8)
     return np.concatenate([packed, scales], axis=1)
@@ -216,7 +253,7 @@ def _quantise_nvfp4_latents(x: np.ndarray) -> np.ndarray:
     sc_code = encode_e4m3(amax / 6.0)
     sc_val = _E4M3_POS[sc_code & 0x7F]
     safe = np.where(sc_val > 0, sc_val, 1.0)
-    codes = encode_e2m1(nope / safe[:, :, None]).reshape(n, D_NOPE)
+    codes = encode_e2m1_fast((nope / safe[:, :, None]).astype(np.float32)).reshape(n, D_NOPE)
     codes = np.where(np.repeat(sc_val > 0, 16, axis=1), codes, 0).astype(np.uint8)
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
     rope = encode_e4m3(x[:, D_NOPE:])
@@ -280,12 +317,13 @@ def make_inputs(
         scales = rng.uniform(0.5, 2.0, (num_pages, page_size)).astype(np.float32)
         key_pool[:, page_size * IDX_DIM:page_size * kb] = scales.view(np.uint8).reshape(num_pages, page_size * 4)
     elif key_fmt == "mxfp4":
-        for p0 in range(0, num_pages, 512):
-            p1 = min(num_pages, p0 + 512)
-            x = rng.standard_normal(((p1 - p0) * page_size, IDX_DIM), dtype=np.float32)
+        def fill_keys(r, p0, p1):
+            x = r.standard_normal(((p1 - p0) * page_size, IDX_DIM), dtype=np.float32)
             enc = _quantise_mxfp4_keys(x).reshape(p1 - p0, page_size, 68)
             key_pool[p0:p1, :page_size * 64] = enc[:, :, :64].reshape(p1 - p0, -1)
             key_pool[p0:p1, page_size * 64:page_size * 68] = enc[:, :, 64:].reshape(p1 - p0, -1)
+
+        _chunked(seed, 1, num_pages, 256, fill_keys)
     else:
         raise ValueError(key_fmt)
 
@@ -296,10 +334,11 @@ def make_inputs(
             vals = sample_e4m3_normal(rng, num_pages * page_size * D_QK)
             lat_pool[:, :page_size * D_QK] = vals.reshape(num_pages, page_size * D_QK)
     elif lat_fmt == "nvfp4":
-        for p0 in range(0, num_pages, 256):
-            p1 = min(num_pages, p0 + 256)
-            x = rng.standard_normal(((p1 - p0) * page_size, D_QK), dtype=np.float32)
+        def fill_lat(r, p0, p1):
+            x = r.standard_normal(((p1 - p0) * page_size, D_QK), dtype=np.float32)
             lat_pool[p0:p1, :page_size * lb] = _quantise_nvfp4_latents(x).reshape(p1 - p0, -1)
+
+        _chunked(seed, 2, num_pages, 64, fill_lat)
     else:
         raise ValueError(lat_fmt)
 

@@ -98,13 +98,19 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert st == dsa.DSA_ERR_INVALID
 
 
-def test_fp4_formats_report_unsupported_until_built(lib):
+def test_fp4_formats_take_their_own_page_strides(lib):
+    """MXFP4 keys are 68 B and NVFP4 latents 352 B per token: a page stride below
+    64 rows of the format (or not a multiple of 16 B) is rejected."""
     p = _params(key_fmt=dsa.DSA_KEY_MXFP4_68, key_page_stride=64 * 68,
                 lat_fmt=dsa.DSA_LAT_NVFP4_352, lat_page_stride=64 * 352)
-    try:
-        assert dsa.workspace_size(p) > 0
-    except dsa.DSAError as e:
-        assert e.status == dsa.DSA_ERR_UNSUPPORTED
+    assert dsa.workspace_size(p) > 0
+    for kw in (dict(key_page_stride=64 * 68 - 16), dict(lat_page_stride=64 * 352 - 16),
+               dict(key_page_stride=64 * 68 + 8)):
+        q = _params(**{**dict(key_fmt=dsa.DSA_KEY_MXFP4_68, key_page_stride=64 * 68,
+                              lat_fmt=dsa.DSA_LAT_NVFP4_352, lat_page_stride=64 * 352), **kw})
+        with pytest.raises(dsa.DSAError) as e:
+            dsa.workspace_size(q)
+        assert e.value.status == dsa.DSA_ERR_INVALID
 
 
 def test_library_missing_fails_loudly(monkeypatch, tmp_path):

@@ -14,7 +14,7 @@ import gen
 from oracle import dsa as O
 
 from dsa_testlib import (Dev, bf16_to_np, check_attention, check_scores, check_selection,
-                         rows_scores_oracle)
+                         rows_error_scale, rows_scores_oracle, score_error_scale)
 
 pytestmark = pytest.mark.gpu
 
@@ -47,8 +47,9 @@ def test_indexer_scores_small(case):
     d = Dev(inp)
     sc = d.scores().cpu().numpy()
     ref = rows_scores_oracle(inp)
+    es = rows_error_scale(inp)
     for r, rs in ref.items():
-        check_scores(sc[r, :len(rs)], rs)
+        check_scores(sc[r, :len(rs)], rs, es[r])
         # entries past L are untouched
         assert np.isnan(sc[r, len(rs):d.cap]).all()
 
@@ -169,7 +170,7 @@ def test_decode_end_to_end_small(case):
     res = O.decode(inp)
     for (b, t), r in res.items():
         row = b * inp.n_q + t
-        check_selection(idx[row], r["idx"], r["scores"], inp.topk)
+        check_selection(idx[row], r["idx"], r["scores"], inp.topk, score_error_scale(inp, b, t))
     # attention over the GPU's own (validated) selection
     ro, rl = _oracle_mla_all(inp, idx)
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
@@ -226,6 +227,105 @@ def test_device_error_word():
     assert dsa.get_device_error(d.ws) & dsa.DSA_DEVERR_TOPK_INDEX
 
 
+# ----------------------------------------------------------------------------- FP4 formats
+
+SMALL_FP4 = [
+    # (batch, n_q, ctx, bt_mode, holes, key_pad, lat_pad, key_fmt, lat_fmt)
+    (3, 1, [4096 + 37, 2049, 300], "permuted", True, 0, 0, "mxfp4", "nvfp4"),
+    (2, 6, [9000, 700], "permuted", False, 16, 32, "mxfp4", "fp8"),
+    (2, 1, [3000, 65], "identity", False, 0, 16, "fp8", "nvfp4"),
+]
+
+
+@functools.lru_cache(maxsize=None)
+def _small_fp4(i):
+    b, nq, ctx, mode, holes, kp, lp, kf, lf = SMALL_FP4[i]
+    return gen.make_inputs(b, nq, ctx, seed=200 + i, bt_mode=mode, holes=holes, key_page_pad=kp,
+                           lat_page_pad=lp, key_fmt=kf, lat_fmt=lf, signed_w=i == 1)
+
+
+def _mx_block_exponent_spread(inp):
+    """Largest spread of a token's four E8M0 exponents (the MXFP4 key path is exact up to 8)."""
+    e = inp.key_pool[:, 64 * 64:64 * 68].reshape(-1, 4).astype(np.int64)
+    return int((e.max(axis=1) - e.min(axis=1)).max())
+
+
+@pytest.mark.parametrize("case", range(len(SMALL_FP4)))
+def test_fp4_indexer_scores_small(case):
+    inp = _small_fp4(case)
+    if inp.key_fmt == "mxfp4":
+        assert _mx_block_exponent_spread(inp) <= 8
+    d = Dev(inp)
+    sc = d.scores().cpu().numpy()
+    es = rows_error_scale(inp)
+    for r, rs in rows_scores_oracle(inp).items():
+        check_scores(sc[r, :len(rs)], rs, es[r])
+        assert np.isnan(sc[r, len(rs):d.cap]).all()
+
+
+@pytest.mark.parametrize("case", range(len(SMALL_FP4)))
+def test_fp4_sparse_mla_over_oracle_indices(case):
+    import torch
+
+    inp = _small_fp4(case)
+    d = Dev(inp)
+    ref = {r: O.topk_select(s, 2048) for r, s in rows_scores_oracle(inp).items()}
+    idx = np.stack([ref[r] for r in range(d.rows)])
+    out, lse = d.mla(torch.from_numpy(idx).cuda())
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+
+
+@pytest.mark.parametrize("case", range(len(SMALL_FP4)))
+def test_fp4_decode_end_to_end_small(case):
+    inp = _small_fp4(case)
+    d = Dev(inp)
+    out, lse, idx = d.decode()
+    idx = idx.cpu().numpy()
+    for (b, t), r in O.decode(inp).items():
+        check_selection(idx[b * inp.n_q + t], r["idx"], r["scores"], inp.topk, score_error_scale(inp, b, t))
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+
+
+def test_mxfp4_key_with_spread_exponents_stays_close():
+    """A token whose block exponents spread past 8 loses only what E4M3 cannot
+    hold below 2^-9 of its largest block: its score stays within 1e-3 of the
+    exact one when the small blocks' share is tiny."""
+    inp = gen.make_inputs(1, 1, [640], seed=210, key_fmt="mxfp4", lat_fmt="fp8")
+    pool = inp.key_pool
+    # token 5: blocks 1..3 get exponents 12 below block 0
+    e = pool[0, 64 * 64 + 4 * 5:64 * 64 + 4 * 5 + 4].astype(np.int64)
+    e[1:] = np.maximum(e[0] - 12, 0)
+    pool[0, 64 * 64 + 4 * 5:64 * 64 + 4 * 5 + 4] = e.astype(np.uint8)
+    d = Dev(inp)
+    sc = d.scores().cpu().numpy()
+    ref = rows_scores_oracle(inp)[0]
+    check_scores(sc[0, :len(ref)], ref, score_error_scale(inp, 0, 0))
+
+
+@pytest.mark.slow
+def test_workload_fp4_decode():
+    """32 requests x 6 causal query rows at 256K context with MXFP4 keys and NVFP4
+    latents, in the benchmark's launch configuration, checked on sampled rows."""
+    inp = _workload("b32x6_ctx256k_fp4")
+    assert _mx_block_exponent_spread(inp) <= 8
+    d = Dev(inp)
+    out, lse, idx = d.decode()
+    sc = d.scores().cpu().numpy()
+    idx, out, lse = idx.cpu().numpy(), bf16_to_np(out), lse.cpu().numpy()
+    for b in (0, 31):
+        res = O.decode(inp, requests=[b])
+        for t in (0, 5):
+            r = res[(b, t)]
+            row = b * inp.n_q + t
+            es = score_error_scale(inp, b, t)
+            check_scores(sc[row, :len(r["scores"])], r["scores"], es)
+            check_selection(idx[row], r["idx"], r["scores"], inp.topk, es)
+            o2, l2 = O.sparse_mla(inp, b, t, idx[row])
+            check_attention(out[row][None], lse[row][None], o2[None], l2[None])
+
+
 # ----------------------------------------------------------------------------- the five workloads
 
 def plant_tau_ties(inp, b, rng, n_exact=16, n_near=16):
@@ -276,8 +376,9 @@ def test_workload_decode(name):
     idx, out, lse = idx.cpu().numpy(), bf16_to_np(out), lse.cpu().numpy()
     for b in WL_ROWS[name]:
         r = O.decode(inp, requests=[b])[(b, 0)]
-        check_scores(sc[b, :len(r["scores"])], r["scores"])
-        nd = check_selection(idx[b], r["idx"], r["scores"], inp.topk)
+        es = score_error_scale(inp, b, 0)
+        check_scores(sc[b, :len(r["scores"])], r["scores"], es)
+        nd = check_selection(idx[b], r["idx"], r["scores"], inp.topk, es)
         # top-k alone on the oracle's own scores is bit-exact
         ti, _ = d.topk(np.pad(r["scores"], (0, d.cap - len(r["scores"])))[None].repeat(inp.batch, 0))
         assert np.array_equal(ti.cpu().numpy()[b], r["idx"])

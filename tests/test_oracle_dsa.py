@@ -274,6 +274,16 @@ def test_generator_fp4_round_trip_error():
     assert 0.5 < np.abs(k).std() < 2.0 and 0.5 < np.abs(c[:, :512]).std() < 2.0
 
 
+def test_generator_fast_e2m1_encoder_matches_reference():
+    rng = np.random.default_rng(5)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mids = (grid[1:] + grid[:-1]) / 2
+    x = np.concatenate([rng.standard_normal(200000) * 3, mids, -mids, grid, -grid,
+                        np.nextafter(mids, 0), np.nextafter(mids, 9), [7.0, -7.0, 1e30, -0.0]])
+    x = x.astype(np.float32)
+    assert np.array_equal(gen.encode_e2m1_fast(x), gen.encode_e2m1(x))
+
+
 # ----------------------------------------------------------------------------- byte model
 
 def test_byte_model_article_numbers():
