@@ -21,9 +21,9 @@ DSA_LAT_FP8_576, DSA_LAT_NVFP4_352 = 0, 1
 DSA_EMIT_PHYS_ROWS = 0x1
 DSA_DEVERR_BLOCK_TABLE, DSA_DEVERR_CTX, DSA_DEVERR_TOPK_INDEX = 0x1, 0x2, 0x4
 
-# Kernels one dsa_decode launches (q quantisation, indexer, 5 top-k passes,
-# sparse MLA, split combine); kept in step with csrc/.
-KERNELS_PER_DECODE = 9
+# Kernels one dsa_decode launches (q quantisation, indexer, 3 top-k passes:
+# sample / filter / select, sparse MLA, split combine); kept in step with csrc/.
+KERNELS_PER_DECODE = 7
 
 EXPORTS = (
     "dsa_workspace_size",
