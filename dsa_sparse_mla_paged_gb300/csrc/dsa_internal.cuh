@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dsa.h"
 
 namespace dsa {
@@ -86,6 +88,36 @@ __device__ __forceinline__ int row_visible_len(const int32_t* ctx_lens, int b, i
     return -1;
   }
   return c - n_q + t + 1;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialisation, so the next kernel in the stream is scheduled as soon as the
+// current one lets it (pdl_trigger, or the exit of all its CTAs) instead of
+// after its completion and memory flush. Each kernel does only on-chip set-up
+// (shared memory, barriers, TMEM) before pdl_wait, which returns once every
+// earlier grid in the stream has completed and its memory is visible; no
+// global access comes before it. Only the small query-quantisation kernel
+// triggers early (the scorer's prologue then overlaps it); a waiting grid that
+// shared SMs with a long-running one slowed that one down (measured), so the
+// others let their dependents in when they exit.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Number of SMs of the current device.

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
                                                           const int32_t* __restrict__ ctx_lens, int batch,
                                                           int n_q, int cap, int* __restrict__ tile_prefix,
                                                           int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (row == gridDim.x - 1) {
@@ -92,11 +94,10 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
 
 cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
                                const float* w, const int32_t* ctx_lens, cudaStream_t st) {
-  idx_q_quant_kernel<<<L.rows + 1, 128, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(q_idx), w, reinterpret_cast<uint8_t*>(ws + L.q8),
-      reinterpret_cast<float*>(ws + L.wq), ctx_lens, p.batch, p.n_q, L.cap,
-      reinterpret_cast<int*>(ws + L.tiles), reinterpret_cast<int*>(ws + L.err));
-  return cudaGetLastError();
+  return launch_pdl(idx_q_quant_kernel, dim3(L.rows + 1), dim3(128), 0, st,
+                    static_cast<const __nv_bfloat16*>(q_idx), w, reinterpret_cast<uint8_t*>(ws + L.q8),
+                    reinterpret_cast<float*>(ws + L.wq), ctx_lens, p.batch, p.n_q, L.cap,
+                    reinterpret_cast<int*>(ws + L.tiles), reinterpret_cast<int*>(ws + L.err));
 }
 
 // ---------------------------------------------------------------------------
@@ -318,9 +319,6 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long T = a.tile_prefix[a.batch - 1];
-  const long long t_begin = T * blockIdx.x / gridDim.x;
-  const long long t_end = T * (blockIdx.x + 1) / gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) { ptx::mbar_init(full + i, kMx ? 4 : 1); ptx::mbar_init(empty + i, 1 + 4); }
@@ -338,6 +336,10 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the tile plan and the query come from the previous kernel
+  const long long T = a.tile_prefix[a.batch - 1];
+  const long long t_begin = T * blockIdx.x / gridDim.x;
+  const long long t_end = T * (blockIdx.x + 1) / gridDim.x;
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -679,11 +681,8 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   // enough tiles for every SM is the common case; with fewer, one CTA per tile
   const long long max_tiles = (long long)p.batch * ((L.cap + kTileTok - 1) / kTileTok);
   const int grid = int(std::min<long long>(sm_count(), std::max<long long>(1, max_tiles)));
-  if (mx)
-    indexer_tc_kernel<true><<<grid, kMxThreads, smem, st>>>(kmap, qmap, a);
-  else
-    indexer_tc_kernel<false><<<grid, kTcThreads, smem, st>>>(kmap, qmap, a);
-  return cudaGetLastError();
+  if (mx) return launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(kMxThreads), smem, st, kmap, qmap, a);
+  return launch_pdl(indexer_tc_kernel<false>, dim3(grid), dim3(kTcThreads), smem, st, kmap, qmap, a);
 }
 
 }  // namespace dsa

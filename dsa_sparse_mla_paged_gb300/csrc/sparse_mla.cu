@@ -276,6 +276,7 @@ __device__ void converter_role_nv(const MlaTc& a, int ct, int lane, int nt, cons
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
     sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, MlaTc a) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = sm;
@@ -555,6 +556,7 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* 
                                                                    const float* __restrict__ lpart, int splits,
                                                                    __nv_bfloat16* __restrict__ out,
                                                                    float* __restrict__ lse) {
+  pdl_wait();
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y * kCombHeads + (threadIdx.x >> 7);
@@ -630,11 +632,11 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kTcMlaSmem));
   if (e != cudaSuccess) return e;
-  dim3 grid(2 * L.splits, L.rows);
-  sparse_mla_tc_kernel<<<grid, kTcMlaThreads, kTcMlaSmem, st>>>(qmap, t);
-  dim3 g2(L.rows, kHeads / kCombHeads);
-  mla_combine_kernel<<<g2, kCombThreads, 0, st>>>(t.opart, t.lpart, L.splits, static_cast<__nv_bfloat16*>(out), lse);
-  return cudaGetLastError();
+  e = launch_pdl(sparse_mla_tc_kernel, dim3(2 * L.splits, L.rows), dim3(kTcMlaThreads), kTcMlaSmem, st, qmap, t);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(mla_combine_kernel, dim3(L.rows, kHeads / kCombHeads), dim3(kCombThreads), 0, st,
+                    static_cast<const float*>(t.opart), static_cast<const float*>(t.lpart), int(L.splits),
+                    static_cast<__nv_bfloat16*>(out), lse);
 }
 
 }  // namespace dsa

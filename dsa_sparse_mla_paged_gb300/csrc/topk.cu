@@ -195,6 +195,7 @@ constexpr int kSampleThreads = 1024;
 constexpr int kSamplePer = kSampleMax / kSampleThreads;  // 8
 
 __global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(TopkArgs a) {
+  pdl_wait();
   __shared__ int smw[64];
   __shared__ int hist[2048];
   const Row w = row_of(a, blockIdx.x);
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(TopkArgs a)
 
 // ---------------------------------------------------------------- filter
 __global__ void __launch_bounds__(kFiltThreads) topk_filter_kernel(TopkArgs a) {
+  pdl_wait();
   __shared__ int smw[8];
   __shared__ int s_base;
   const Row w = row_of(a, blockIdx.y);
@@ -342,6 +344,7 @@ __device__ void select_whole_row(const TopkArgs& a, const Row& w, int* hist, int
 constexpr size_t kSelSmem = size_t(kCandCap) * 8 + 2048 * 4;
 
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(TopkArgs a) {
+  pdl_wait();
   extern __shared__ uint32_t sel_smem[];
   uint32_t* ckey = sel_smem;                                  // [kCandCap]
   int* cidx = reinterpret_cast<int*>(sel_smem + kCandCap);    // [kCandCap]
@@ -466,12 +469,12 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   a.err = reinterpret_cast<int*>(ws + L.err);
   a.topk_idx = topk_idx;
   a.phys_rows = phys_rows;
-  topk_sample_kernel<<<L.rows, kSampleThreads, 0, st>>>(a);
-  topk_filter_kernel<<<dim3(L.max_chunks, L.rows), kFiltThreads, 0, st>>>(a);
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSelSmem));
-  if (e != cudaSuccess) return e;
-  topk_select_kernel<<<L.rows, kSelThreads, kSelSmem, st>>>(a);
-  return cudaGetLastError();
+  if (e == cudaSuccess) e = launch_pdl(topk_sample_kernel, dim3(L.rows), dim3(kSampleThreads), 0, st, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(topk_filter_kernel, dim3(L.max_chunks, L.rows), dim3(kFiltThreads), 0, st, a);
+  if (e == cudaSuccess) e = launch_pdl(topk_select_kernel, dim3(L.rows), dim3(kSelThreads), kSelSmem, st, a);
+  return e;
 }
 
 }  // namespace dsa
