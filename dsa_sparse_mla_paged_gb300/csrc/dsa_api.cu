@@ -82,7 +82,8 @@ dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, c
   if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
   char* w8 = static_cast<char*>(ws);
   cudaError_t e = launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
-  if (e == cudaSuccess) e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, score_stride, stream);
+  if (e == cudaSuccess)
+    e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, score_stride, stream);
   return cuda_status(e);
 }
 

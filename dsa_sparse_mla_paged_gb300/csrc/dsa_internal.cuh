@@ -79,6 +79,14 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   return L;
 }
 
+// Order-preserving 32-bit key of an fp32 score (larger score -> larger key;
+// -0 and +0 share one key). Top-k compares scores only through this key.
+__device__ __forceinline__ uint32_t score_order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Visible length of row (b, t): ctx_b - n_q + t + 1, or -1 when ctx_b is invalid.
 __device__ __forceinline__ int row_visible_len(const int32_t* ctx_lens, int b, int t, int n_q,
                                                int cap, int* err) {

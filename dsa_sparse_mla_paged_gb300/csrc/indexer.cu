@@ -225,12 +225,21 @@ struct EpiState {
 // thread's token row and store the score, then step to the next block.
 __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
                                           int lane, TileWalk& w, EpiState& e, int& cur_b, int& ctx,
-                                          float (&wl)[kMaxNQ]) {
+                                          float (&wl)[kMaxNQ], float (&wr)[kIdxHeads]) {
   if (e.t == 0 && w.b != cur_b) {
     cur_b = w.b;
     ctx = a.ctx_lens[w.b];
+    if (a.n_q == 1) {
+      const float4* src = reinterpret_cast<const float4*>(a.wq + size_t(w.b) * kIdxHeads);
 #pragma unroll
-    for (int t = 0; t < kMaxNQ; ++t) wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
+      for (int i = 0; i < kIdxHeads / 4; ++i) {
+        const float4 f = src[i];
+        wr[4 * i] = f.x; wr[4 * i + 1] = f.y; wr[4 * i + 2] = f.z; wr[4 * i + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < kMaxNQ; ++t) wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
+    }
   }
   float scale = sc[0], wt = wl[0];
 #pragma unroll
@@ -239,9 +248,19 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
 #pragma unroll
   for (int t = 1; t < kMaxNQ; ++t)
     if (e.t == t) wt = wl[t];
-  float sum = 0.f;
+  // four independent partial sums (heads h = 4i + j), added pairwise: a short
+  // dependency chain per block. One query row: every thread holds all 32 head
+  // weights; several rows: lane h holds w'_h of each row and shares it.
+  float part[4] = {0.f, 0.f, 0.f, 0.f};
+  if (a.n_q == 1) {
 #pragma unroll
-  for (int h = 0; h < kIdxHeads; ++h) sum = fmaf(__shfl_sync(0xffffffffu, wt, h), fmaxf(scale * v[h], 0.f), sum);
+    for (int h = 0; h < kIdxHeads; ++h) part[h & 3] = fmaf(wr[h], fmaxf(scale * v[h], 0.f), part[h & 3]);
+  } else {
+#pragma unroll
+    for (int h = 0; h < kIdxHeads; ++h)
+      part[h & 3] = fmaf(__shfl_sync(0xffffffffu, wt, h), fmaxf(scale * v[h], 0.f), part[h & 3]);
+  }
+  const float sum = (part[0] + part[1]) + (part[2] + part[3]);
   const int tok = w.j * kTileTok + rowt;
   const int Lt = ctx - a.n_q + e.t + 1;
   if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + e.t) * a.score_stride + tok] = sum;
@@ -360,6 +379,9 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
       }
       int rs = 0;         // MXFP4 raw slot
       uint32_t rph = 0;   // its phase bit
+      // keys are read once: keep them from pushing the score rows (read next
+      // by the top-k passes) out of L2
+      const uint64_t pol = ptx::policy_evict_first();
       TileWalk base;
       walk_start(a, t_begin, base);
       int base_np = (a.ctx_lens[base.b] + kPage - 1) / kPage;
@@ -391,8 +413,8 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
               if (!ok) break;
               if (lane < 1 + two) {
                 const int pg = page_or_zero(a, lane ? pg1 : pg0);
-                ptx::bulk_load(raw + size_t(rs) * kMxRawTile + lane * kMxPageBytes,
-                               a.key_pool + size_t(pg) * a.key_page_stride, kMxPageBytes, rfull + rs);
+                ptx::bulk_load_hint(raw + size_t(rs) * kMxRawTile + lane * kMxPageBytes,
+                                    a.key_pool + size_t(pg) * a.key_page_stride, kMxPageBytes, rfull + rs, pol);
               }
               if (++rs == R) { rs = 0; rph ^= 1u; }
             }
@@ -421,14 +443,14 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
               uint8_t* kdst = keys + (size_t(s) * G + lane) * kKeyTileBytes;
               float* sdst = scl + (size_t(s) * G + lane) * kTileTok;
               const int p0 = page_or_zero(a, pg0);
-              ptx::tma_load_3d(kdst, &kmap, full + s, 0, 0, p0);
-              ptx::bulk_load(sdst, a.key_pool + size_t(p0) * a.key_page_stride + kPage * kIdxDim, kPage * 4,
-                             full + s);
+              ptx::tma_load_3d_hint(kdst, &kmap, full + s, 0, 0, p0, pol);
+              ptx::bulk_load_hint(sdst, a.key_pool + size_t(p0) * a.key_page_stride + kPage * kIdxDim, kPage * 4,
+                                  full + s, pol);
               if (two) {
                 const int p1 = page_or_zero(a, pg1);
-                ptx::tma_load_3d(kdst + kPage * kIdxDim, &kmap, full + s, 0, 0, p1);
-                ptx::bulk_load(sdst + kPage, a.key_pool + size_t(p1) * a.key_page_stride + kPage * kIdxDim,
-                               kPage * 4, full + s);
+                ptx::tma_load_3d_hint(kdst + kPage * kIdxDim, &kmap, full + s, 0, 0, p1, pol);
+                ptx::bulk_load_hint(sdst + kPage, a.key_pool + size_t(p1) * a.key_page_stride + kPage * kIdxDim,
+                                    kPage * 4, full + s, pol);
               }
             }
           }
@@ -531,6 +553,7 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
       walk_start(a, t_begin, w);
       int cur_b = -1, ctx = 0;
       float wl[kMaxNQ];  // lane h holds w'_h of each query row of the current request
+      float wr[kIdxHeads];  // one query row: all head weights
       int s = 0, acc = 0;
       uint32_t aph = 0;
       for (long long t0 = t_begin; t0 < t_end; t0 += G) {
@@ -555,11 +578,11 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < nb; c += 2) {
           if (c + 1 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 1) * 32), vb);
-          epi_block(a, va, sc, rowt, lane, w, e, cur_b, ctx, wl);
+          epi_block(a, va, sc, rowt, lane, w, e, cur_b, ctx, wl, wr);
           if (c + 1 < nb) {
             ptx::tmem_ld_wait(vb);
             if (c + 2 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 2) * 32), va);
-            epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ctx, wl);
+            epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ctx, wl, wr);
             if (c + 2 < nb) ptx::tmem_ld_wait(va);
           }
         }

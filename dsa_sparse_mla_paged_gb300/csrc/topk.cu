@@ -45,11 +45,7 @@ struct TopkArgs {
   int32_t* phys_rows;
 };
 
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;  // -0 == +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+__device__ __forceinline__ uint32_t order_key(float f) { return score_order_key(f); }
 
 // Exclusive block scan of one int per thread (NT threads); *total gets the sum.
 template <int NT>
@@ -121,12 +117,18 @@ __device__ __forceinline__ int block_sum(int v, int* smw) {
 // The k-th largest (1-based) of the keys held by the CTA (PER per thread; key
 // 0 marks an empty slot and is never counted; 1 <= k <= number of keys).
 // The bits all keys share (from the block's min and max key) are skipped; the
-// rest are radix-selected 11 bits per pass with a shared histogram of 2048 bins,
-// so bins stay spread out even when the values crowd into a narrow range.
+// rest are radix-selected 11 bits per pass with a shared histogram of 2048 bins
+// (two buffers alternate, so `hist` holds 4096 ints and a buffer is cleared
+// while the other fills). Per pass: histogram; per-warp sums of the bins from
+// the top (each thread owns nb / NT bins); every warp scans the warp sums and
+// the thread holding the k-th key finds its bin: three block barriers.
 template <int NT, int PER>
 __device__ uint32_t block_kth_key(const uint32_t (&keys)[PER], int k, int* hist, int* smw) {
   constexpr int NW = NT / 32;
+  constexpr int kBins = 2048;
+  constexpr int kMaxPer = (kBins + NT - 1) / NT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ int s_sel[2];
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
   for (int i = 0; i < PER; ++i)
@@ -134,58 +136,77 @@ __device__ uint32_t block_kth_key(const uint32_t (&keys)[PER], int k, int* hist,
   mn = __reduce_min_sync(0xffffffffu, mn);
   mx = __reduce_max_sync(0xffffffffu, mx);
   if (lane == 0) { smw[warp] = int(mn); smw[NW + warp] = int(mx); }
+  for (int i = threadIdx.x; i < kBins; i += NT) hist[i] = 0;
   __syncthreads();
   mn = lane < NW ? uint32_t(smw[lane]) : 0xFFFFFFFFu;
   mx = lane < NW ? uint32_t(smw[NW + lane]) : 0u;
   mn = __reduce_min_sync(0xffffffffu, mn);
   mx = __reduce_max_sync(0xffffffffu, mx);
-  __syncthreads();
   const uint32_t diff = mn ^ mx;
   if (diff == 0) return mx;
-  int lo_bit = 32 - __clz(diff);                  // bits [lo_bit, 32) are common to all keys
+  int lo_bit = 32 - __clz(diff);  // bits [lo_bit, 32) are common to all keys
   uint32_t prefix = lo_bit >= 32 ? 0u : (mx >> lo_bit) << lo_bit;
   int kk = k;
-  __shared__ int s_sel[2];
+  int buf = 0;
+  __syncthreads();  // every warp has read smw before it is reused below
   while (lo_bit > 0) {
     const int width = min(11, lo_bit);
     const int sh = lo_bit - width;
     const int nb = 1 << width;
-    for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
-    __syncthreads();
+    int* H = hist + buf * kBins;
+    int* Hn = hist + (buf ^ 1) * kBins;
+    for (int i = threadIdx.x; i < kBins; i += NT) Hn[i] = 0;  // the next pass's buffer
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const uint32_t u = keys[i];
       const bool match = u != 0u && (lo_bit >= 32 || (u >> lo_bit) == (prefix >> lo_bit));
-      if (match) atomicAdd(&hist[(u >> sh) & uint32_t(nb - 1)], 1);
+      if (match) atomicAdd(&H[(u >> sh) & uint32_t(nb - 1)], 1);
     }
     __syncthreads();
-    // bins from the top: thread t owns bins nb-1-t*per .. (per >= 1 when nb >= NT, else one or none)
-    const int per = (nb + NT - 1) / NT;
-    int cnt = 0;
-    for (int j = 0; j < per; ++j) {
-      const int bin = nb - 1 - int(threadIdx.x) * per - j;
-      if (bin >= 0) cnt += hist[bin];
+    // thread t owns bins nb-1-t*per .. nb-per-t*per (from the top)
+    const int per = nb >= NT ? nb / NT : 1;
+    const int top = nb - 1 - int(threadIdx.x) * per;
+    int cnt[kMaxPer];
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j) {
+      cnt[j] = (j < per && top - j >= 0) ? H[top - j] : 0;
+      c += cnt[j];
     }
-    int tot;
-    const int before = block_excl_scan<NT>(cnt, &tot, smw);
-    if (before < kk && kk <= before + cnt) {
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) smw[warp] = incl;
+    __syncthreads();
+    int wsum = lane < NW ? smw[lane] : 0;  // warp totals, scanned in every warp
+    int wincl = wsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+      if (lane >= o) wincl += y;
+    }
+    const int base = __shfl_sync(0xffffffffu, wincl - wsum, warp);
+    const int before = base + incl - c;
+    if (before < kk && kk <= before + c) {
       int cum = before;
-      for (int j = 0; j < per; ++j) {
-        const int bin = nb - 1 - int(threadIdx.x) * per - j;
-        if (bin < 0) break;
-        if (kk <= cum + hist[bin]) {
-          s_sel[0] = bin;
+#pragma unroll
+      for (int j = 0; j < kMaxPer; ++j) {
+        if (j < per && kk <= cum + cnt[j]) {
+          s_sel[0] = top - j;
           s_sel[1] = kk - cum;
           break;
         }
-        cum += hist[bin];
+        cum += cnt[j];
       }
     }
     __syncthreads();
     prefix |= uint32_t(s_sel[0]) << sh;
     kk = s_sel[1];
     lo_bit = sh;
-    __syncthreads();
+    buf ^= 1;
   }
   return prefix;
 }
@@ -194,10 +215,10 @@ __device__ uint32_t block_kth_key(const uint32_t (&keys)[PER], int k, int* hist,
 constexpr int kSampleThreads = 1024;
 constexpr int kSamplePer = kSampleMax / kSampleThreads;  // 8
 
-__global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kSampleThreads, 1) topk_sample_kernel(TopkArgs a) {
   pdl_wait();
   __shared__ int smw[64];
-  __shared__ int hist[2048];
+  __shared__ int hist[4096];
   const Row w = row_of(a, blockIdx.x);
   int* st = a.state + size_t(w.r) * kRowState;
   if (w.L <= a.K) return;
@@ -341,14 +362,14 @@ __device__ void select_whole_row(const TopkArgs& a, const Row& w, int* hist, int
   }
 }
 
-constexpr size_t kSelSmem = size_t(kCandCap) * 8 + 2048 * 4;
+constexpr size_t kSelSmem = size_t(kCandCap) * 8 + 4096 * 4;
 
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(TopkArgs a) {
   pdl_wait();
   extern __shared__ uint32_t sel_smem[];
   uint32_t* ckey = sel_smem;                                  // [kCandCap]
   int* cidx = reinterpret_cast<int*>(sel_smem + kCandCap);    // [kCandCap]
-  int* hist = cidx + kCandCap;                                // [2048]
+  int* hist = cidx + kCandCap;                                // [4096]
   __shared__ int smw[64];
   const Row w = row_of(a, blockIdx.x);
   int32_t* out = a.topk_idx + size_t(w.r) * a.K;
