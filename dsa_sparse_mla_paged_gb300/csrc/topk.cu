@@ -7,8 +7,10 @@
 //
 // Scores are compared through an order-preserving 32-bit key (larger score ->
 // larger key; -0 and +0 share one key). Three kernels:
-//   sample  one CTA per row: from <= 8,192 evenly spaced scores, pick a key g
-//           that about 2K tokens of the row are expected to reach
+//   sample  one cluster of 8 CTAs per row: the 8,192 threads read <= 8,192
+//           evenly spaced scores (one each, so no SM issues more than 1,024
+//           scattered reads) into the first CTA's shared memory, which picks a
+//           key g that about 2K tokens of the row are expected to reach
 //   filter  one CTA per 4,096-token chunk: compact the chunk's tokens with
 //           key >= g, in index order, into the row's candidate buffer (a
 //           region reserved with one atomic; its place recorded per chunk)
@@ -22,6 +24,7 @@
 // runs an exact radix select over the whole row by itself. No CTA ever waits
 // on another; the result does not depend on the order of the atomics.
 #include "dsa_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace dsa {
 
@@ -213,29 +216,51 @@ __device__ uint32_t block_kth_key(const uint32_t (&keys)[PER], int k, int* hist,
 
 // ---------------------------------------------------------------- sample
 constexpr int kSampleThreads = 1024;
-constexpr int kSamplePer = kSampleMax / kSampleThreads;  // 8
+constexpr int kSampleCluster = 8;
+constexpr int kSamplePer = kSampleMax / kSampleThreads;  // 8 samples per thread of the first CTA
+constexpr size_t kSampleSmem = size_t(kSampleMax) * 4 + 4096 * 4;
 
-__global__ void __launch_bounds__(kSampleThreads, 1) topk_sample_kernel(TopkArgs a) {
-  pdl_wait();
+__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads, 1)
+    topk_sample_kernel(TopkArgs a) {
+  extern __shared__ uint32_t sample_smem[];
+  uint32_t* sk = sample_smem;                                  // [8192] sample keys (first CTA)
+  int* hist = reinterpret_cast<int*>(sample_smem + kSampleMax);  // [4096]
   __shared__ int smw[64];
-  __shared__ int hist[4096];
-  const Row w = row_of(a, blockIdx.x);
-  int* st = a.state + size_t(w.r) * kRowState;
-  if (w.L <= a.K) return;
+  pdl_wait();
+  ptx::cluster_sync();  // every CTA of the cluster runs before any remote store
+  const uint32_t rank = ptx::cluster_ctarank();
+  const Row w = row_of(a, blockIdx.y);
+  if (w.L <= a.K) return;  // the whole cluster (one row) returns
   const int ns = min(w.L, kSampleMax);
-  const float* row = a.scores + size_t(w.r) * a.stride;
-  // evenly spaced positions (any fixed spread serves: g only has to be a good guess)
-  const float step = float(w.L) / float(ns);
+  // sample i = rank * 1024 + t at evenly spaced positions (any fixed spread
+  // serves: g only has to be a good guess)
+  {
+    const int i = int(rank) * kSampleThreads + threadIdx.x;
+    const float step = float(w.L) / float(ns);
+    const float* row = a.scores + size_t(w.r) * a.stride;
+    const uint32_t key = i < ns ? order_key(__ldcg(row + min(w.L - 1, int(float(i) * step)))) : 0u;
+    ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_u32(sk + i), 0), key);
+  }
+  ptx::cluster_sync();  // the first CTA holds every sample
+  if (rank != 0) return;
   uint32_t keys[kSamplePer];
 #pragma unroll
-  for (int u = 0; u < kSamplePer; ++u) {
-    const int i = threadIdx.x + u * kSampleThreads;
-    const int pos = min(w.L - 1, int(float(i) * step));
-    keys[u] = i < ns ? order_key(__ldcg(row + pos)) : 0u;
-  }
-  // the r-th largest sample: about 2K tokens of the row are expected at or above it
+  for (int u = 0; u < kSamplePer; ++u) keys[u] = sk[threadIdx.x * kSamplePer + u];
+  // the r-th largest sample: about 2K tokens of the row are expected at or above it.
+  // For small r the r-th largest of the threads' maxima (8 samples each) serves:
+  // the top r samples almost always sit in r different threads, and a slightly
+  // lower g only adds candidates.
   const int r = int((int64_t(2) * a.K * ns + w.L - 1) / w.L);
-  const uint32_t g = r < ns ? block_kth_key<kSampleThreads, kSamplePer>(keys, r, hist, smw) : 0u;
+  uint32_t g = 0u;
+  if (r <= 64) {
+    uint32_t m[1] = {0u};
+#pragma unroll
+    for (int u = 0; u < kSamplePer; ++u) m[0] = max(m[0], keys[u]);
+    g = block_kth_key<kSampleThreads, 1>(m, r, hist, smw);
+  } else if (r < ns) {
+    g = block_kth_key<kSampleThreads, kSamplePer>(keys, r, hist, smw);
+  }
+  int* st = a.state + size_t(w.r) * kRowState;
   if (threadIdx.x == 0) {
     st[0] = int(g);
     st[1] = 0;  // candidate cursor
@@ -491,7 +516,10 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   a.topk_idx = topk_idx;
   a.phys_rows = phys_rows;
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSelSmem));
-  if (e == cudaSuccess) e = launch_pdl(topk_sample_kernel, dim3(L.rows), dim3(kSampleThreads), 0, st, a);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(topk_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSampleSmem));
+  if (e == cudaSuccess)
+    e = launch_pdl(topk_sample_kernel, dim3(kSampleCluster, L.rows), dim3(kSampleThreads), kSampleSmem, st, a);
   if (e == cudaSuccess)
     e = launch_pdl(topk_filter_kernel, dim3(L.max_chunks, L.rows), dim3(kFiltThreads), 0, st, a);
   if (e == cudaSuccess) e = launch_pdl(topk_select_kernel, dim3(L.rows), dim3(kSelThreads), kSelSmem, st, a);
