@@ -430,28 +430,24 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, 1)
           ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
           if (!ok) break;
           if (lane == 0) ptx::mbar_arrive_expect_tx(full + s, bytes);
-          // lane g issues the copies of tile g (keys and scales of its pages);
+          // lanes 2g and 2g+1 issue the copies of tile g (keys and scales of its
+          // first and second page; measured 2% faster than one lane per tile);
           // all key copies of the stage go out before its query loads, since a
           // query slot is released by the MMA warp only once it has this stage
           // in hand
           {
-            const int src = i0 + min(lane, ng - 1);
+            const int gg = lane >> 1, page = lane & 1;
+            const int src = i0 + min(gg, ng - 1);
             const int pg0 = __shfl_sync(0xffffffffu, cur.pg0, src);
             const int pg1 = __shfl_sync(0xffffffffu, cur.pg1, src);
             const int two = __shfl_sync(0xffffffffu, cur.two, src);
-            if (lane < ng) {
-              uint8_t* kdst = keys + (size_t(s) * G + lane) * kKeyTileBytes;
-              float* sdst = scl + (size_t(s) * G + lane) * kTileTok;
-              const int p0 = page_or_zero(a, pg0);
-              ptx::tma_load_3d_hint(kdst, &kmap, full + s, 0, 0, p0, pol);
-              ptx::bulk_load_hint(sdst, a.key_pool + size_t(p0) * a.key_page_stride + kPage * kIdxDim, kPage * 4,
+            if (gg < ng && (page == 0 || two)) {
+              const int p = page_or_zero(a, page ? pg1 : pg0);
+              uint8_t* kdst = keys + (size_t(s) * G + gg) * kKeyTileBytes + page * kPage * kIdxDim;
+              float* sdst = scl + (size_t(s) * G + gg) * kTileTok + page * kPage;
+              ptx::tma_load_3d_hint(kdst, &kmap, full + s, 0, 0, p, pol);
+              ptx::bulk_load_hint(sdst, a.key_pool + size_t(p) * a.key_page_stride + kPage * kIdxDim, kPage * 4,
                                   full + s, pol);
-              if (two) {
-                const int p1 = page_or_zero(a, pg1);
-                ptx::tma_load_3d_hint(kdst + kPage * kIdxDim, &kmap, full + s, 0, 0, p1, pol);
-                ptx::bulk_load_hint(sdst + kPage, a.key_pool + size_t(p1) * a.key_page_stride + kPage * kIdxDim,
-                                    kPage * 4, full + s, pol);
-              }
             }
           }
           }
