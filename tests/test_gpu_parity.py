@@ -176,6 +176,24 @@ def test_decode_end_to_end_small(case):
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
 
 
+@pytest.mark.parametrize("nq,topk,ctx", [(8, 2048, [5000, 2100]), (2, 100, [3000, 90, 700]), (1, 1000, [1500, 40000])])
+def test_decode_query_rows_and_k(nq, topk, ctx):
+    """The largest query-row count (one 128-token tile per pipeline stage, shared
+    head weights) and top-k sizes other than 2048 (fewer attention splits)."""
+    inp = gen.make_inputs(len(ctx), nq, ctx, seed=300 + nq + topk, bt_mode="permuted", topk=topk)
+    d = Dev(inp)
+    out, lse, idx = d.decode()
+    idx = idx.cpu().numpy()
+    sc = d.scores().cpu().numpy()
+    es = rows_error_scale(inp)
+    for (b, t), r in O.decode(inp).items():
+        row = b * inp.n_q + t
+        check_scores(sc[row, :len(r["scores"])], r["scores"], es[row])
+        check_selection(idx[row], r["idx"], r["scores"], inp.topk, es[row])
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+
+
 def test_determinism_and_batch_invariance():
     inp = gen.make_inputs(4, 1, [5000, 7000, 3000, 9000], seed=11, bt_mode="permuted")
     d = Dev(inp)
