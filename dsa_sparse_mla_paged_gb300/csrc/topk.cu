@@ -409,6 +409,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(TopkArgs a)
     }
     return;
   }
+  // the row state and the first window of chunk records are loaded together
+  const int nch = (w.L + kTopkChunk - 1) / kTopkChunk;
+  const int* ci = a.chunkinfo + size_t(w.r) * a.max_chunks * 2;
+  const int2 rec0 = int(threadIdx.x) < nch ? *reinterpret_cast<const int2*>(ci + 2 * threadIdx.x) : make_int2(0, 0);
   const int* st = a.state + size_t(w.r) * kRowState;
   const int total = st[1];
   if (st[2] != 0 || total < a.K) {
@@ -418,19 +422,17 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(TopkArgs a)
   // gather the candidates chunk by chunk (index order again): chunks in
   // windows of 1024; positions spread over all threads, each finds its chunk
   // by binary search over the window's offsets
-  const int nch = (w.L + kTopkChunk - 1) / kTopkChunk;
-  const int* ci = a.chunkinfo + size_t(w.r) * a.max_chunks * 2;
   const uint64_t* cand = a.cand + size_t(w.r) * kCandCap;
   int* wpre = hist;          // [1024] window prefix of counts
   int* wsrc = hist + 1024;   // [1024] source offsets
   int done = 0;
   for (int c0 = 0; c0 < nch; c0 += kSelThreads) {
     const int c = c0 + threadIdx.x;
-    const int cnt = c < nch ? ci[2 * c + 1] : 0;
+    const int2 rec = c0 == 0 ? rec0 : (c < nch ? *reinterpret_cast<const int2*>(ci + 2 * c) : make_int2(0, 0));
     int tot;
-    const int pre = block_excl_scan<kSelThreads>(cnt, &tot, smw);
+    const int pre = block_excl_scan<kSelThreads>(rec.y, &tot, smw);
     wpre[threadIdx.x] = pre;
-    wsrc[threadIdx.x] = c < nch ? ci[2 * c] : 0;
+    wsrc[threadIdx.x] = rec.x;
     __syncthreads();
     const int nw = min(kSelThreads, nch - c0);
     for (int pos = threadIdx.x; pos < tot; pos += kSelThreads) {
