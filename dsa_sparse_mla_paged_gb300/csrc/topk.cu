@@ -103,20 +103,6 @@ __device__ __forceinline__ int phys_row(const TopkArgs& a, int b, int s) {
   return pg * kPage + (s % kPage);
 }
 
-// Sum of one int over the CTA (NT threads); every thread gets the total.
-template <int NT>
-__device__ __forceinline__ int block_sum(int v, int* smw) {
-  constexpr int NW = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ws = __reduce_add_sync(0xffffffffu, v);
-  if (lane == 0) smw[warp] = ws;
-  __syncthreads();
-  int t = lane < NW ? smw[lane] : 0;
-  t = __reduce_add_sync(0xffffffffu, t);
-  __syncthreads();
-  return t;
-}
-
 // The k-th largest (1-based) of the keys held by the CTA (PER per thread; key
 // 0 marks an empty slot and is never counted; 1 <= k <= number of keys).
 // The bits all keys share (from the block's min and max key) are skipped; the
@@ -457,34 +443,27 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(TopkArgs a)
     mk[u] = i < total ? ckey[i] : 0u;
   }
   const uint32_t tau = block_kth_key<kSelThreads, kSelPer>(mk, a.K, hist, smw);
-  int gt = 0;
+  // one scan of (keys > tau, keys == tau) packed 16 | 16 bits: the tokens
+  // selected before this thread are those above tau plus the first `need`
+  // ties in index order
+  int gt = 0, ne = 0;
 #pragma unroll
-  for (int u = 0; u < kSelPer; ++u) gt += mk[u] > tau;
-  const int need = a.K - block_sum<kSelThreads>(gt, smw);
-  // ordered write: thread t takes candidates t*8 .. t*8+7
-  int ne = 0, ns = 0;
-#pragma unroll
-  for (int u = 0; u < kSelPer; ++u) ne += (threadIdx.x * kSelPer + u < total) && mk[u] == tau;
-  int te;
-  int eq = block_excl_scan<kSelThreads>(ne, &te, smw);
-  {
-    int e = eq;
-#pragma unroll
-    for (int u = 0; u < kSelPer; ++u) {
-      if (threadIdx.x * kSelPer + u >= total) break;
-      if (mk[u] > tau) ++ns;
-      else if (mk[u] == tau && e++ < need) ++ns;
-    }
+  for (int u = 0; u < kSelPer; ++u) {
+    const bool valid = threadIdx.x * kSelPer + u < total;
+    gt += valid && mk[u] > tau;
+    ne += valid && mk[u] == tau;
   }
-  int ts;
-  int p = block_excl_scan<kSelThreads>(ns, &ts, smw);
+  int tot;
+  const int pre = block_excl_scan<kSelThreads>((gt << 16) | ne, &tot, smw);
+  const int need = a.K - (tot >> 16);
+  int e = pre & 0xFFFF;
+  int p = (pre >> 16) + min(e, need);
+  // ordered write: thread t takes candidates t*8 .. t*8+7
 #pragma unroll
   for (int u = 0; u < kSelPer; ++u) {
     const int i = threadIdx.x * kSelPer + u;
     if (i >= total) break;
-    bool sel = false;
-    if (mk[u] > tau) sel = true;
-    else if (mk[u] == tau) sel = eq++ < need;
+    const bool sel = mk[u] > tau || (mk[u] == tau && e++ < need);
     if (sel) {
       if (p < a.K) {
         out[p] = cidx[i];
