@@ -421,15 +421,33 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(TopkArgs a)
     wsrc[threadIdx.x] = rec.x;
     __syncthreads();
     const int nw = min(kSelThreads, nch - c0);
-    for (int pos = threadIdx.x; pos < tot; pos += kSelThreads) {
-      int lo = 0, hi = nw - 1;  // last chunk with wpre <= pos
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (wpre[mid] <= pos) lo = mid; else hi = mid - 1;
+    // every position's source first, then all loads in flight at once
+    // (tot <= kCandCap: at most kCandCap / kSelThreads positions per thread)
+    constexpr int kPos = kCandCap / kSelThreads;
+    int srcs[kPos];
+#pragma unroll
+    for (int u = 0; u < kPos; ++u) {
+      const int pos = threadIdx.x + u * kSelThreads;
+      srcs[u] = -1;
+      if (pos < tot) {
+        int lo = 0, hi = nw - 1;  // last chunk with wpre <= pos
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (wpre[mid] <= pos) lo = mid; else hi = mid - 1;
+        }
+        srcs[u] = wsrc[lo] + (pos - wpre[lo]);
       }
-      const uint64_t v = cand[wsrc[lo] + (pos - wpre[lo])];
-      ckey[done + pos] = uint32_t(v >> 32);
-      cidx[done + pos] = int(uint32_t(v));
+    }
+    uint64_t vals[kPos];
+#pragma unroll
+    for (int u = 0; u < kPos; ++u) vals[u] = srcs[u] >= 0 ? cand[srcs[u]] : 0ull;
+#pragma unroll
+    for (int u = 0; u < kPos; ++u) {
+      const int pos = threadIdx.x + u * kSelThreads;
+      if (srcs[u] >= 0) {
+        ckey[done + pos] = uint32_t(vals[u] >> 32);
+        cidx[done + pos] = int(uint32_t(vals[u]));
+      }
     }
     done += tot;
     __syncthreads();
