@@ -91,7 +91,7 @@ typedef enum { DSA_LAT_FP8_576 = 0, DSA_LAT_NVFP4_352 = 1 } dsa_lat_fmt_t;
 typedef struct {
   int32_t batch;              /* B >= 1 */
   int32_t n_q;                /* query tokens per request, 1..8 */
-  int32_t topk;               /* K; this build: 2048 */
+  int32_t topk;               /* K, 1..2048 (the article's K is 2048) */
   int32_t page_size;          /* tokens per page; this build: 64 */
   int32_t max_pages_per_req;  /* row stride of block_table (entries); ctx_b <= this * page_size */
   int32_t idx_heads;          /* 32 */
@@ -121,8 +121,12 @@ dsa_status_t dsa_workspace_size(const dsa_params_t* params, size_t* bytes);
  * weights):
  *   amax_h = max_d |q[h,d]|, q8_h = E4M3_rne_sat(q_h * (448/amax_h)),
  *   w'_h = w_h * (amax_h/448)        (IEEE fp32, round to nearest);
- *   score[row][s] = sum_h w'_h * max(0, scale_s * (q8_h . kfp8_s))
- * for s < L_{b,t}; entries s >= L_{b,t} are left untouched.
+ *   score[row][s] = sum_h w'_h * max(0, q8_h . k_s)
+ * for s < L_{b,t}; entries s >= L_{b,t} are left untouched. The key k_s is
+ * E4M3(k) * scale_s (DSA_KEY_FP8_132) or E2M1(k) * 2^(e_blk - 127) with one
+ * E8M0 exponent e_blk per 32 values (DSA_KEY_MXFP4_68, section "量化：原生 MXFP4
+ * 索引器"); exact while a token's four exponents lie within 8 of each other,
+ * the nearest E4M3 rewrite of the smaller blocks beyond that.
  *   q_idx  bf16 [B, n_q, idx_heads, idx_dim]      (16-B aligned)
  *   w      fp32 [B, n_q, idx_heads]
  *   key_pool   num_pages pages of key_page_stride bytes (16-B aligned)
@@ -149,7 +153,10 @@ dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t s
 
 /* Stage 3, exact absorbed-MLA attention over the selected tokens
  * ("K3.1 Pro 中的稀疏注意力": attention runs exactly, but only over those tokens).
- * For each row and head h, with c_s = E4M3(latent_s) * latent_scale:
+ * For each row and head h, with c_s = E4M3(latent_s) * latent_scale
+ * (DSA_LAT_FP8_576), or for DSA_LAT_NVFP4_352 the 512 nope values
+ * E2M1 * E4M3(block scale of 16) and the 64 rope values E4M3, all times
+ * latent_scale (recipes page, "NVFP4 KV cache"):
  *   logit_s = softmax_scale * q_h . c_s  (576 dims), s in S = {topk_idx >= 0}
  *   out[h]  = sum_s softmax(logit)_s * c_s[0:512]          (bf16, RNE)
  *   lse[h]  = ln sum_s exp(logit_s)                        (fp32)
@@ -176,7 +183,7 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
 /* Stage 2 without a workspace, for callers that cannot allocate device memory
  * when they select tokens (a plugin whose host owns every device byte, a
  * real-time loop that must not enter the allocator, a caller handed only input
- * and output pointers). The paper has no counterpart: this is a deployment
+ * and output pointers). The article has no counterpart: this is a deployment
  * variant of dsa_topk, with the same arguments minus the workspace and the same
  * results bit for bit.
  * - Scratch: one static device array of about 4.3 MB inside libdsa, held by
