@@ -194,6 +194,40 @@ def test_decode_query_rows_and_k(nq, topk, ctx):
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
 
 
+@pytest.mark.parametrize("kf,lf", [("fp8", "fp8"), ("mxfp4", "nvfp4")])
+def test_decode_on_packed_block_rows(kf, lf):
+    """A packed block-row cache (the article's cache: every layer's key page and
+    latent page of one block in one power-of-two row): layer 1 of 3 is decoded in
+    place through pool pointers into the row and the row size as page stride."""
+    import torch
+    import dsa_sparse_mla_paged_gb300 as dsa
+
+    inp = gen.make_inputs(2, 2, [3000, 1500], seed=320, bt_mode="permuted", key_fmt=kf, lat_fmt=lf)
+    kp, lp = inp.page_size * O.KEY_BYTES[kf], inp.page_size * O.LAT_BYTES[lf]
+    layer = kp + lp
+    row = 1 << (3 * layer - 1).bit_length()
+    rng = np.random.default_rng(5)
+    packed = rng.integers(0, 256, (inp.num_pages, row), dtype=np.uint8)  # other layers: any bytes
+    packed[:, layer:layer + kp] = inp.key_pool[:, :kp]
+    packed[:, layer + kp:2 * layer] = inp.lat_pool[:, :lp]
+    d = Dev(inp)
+    buf = torch.from_numpy(packed).cuda()
+    d.key_pool = buf.view(-1)[layer:]
+    d.lat_pool = buf.view(-1)[layer + kp:]
+    d.p = dsa.make_params(batch=inp.batch, n_q=inp.n_q, max_pages_per_req=inp.max_pages, num_pages=inp.num_pages,
+                          key_page_stride=row, lat_page_stride=row, key_fmt=d.p.key_fmt, lat_fmt=d.p.lat_fmt,
+                          softmax_scale=inp.softmax_scale, latent_scale=inp.latent_scale)
+    d.ws = torch.zeros(dsa.workspace_size(d.p), dtype=torch.uint8, device="cuda")
+    out, lse, idx = d.decode()
+    idx = idx.cpu().numpy()
+    for (b, t), r in O.decode(inp).items():
+        row_i = b * inp.n_q + t
+        check_selection(idx[row_i], r["idx"], r["scores"], inp.topk, score_error_scale(inp, b, t))
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+    assert dsa.get_device_error(d.ws) == 0
+
+
 def test_determinism_and_batch_invariance():
     inp = gen.make_inputs(4, 1, [5000, 7000, 3000, 9000], seed=11, bt_mode="permuted")
     d = Dev(inp)
