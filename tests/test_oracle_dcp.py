@@ -1,0 +1,91 @@
+"""Pins of the decode-context-parallel exact top-k merge oracle (CPU)."""
+import numpy as np
+import pytest
+
+from oracle import dcp as D
+from oracle import dsa as O
+
+
+def _brute_order(scores, W, k):
+    """The merge order by plain Python sorting of (key desc, position asc, shard asc)."""
+    s = np.asarray(scores, np.float32)
+    items = []
+    for r in range(W):
+        toks = list(range(r, len(s), W))
+        keys = [int(D.bf16_order_key(D.bf16_rne_bits(np.array([s[t]], np.float32)))[0]) for t in toks]
+        ranked = sorted(zip(keys, toks), key=lambda kt: (-kt[0], kt[1]))
+        items += [(-key, j, r, tok) for j, (key, tok) in enumerate(ranked)]
+    items.sort()
+    sel = sorted(t for *_, t in items[:k])
+    return np.array(sel + [-1] * (k - len(sel)), np.int32)
+
+
+def test_bf16_rounding_and_key_order():
+    x = np.array([1.0, 1.00390625, 1.0078125, -1.0, 0.0, -0.0, 3.0e38, -3.0e38, 1.001953125, 1.005859375], np.float32)
+    b = D.bf16_rne_bits(x)
+    # 1 + 2^-8 and 1 + 3*2^-9 are exact midpoints: ties go to the even mantissa
+    assert list(b[:4]) == [0x3F80, 0x3F80, 0x3F81, 0xBF80]
+    assert b[8] == 0x3F80 and b[9] == 0x3F81
+    k = D.bf16_order_key(b)
+    assert k[4] == k[5]  # -0 == +0
+    order = np.argsort(k, kind="stable")
+    vals = x[order].astype(np.float64)
+    assert (np.diff(vals[np.r_[True, np.diff(k[order]) != 0]]) > 0).all()
+
+
+def test_pack_orders_key_then_position_then_shard():
+    a = D.pack(np.array([5]), np.array([0]), 3)[0]
+    assert D.pack(np.array([6]), np.array([4000]), 15)[0] > a      # higher key wins
+    assert D.pack(np.array([5]), np.array([1]), 0)[0] < a          # earlier position wins
+    assert D.pack(np.array([5]), np.array([0]), 4)[0] < a          # lower shard wins
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("levels", [None, 6])
+def test_merge_is_the_ideal_top_k(W, levels):
+    rng = np.random.default_rng(W * 10 + (levels or 0))
+    for L in (50, 257, 3000):
+        s = rng.standard_normal(L).astype(np.float32)
+        if levels:
+            s = (np.round(s * levels) / levels).astype(np.float32)  # many exact ties
+        k = 64
+        res = D.merge(s, W, k)
+        assert np.array_equal(res["idx"], D.ideal_topk(s, W, k))
+        assert np.array_equal(res["idx"], _brute_order(s, W, k))
+
+
+def test_single_shard_is_the_top_k_of_bf16_scores():
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal(5000).astype(np.float32)
+    b = (D.bf16_rne_bits(s).astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(D.merge(s, 1, 256)["idx"], O.topk_select(b, 256))
+
+
+def test_resend_when_one_shard_holds_most_of_the_top_k():
+    rng = np.random.default_rng(4)
+    W, k, L = 8, 128, 20000
+    s = rng.standard_normal(L).astype(np.float32)
+    s[2::W] += 10.0  # shard 2 holds every top token
+    res = D.merge(s, W, k)
+    m = res["m"]
+    assert res["resent"] == [2]
+    assert res["words"] == W * m + k
+    assert np.array_equal(res["idx"], D.ideal_topk(s, W, k))
+    assert set((res["idx"] % W).tolist()) == {2}  # every winner is shard 2's
+
+
+def test_no_resend_on_spread_scores_and_traffic():
+    rng = np.random.default_rng(5)
+    W, k = 8, 2048
+    s = rng.standard_normal(1 << 17).astype(np.float32)
+    res = D.merge(s, W, k)
+    assert res["resent"] == []
+    # 1.5 K candidates of 4 B against every shard's full top-K as (fp32, id) pairs
+    assert res["words"] == W * res["m"] == W * 384
+    assert (W * k * 8) / (res["words"] * 4) > 10
+
+
+def test_short_rows_send_everything():
+    s = np.random.default_rng(6).standard_normal(100).astype(np.float32)
+    res = D.merge(s, 4, 2048)
+    assert res["resent"] == [] and np.array_equal(res["idx"][:100], np.arange(100))
