@@ -5,8 +5,8 @@ module only turns tensors into device pointers and status codes into
 exceptions. There is no fallback: if libdsa.so is missing, ``load()`` raises.
 
 Entry points mirror include/dsa.h: ``workspace_size``, ``indexer_scores``,
-``topk``, ``topk_noalloc``, ``sparse_mla_decode``, ``decode``,
-``get_device_error``, ``status_string``.
+``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``sparse_mla_decode``,
+``decode``, ``get_device_error``, ``status_string``.
 """
 from __future__ import annotations
 
@@ -30,6 +30,7 @@ EXPORTS = (
     "dsa_indexer_scores",
     "dsa_topk",
     "dsa_topk_noalloc",
+    "dsa_dcp_topk_merge",
     "dsa_sparse_mla_decode",
     "dsa_decode",
     "dsa_get_device_error",
@@ -98,6 +99,7 @@ def load() -> ctypes.CDLL:
         "dsa_indexer_scores": [P, vp, vp, vp, vp, vp, vp, i64, vp, sz, vp],
         "dsa_topk": [P, vp, i64, vp, vp, vp, vp, vp, sz, vp],
         "dsa_topk_noalloc": [P, vp, i64, vp, vp, vp, vp, vp],
+        "dsa_dcp_topk_merge": [P, vp, i64, vp, ctypes.c_int32, vp, vp, vp, sz, vp],
         "dsa_sparse_mla_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_get_device_error": [vp, vp, ctypes.POINTER(ctypes.c_int32)],
@@ -166,6 +168,14 @@ def topk_noalloc(params, scores, score_stride, ctx_lens, block_table, topk_idx, 
     _check("dsa_topk_noalloc", load().dsa_topk_noalloc(
         ctypes.byref(params), _ptr(scores), int(score_stride), _ptr(ctx_lens), _ptr(block_table),
         _ptr(topk_idx), _ptr(phys_rows), _stream(stream)))
+
+
+def dcp_topk_merge(params, scores, score_stride, ctx_lens, world, topk_idx, stats, ws, stream=None):
+    """The exact top-k merge of `world` token shards (decode context parallelism,
+    emulated on one GPU); `stats` int32 [rows, 2] or None (see include/dsa.h)."""
+    _check("dsa_dcp_topk_merge", load().dsa_dcp_topk_merge(
+        ctypes.byref(params), _ptr(scores), int(score_stride), _ptr(ctx_lens), int(world), _ptr(topk_idx),
+        _ptr(stats), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def sparse_mla_decode(params, q, lat_pool, block_table, ctx_lens, topk_idx, out, lse, ws, stream=None):

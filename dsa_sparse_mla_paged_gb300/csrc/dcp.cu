@@ -1,0 +1,347 @@
+// Decode context parallelism, emulated on one GPU: the exact top-k merge of W
+// token shards ("vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "长上下文：带稀疏
+// indexer 的 decode 上下文并行", "流量减少 10× 的精确 top-k 合并").
+//
+// Shard r of a row holds tokens s with s mod W == r. Two kernels:
+//   shard  one CTA per (shard, row): the shard's first min(K, L_r) tokens in
+//          the shard's order (bf16 score key desc, token asc), as the lists a
+//          GPU would keep (key, token) by position
+//   merge  one CTA per row: round 1 packs each shard's first m = ceil(1.5 K / W)
+//          candidates into 32-bit words (key16 << 16 | (4095 - position) << 4 |
+//          (15 - shard)), radix-selects the K largest, and finds the shards
+//          whose m candidates were all selected while they hold more; those
+//          send their first K and round 2 selects again. The winners are
+//          written in ascending token order with the round's traffic.
+#include "block_select.cuh"
+#include "dsa_internal.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kDcpThreads = 1024;
+constexpr int kTieCap = 4096;  // ties at the shard threshold gathered and sorted in shared memory
+
+struct DcpArgs {
+  const float* scores;
+  int64_t stride;
+  const int32_t* ctx_lens;
+  int n_q, cap, K, W, m;
+  uint32_t* lkey;   // [rows][kDcpMaxWorld][K] key16 by position
+  int32_t* ltok;    // [rows][kDcpMaxWorld][K] token by position
+  int32_t* lcount;  // [rows][kDcpMaxWorld]
+  int32_t* topk_idx;
+  int32_t* stats;   // [rows][2] or null: re-sent shard mask, words exchanged
+  int* err;
+};
+
+// Visible length of a row, or 0 (and the error bit) for an invalid context.
+__device__ __forceinline__ int dcp_row_len(const DcpArgs& a, int row, bool report) {
+  const int b = row / a.n_q, t = row - b * a.n_q;
+  const int ctx = a.ctx_lens[b];
+  if (ctx < a.n_q || ctx > a.cap || ctx - a.n_q + t + 1 > a.stride) {
+    if (report && threadIdx.x == 0) atomicOr(a.err, DSA_DEVERR_CTX);
+    return 0;
+  }
+  return ctx - a.n_q + t + 1;
+}
+
+// 16-bit order key of the bf16 rounding (nearest even) of an fp32 score.
+__device__ __forceinline__ uint32_t bf16_order_key(float f) {
+  const uint64_t u = __float_as_uint(f);
+  uint32_t b = uint32_t((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16) & 0xFFFFu;
+  if (b == 0x8000u) b = 0u;
+  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+
+// Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory by
+// the whole CTA.
+template <int NT>
+__device__ void bitonic_sort_u64(uint64_t* v, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < (n >> 1); i += NT) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint64_t x = v[lo], y = v[hi];
+        if ((x > y) == up) { v[lo] = y; v[hi] = x; }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+// ---------------------------------------------------------------- shard lists
+// The n-th largest key16 of the shard (two 8-bit histogram passes), then the
+// tokens above it and the lowest-token ties at it, sorted into the shard order.
+__global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
+  pdl_wait();
+  __shared__ int hist[256];
+  __shared__ int s_sel[4];  // high byte, count above it, threshold key, ties wanted
+  __shared__ int s_n[2];    // list fill, tie fill
+  extern __shared__ uint64_t dcp_smem[];
+  uint64_t* list = dcp_smem;                                   // [2048] (0xFFFF - key) << 32 | token
+  uint32_t* ties = reinterpret_cast<uint32_t*>(list + kMaxTopK);  // [kTieCap] tokens at the threshold
+  const int r = blockIdx.x, row = blockIdx.y;
+  const int L = dcp_row_len(a, row, false);
+  const int Lr = L > r ? (L - 1 - r) / a.W + 1 : 0;
+  const int n = min(a.K, Lr);
+  int32_t* cnt_out = a.lcount + size_t(row) * kDcpMaxWorld + r;
+  if (n == 0) {
+    if (threadIdx.x == 0) *cnt_out = 0;
+    return;
+  }
+  const float* src = a.scores + size_t(row) * a.stride + r;
+  // pass 1: high byte
+  for (int i = threadIdx.x; i < 256; i += kDcpThreads) hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < Lr; i += kDcpThreads)
+    atomicAdd(&hist[bf16_order_key(__ldcg(src + size_t(i) * a.W)) >> 8], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int above = 0, h = 255;
+    for (; h > 0; --h) {
+      if (above + hist[h] >= n) break;
+      above += hist[h];
+    }
+    s_sel[0] = h;
+    s_sel[1] = above;
+  }
+  __syncthreads();
+  const uint32_t hb = uint32_t(s_sel[0]);
+  const int above_hb = s_sel[1];
+  // pass 2: low byte within the high byte
+  for (int i = threadIdx.x; i < 256; i += kDcpThreads) hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < Lr; i += kDcpThreads) {
+    const uint32_t k = bf16_order_key(__ldcg(src + size_t(i) * a.W));
+    if ((k >> 8) == hb) atomicAdd(&hist[k & 255u], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int above = above_hb, l = 255;
+    for (; l > 0; --l) {
+      if (above + hist[l] >= n) break;
+      above += hist[l];
+    }
+    s_sel[2] = int((hb << 8) | uint32_t(l));
+    s_sel[3] = n - above;  // ties at the threshold to take (lowest tokens first)
+    s_n[0] = 0;
+    s_n[1] = 0;
+  }
+  __syncthreads();
+  const uint32_t tau = uint32_t(s_sel[2]);
+  const int need = s_sel[3];
+  const int n_ties = hist[tau & 255u];
+  // pass 3: tokens above the threshold, and the ties (all of them when they fit)
+  for (int i = threadIdx.x; i < Lr; i += kDcpThreads) {
+    const uint32_t k = bf16_order_key(__ldcg(src + size_t(i) * a.W));
+    if (k > tau) {
+      list[atomicAdd(&s_n[0], 1)] = (uint64_t(0xFFFFu - k) << 32) | uint32_t(r + i * a.W);
+    } else if (k == tau && n_ties <= kTieCap) {
+      ties[atomicAdd(&s_n[1], 1)] = uint32_t(r + i * a.W);
+    }
+  }
+  __syncthreads();
+  const int n_gt = s_n[0];
+  if (n_ties <= kTieCap) {
+    // lowest `need` tokens among the ties
+    const int p = pow2_at_least(n_ties);
+    for (int i = n_ties + threadIdx.x; i < p; i += kDcpThreads) ties[i] = 0xFFFFFFFFu;
+    __syncthreads();
+    // ascending 32-bit bitonic sort of the tie tokens in place
+    for (int size = 2; size <= p; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = threadIdx.x; i < (p >> 1); i += kDcpThreads) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const uint32_t x = ties[lo], y = ties[hi];
+          if ((x > y) == up) { ties[lo] = y; ties[hi] = x; }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = threadIdx.x; i < need; i += kDcpThreads)
+      list[n_gt + i] = (uint64_t(0xFFFFu - tau) << 32) | ties[i];
+  } else {
+    // many equal keys: the ties in token order, chunk by chunk
+    __shared__ int smw[64];
+    int taken = 0;
+    for (int base = 0; base < Lr && taken < need; base += kDcpThreads) {
+      const int i = base + threadIdx.x;
+      const int is_tie = (i < Lr && bf16_order_key(__ldcg(src + size_t(i) * a.W)) == tau) ? 1 : 0;
+      int tot;
+      const int pre = block_excl_scan<kDcpThreads>(is_tie, &tot, smw);
+      if (is_tie && taken + pre < need)
+        list[n_gt + taken + pre] = (uint64_t(0xFFFFu - tau) << 32) | uint32_t(r + i * a.W);
+      taken += tot;
+    }
+  }
+  __syncthreads();
+  // the shard order: key desc, token asc
+  const int p = pow2_at_least(n);
+  for (int i = n + threadIdx.x; i < p; i += kDcpThreads) list[i] = ~0ull;
+  bitonic_sort_u64<kDcpThreads>(list, p);
+  uint32_t* kout = a.lkey + (size_t(row) * kDcpMaxWorld + r) * a.K;
+  int32_t* tout = a.ltok + (size_t(row) * kDcpMaxWorld + r) * a.K;
+  for (int j = threadIdx.x; j < n; j += kDcpThreads) {
+    kout[j] = 0xFFFFu - uint32_t(list[j] >> 32);
+    tout[j] = int32_t(uint32_t(list[j]));
+  }
+  if (threadIdx.x == 0) *cnt_out = n;
+}
+
+// ---------------------------------------------------------------- merge
+// Candidate c of a round (shard lists laid end to end, `cnt` per shard) -> word.
+template <int PER>
+__device__ __forceinline__ void round_words(const DcpArgs& a, int row, const int* cnt, const int* off, int total,
+                                            uint32_t (&words)[PER]) {
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int c = threadIdx.x + u * kDcpThreads;
+    words[u] = 0u;
+    if (c < total) {
+      int r = 0;
+      while (r + 1 < a.W && off[r + 1] <= c) ++r;
+      const int j = c - off[r];
+      const uint32_t key = a.lkey[(size_t(row) * kDcpMaxWorld + r) * a.K + j];
+      words[u] = (key << 16) | (uint32_t(4095 - j) << 4) | uint32_t(15 - r);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
+  pdl_wait();
+  extern __shared__ uint64_t dcp_smem[];
+  int* hist = reinterpret_cast<int*>(dcp_smem);                   // [4096] radix select
+  uint64_t* win = dcp_smem + 2048;                                 // [2048] winners (token)
+  __shared__ int smw[64];
+  __shared__ int cnt[kDcpMaxWorld], off[kDcpMaxWorld + 1], held[kDcpMaxWorld], sel[kDcpMaxWorld];
+  __shared__ int s_nwin, s_resend, s_words;
+  const int row = blockIdx.x;
+  const int L = dcp_row_len(a, row, true);
+  int32_t* out = a.topk_idx + size_t(row) * a.K;
+  if (L <= a.K) {
+    // every visible token is kept, as in the single-GPU top-k
+    for (int i = threadIdx.x; i < a.K; i += kDcpThreads) out[i] = i < L ? i : -1;
+    if (a.stats && threadIdx.x == 0) {
+      a.stats[2 * row] = 0;
+      a.stats[2 * row + 1] = L;
+    }
+    return;
+  }
+  if (threadIdx.x < a.W) {
+    held[threadIdx.x] = a.lcount[size_t(row) * kDcpMaxWorld + threadIdx.x];
+    sel[threadIdx.x] = 0;
+  }
+  if (threadIdx.x == 0) { s_nwin = 0; s_resend = 0; }
+  __syncthreads();
+  uint32_t tau = 0;
+  for (int round = 0; round < 2; ++round) {
+    if (threadIdx.x == 0) {
+      int o = 0, words = round == 0 ? 0 : s_words;
+      for (int r = 0; r < a.W; ++r) {
+        const bool full = (s_resend >> r) & 1;
+        cnt[r] = min(full ? a.K : a.m, held[r]);
+        off[r] = o;
+        o += cnt[r];
+        if (round == 0 || full) words += cnt[r];
+      }
+      off[a.W] = o;
+      s_words = words;
+    }
+    __syncthreads();
+    const int total = off[a.W];
+    // the K largest words (all distinct); round 2 holds at most ~W/1.5 full lists
+    if (round == 0) {
+      uint32_t wd[4];
+      round_words<4>(a, row, cnt, off, total, wd);
+      tau = block_kth_key<kDcpThreads, 4>(wd, a.K, hist, smw);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (wd[u] != 0u && wd[u] >= tau) atomicAdd(&sel[15 - int(wd[u] & 15u)], 1);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int mask = 0;
+        for (int r = 0; r < a.W; ++r)
+          if (held[r] > a.m && sel[r] == a.m) mask |= 1 << r;
+        s_resend = mask;
+      }
+      __syncthreads();
+      if (s_resend == 0) {
+        // winners of round 1
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (wd[u] != 0u && wd[u] >= tau) {
+            const int r = 15 - int(wd[u] & 15u), j = 4095 - int((wd[u] >> 4) & 4095u);
+            win[atomicAdd(&s_nwin, 1)] = uint32_t(a.ltok[(size_t(row) * kDcpMaxWorld + r) * a.K + j]);
+          }
+        break;
+      }
+    } else {
+      uint32_t wd[32];
+      round_words<32>(a, row, cnt, off, total, wd);
+      tau = block_kth_key<kDcpThreads, 32>(wd, a.K, hist, smw);
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        if (wd[u] != 0u && wd[u] >= tau) {
+          const int r = 15 - int(wd[u] & 15u), j = 4095 - int((wd[u] >> 4) & 4095u);
+          win[atomicAdd(&s_nwin, 1)] = uint32_t(a.ltok[(size_t(row) * kDcpMaxWorld + r) * a.K + j]);
+        }
+    }
+    __syncthreads();
+  }
+  __syncthreads();
+  // winners in ascending token order
+  const int nwin = s_nwin;
+  const int p = pow2_at_least(a.K);
+  for (int i = nwin + threadIdx.x; i < p; i += kDcpThreads) win[i] = ~0ull;
+  bitonic_sort_u64<kDcpThreads>(win, p);
+  for (int i = threadIdx.x; i < a.K; i += kDcpThreads) out[i] = i < nwin ? int32_t(win[i]) : -1;
+  if (a.stats && threadIdx.x == 0) {
+    a.stats[2 * row] = s_resend;
+    a.stats[2 * row + 1] = s_words;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
+                             int64_t score_stride, const int32_t* ctx_lens, int world, int32_t* topk_idx,
+                             int32_t* stats, cudaStream_t st) {
+  DcpArgs a;
+  a.scores = scores;
+  a.stride = score_stride;
+  a.ctx_lens = ctx_lens;
+  a.n_q = p.n_q;
+  a.cap = L.cap;
+  a.K = p.topk;
+  a.W = world;
+  a.m = (3 * p.topk + 2 * world - 1) / (2 * world);  // ceil(1.5 K / W)
+  a.lkey = reinterpret_cast<uint32_t*>(ws + L.dcp_key);
+  a.ltok = reinterpret_cast<int32_t*>(ws + L.dcp_tok);
+  a.lcount = reinterpret_cast<int32_t*>(ws + L.dcp_cnt);
+  a.topk_idx = topk_idx;
+  a.stats = stats;
+  a.err = reinterpret_cast<int*>(ws + L.err);
+  const size_t shard_smem = size_t(kMaxTopK) * 8 + size_t(kTieCap) * 4;
+  const size_t merge_smem = size_t(2048) * 8 + size_t(kMaxTopK) * 8;
+  cudaError_t e = cudaFuncSetAttribute(dcp_shard_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(shard_smem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dcp_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(merge_smem));
+  if (e == cudaSuccess)
+    e = launch_pdl(dcp_shard_kernel, dim3(world, L.rows), dim3(kDcpThreads), shard_smem, st, a);
+  if (e == cudaSuccess) e = launch_pdl(dcp_merge_kernel, dim3(L.rows), dim3(kDcpThreads), merge_smem, st, a);
+  return e;
+}
+
+}  // namespace dsa

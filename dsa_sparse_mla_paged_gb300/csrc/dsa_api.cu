@@ -101,6 +101,20 @@ dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t s
                                  block_table, topk_idx, phys_rows, stream));
 }
 
+dsa_status_t dsa_dcp_topk_merge(const dsa_params_t* params, const float* scores, int64_t score_stride,
+                                const int32_t* ctx_lens, int32_t world, int32_t* topk_idx, int32_t* stats,
+                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if (!scores || !aligned16(scores) || score_stride < 1 || (score_stride & 3)) return DSA_ERR_INVALID;
+  if (!ctx_lens || !topk_idx) return DSA_ERR_INVALID;
+  if (world < 1 || world > dsa::kDcpMaxWorld) return DSA_ERR_INVALID;
+  WsLayout L;
+  if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
+  return cuda_status(launch_dcp_merge(*params, L, static_cast<char*>(ws), scores, score_stride, ctx_lens, world,
+                                      topk_idx, stats, stream));
+}
+
 dsa_status_t dsa_sparse_mla_decode(const dsa_params_t* params, const void* q, const void* lat_pool,
                                    const int32_t* block_table, const int32_t* ctx_lens,
                                    const int32_t* topk_idx, void* out, float* lse, void* ws,

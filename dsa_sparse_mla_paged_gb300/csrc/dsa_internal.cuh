@@ -35,6 +35,9 @@ constexpr int kRowState = 16;     // int32 words of per-row selection state
 constexpr int kSplitTok = 128;
 constexpr int kMaxSplits = (kMaxTopK + kSplitTok - 1) / kSplitTok;
 
+// emulated decode context parallelism: at most this many token shards
+constexpr int kDcpMaxWorld = 16;
+
 // Byte offsets of the workspace regions (all 256-B aligned).
 struct WsLayout {
   size_t err;       // int32 error word
@@ -47,6 +50,9 @@ struct WsLayout {
   size_t opart;     // float [rows][splits][96][512]
   size_t lpart;     // float [rows][splits][96]
   size_t topk;      // int32 [rows][topk] (dsa_decode without topk_idx_out)
+  size_t dcp_key;   // uint32 [rows][kDcpMaxWorld][topk] shard lists: bf16 keys by position
+  size_t dcp_tok;   // int32 [rows][kDcpMaxWorld][topk] shard lists: tokens by position
+  size_t dcp_cnt;   // int32 [rows][kDcpMaxWorld] shard list lengths
   size_t scores;    // float [rows][cap]
   size_t total;
   int rows, cap, max_chunks, splits;
@@ -74,6 +80,9 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.opart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * kDNope * 4);
   L.lpart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * 4);
   L.topk = o; o = align256(o + size_t(L.rows) * p.topk * 4);
+  L.dcp_key = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * p.topk * 4);
+  L.dcp_tok = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * p.topk * 4);
+  L.dcp_cnt = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * 4);
   L.scores = o; o = align256(o + size_t(L.rows) * L.cap * 4);
   L.total = o;
   return L;
@@ -145,6 +154,9 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
 cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                         int64_t score_stride, const int32_t* ctx_lens, const int32_t* block_table,
                         int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st);
+cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
+                             int64_t score_stride, const int32_t* ctx_lens, int world, int32_t* topk_idx,
+                             int32_t* stats, cudaStream_t st);
 cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q,
                               const void* lat_pool, const int32_t* block_table,
                               const int32_t* ctx_lens, const int32_t* topk_idx, void* out,

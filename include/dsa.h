@@ -180,6 +180,34 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
                         float* lse, int32_t* topk_idx_out, void* ws, size_t ws_bytes,
                         cudaStream_t stream);
 
+/* Stage 2 as W decode-context-parallel GPUs would run it, emulated on one GPU
+ * ("vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "长上下文：带稀疏 indexer 的
+ * decode 上下文并行", "流量减少 10× 的精确 top-k 合并"). Shard r of a row holds
+ * the tokens s < L with s mod W == r. Each shard orders its tokens by the
+ * round-to-nearest-even bf16 of the score (higher first, -0 == +0), then by
+ * token; j is a token's position in that order. A candidate travels as the
+ * 32-bit word key16 << 16 | (4095 - j) << 4 | (15 - r), key16 being the
+ * order-preserving 16-bit key of the bf16 score, so word order is the global
+ * order (key desc, position asc, shard asc).
+ *   round 1  every shard sends its first m = ceil(1.5 K / W) candidates (all
+ *            it holds, if fewer); the K largest words are selected.
+ *   round 2  only if some shard holds more than m tokens and all m it sent
+ *            were selected: each such shard sends its first min(K, L_r) and
+ *            the K largest words are selected again.
+ * The result is the top min(K, L) of all tokens under the global order, written
+ * like dsa_topk (ascending token order, -1 padded); rows with L <= K keep every
+ * token. It equals dsa_topk's except where bf16 rounding ties or reorders
+ * scores.
+ *   world   W, 1 .. 16 (shard and position must fit the word's 16 low bits)
+ *   scores, score_stride, ctx_lens, topk_idx  as dsa_topk
+ *   stats   int32 [B * n_q, 2] or NULL: per row the bit mask of shards that
+ *           re-sent in round 2, and the words all shards sent in both rounds
+ *           (a row with L <= K reports 0 and L)
+ * Errors as dsa_topk; the workspace holds the shard lists. */
+dsa_status_t dsa_dcp_topk_merge(const dsa_params_t* params, const float* scores, int64_t score_stride,
+                                const int32_t* ctx_lens, int32_t world, int32_t* topk_idx, int32_t* stats,
+                                void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Stage 2 without a workspace, for callers that cannot allocate device memory
  * when they select tokens (a plugin whose host owns every device byte, a
  * real-time loop that must not enter the allocator, a caller handed only input

@@ -25,7 +25,8 @@ Readings (the page gives the steps, not the bits):
     token id, which would not fit. W <= 16 and positions < 4096.
   * The global order is the pack order: bf16 key desc, then position asc, then
     shard asc. The round sends m = ceil(1.5 K / W) candidates per shard (all a
-    shard holds when it holds fewer).
+    shard holds when it holds fewer), but never more than K: a shard's tokens
+    past its first K cannot be in the top K, and m > K only when W = 1.
   * Re-send test: shard r sent m candidates, holds more than m tokens, and all m
     are among the round's top K; then it sends its first K instead (all it holds
     when fewer) and the selection runs again.
@@ -96,8 +97,8 @@ def merge(scores: np.ndarray, W: int, k: int = 2048) -> dict:
         sel = _select(words, k)
         return toks[sel], owner[sel]
 
-    counts = [m] * W
-    sent = sum(min(m, len(t)) for t, _ in lists)
+    counts = [min(m, k)] * W
+    sent = sum(min(m, k, len(t)) for t, _ in lists)
     tok_sel, own_sel = round_(counts)
     resent = [r for r in range(W)
               if len(lists[r][0]) > m and int((own_sel == r).sum()) == m]

@@ -98,6 +98,21 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert st == dsa.DSA_ERR_INVALID
 
 
+def test_dcp_merge_world_and_arguments_checked(lib):
+    p = _params()
+    need = dsa.workspace_size(p)
+    L = lib
+    for world in (0, -1, 17):
+        st = L.dsa_dcp_topk_merge(ctypes.byref(p), FAKE, 640, FAKE, world, FAKE, None, FAKE, need, None)
+        assert st == dsa.DSA_ERR_INVALID, world
+    st = L.dsa_dcp_topk_merge(ctypes.byref(p), FAKE, 640, FAKE, 8, None, None, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    st = L.dsa_dcp_topk_merge(ctypes.byref(p), FAKE + 4, 640, FAKE, 8, FAKE, None, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
+    st = L.dsa_dcp_topk_merge(ctypes.byref(p), FAKE, 640, FAKE, 16, FAKE, None, FAKE, need - 1, None)
+    assert st == dsa.DSA_ERR_WORKSPACE
+
+
 def test_fp4_formats_take_their_own_page_strides(lib):
     """MXFP4 keys are 68 B and NVFP4 latents 352 B per token: a page stride below
     64 rows of the format (or not a multiple of 16 B) is rejected."""
