@@ -27,9 +27,11 @@ Readings (the page gives the steps, not the bits):
     shard asc. The round sends m = ceil(1.5 K / W) candidates per shard (all a
     shard holds when it holds fewer), but never more than K: a shard's tokens
     past its first K cannot be in the top K, and m > K only when W = 1.
-  * Re-send test: shard r sent m candidates, holds more than m tokens, and all m
-    are among the round's top K; then it sends its first K instead (all it holds
-    when fewer) and the selection runs again.
+  * Re-send test: shard r sent m candidates, holds more than m tokens among its
+    first K, and all m are among the round's top K; then it sends its first K
+    instead (all it holds when fewer) and the selection runs again. (A shard
+    that already sent its first K cannot hold more winners, so m >= K never
+    re-sends.)
   * Exactness: the merged K tokens are the top K of *all* tokens under the same
     order (``ideal_topk``). They may differ from the fp32 top-k where bf16
     rounding ties or reorders scores (the page's BF16 exchange).
@@ -101,7 +103,7 @@ def merge(scores: np.ndarray, W: int, k: int = 2048) -> dict:
     sent = sum(min(m, k, len(t)) for t, _ in lists)
     tok_sel, own_sel = round_(counts)
     resent = [r for r in range(W)
-              if len(lists[r][0]) > m and int((own_sel == r).sum()) == m]
+              if min(k, len(lists[r][0])) > m and int((own_sel == r).sum()) == m]
     if resent:
         for r in resent:
             counts[r] = k

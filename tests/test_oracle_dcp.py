@@ -89,3 +89,11 @@ def test_short_rows_send_everything():
     s = np.random.default_rng(6).standard_normal(100).astype(np.float32)
     res = D.merge(s, 4, 2048)
     assert res["resent"] == [] and np.array_equal(res["idx"][:100], np.arange(100))
+
+
+def test_no_resend_when_m_covers_k():
+    # K = 1, W = 2: m = 1 = K, so the one word a shard sent is all it could win
+    s = np.random.default_rng(7).standard_normal(50).astype(np.float32)
+    res = D.merge(s, 2, 1)
+    assert res["m"] == 1 and res["resent"] == [] and res["words"] == 2
+    assert res["idx"][0] == int(np.argmax(s))
