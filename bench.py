@@ -216,7 +216,7 @@ def run_reference(args, rank):
 
 
 def run_stage(args):
-    """Time one stage entry point alone (for kernel profiles): `--stage indexer|topk|mla`."""
+    """Time one entry point alone (for kernel profiles): `--stage indexer|topk|mla|dcp_merge|dcp_combine`."""
     import torch
 
     import dsa_sparse_mla_paged_gb300 as dsa
@@ -236,8 +236,14 @@ def run_stage(args):
     # inputs of the later stages come from the earlier ones, computed once untimed
     dsa.indexer_scores(d.p, d.q_idx, d.w, d.key_pool, d.block_table, d.ctx, sc, d.cap, d.ws)
     dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws)
+    W = args.world
+    stats = torch.zeros((d.rows, 2), dtype=torch.int32, device="cuda")
+    parts_o = torch.zeros((W, d.rows, 96, 512), dtype=torch.bfloat16, device="cuda")
+    parts_l = torch.zeros((W, d.rows, 96), dtype=torch.float32, device="cuda")
     calls = {
         "indexer": lambda: dsa.indexer_scores(d.p, d.q_idx, d.w, d.key_pool, d.block_table, d.ctx, sc, d.cap, d.ws),
+        "dcp_merge": lambda: dsa.dcp_topk_merge(d.p, sc, d.cap, d.ctx, W, idx, stats, d.ws),
+        "dcp_combine": lambda: dsa.lse_combine(d.p, W, parts_o, parts_l, out, lse),
         "topk": lambda: dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws),
         "mla": lambda: dsa.sparse_mla_decode(d.p, d.q, d.lat_pool, d.block_table, d.ctx, idx, out, lse, d.ws),
     }
@@ -252,11 +258,30 @@ def run_stage(args):
     ev1.record()
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1) / args.steps
-    nbytes = {"indexer": indexer_bytes(inp.ctx, inp.n_q), "topk": 4 * sum(int(c) for c in inp.ctx) * inp.n_q,
-              "mla": step_bytes(inp.ctx, inp.n_q, inp.topk) - indexer_bytes(inp.ctx, inp.n_q)}[args.stage]
+    score_bytes = 4 * sum(int(c) for c in inp.ctx) * inp.n_q
+    nbytes = {"indexer": indexer_bytes(inp.ctx, inp.n_q), "topk": score_bytes,
+              "mla": step_bytes(inp.ctx, inp.n_q, inp.topk) - indexer_bytes(inp.ctx, inp.n_q),
+              # every score read once; the partials read once and the result written
+              "dcp_merge": score_bytes, "dcp_combine": (W + 1) * d.rows * 96 * 512 * 2 + (W + 1) * d.rows * 96 * 4,
+              }[args.stage]
     assert dsa.get_device_error(d.ws) == 0
-    print(json.dumps({"stage": args.stage, "workload": args.workload, "ms": ms, "bytes": nbytes,
-                      "gbs": nbytes / (ms * 1e-3) / 1e9}), flush=True)
+    line = {"stage": args.stage, "workload": args.workload, "ms": ms, "bytes": nbytes,
+            "gbs": nbytes / (ms * 1e-3) / 1e9}
+    if args.stage == "dcp_merge":
+        from oracle import dcp as D
+
+        st = stats.cpu().numpy()
+        full = W * inp.topk * 8  # every shard's local top-K as (fp32 score, int32 token) pairs
+        line.update({"world": W, "resent_rows": int((st[:, 0] != 0).sum()),
+                     "words_per_row": [int(x) for x in st[:, 1]],
+                     "traffic_ratio_vs_full_exchange": [full / (4 * int(x)) for x in st[:, 1]]})
+        # the oracle beside it, on the first row of the same scores
+        row = sc[0, :int(inp.ctx[0]) - inp.n_q + 1].cpu().numpy()
+        t0 = time.perf_counter()
+        res = D.merge(row, W, inp.topk)
+        line["oracle_ms_per_row"] = (time.perf_counter() - t0) * 1e3
+        line["row0_equals_oracle"] = bool(np.array_equal(idx[0].cpu().numpy(), res["idx"]))
+    print(json.dumps(line), flush=True)
 
 
 def run_ours(args, rank, world):
@@ -450,8 +475,9 @@ def main():
     ap.add_argument("--workload", default="b4_ctx1m")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--stage", default="all", choices=["all", "indexer", "topk", "mla"],
-                    help="time one stage entry point alone (kernel profiling)")
+    ap.add_argument("--stage", default="all", choices=["all", "indexer", "topk", "mla", "dcp_merge", "dcp_combine"],
+                    help="time one entry point alone (kernel profiling; the dcp_* stages emulate --world shards)")
+    ap.add_argument("--world", type=int, default=8, help="shards of the dcp_* stages")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     rank = int(os.environ.get("RANK", "0"))

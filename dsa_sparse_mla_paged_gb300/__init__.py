@@ -5,7 +5,7 @@ module only turns tensors into device pointers and status codes into
 exceptions. There is no fallback: if libdsa.so is missing, ``load()`` raises.
 
 Entry points mirror include/dsa.h: ``workspace_size``, ``indexer_scores``,
-``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``sparse_mla_decode``,
+``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``lse_combine``, ``sparse_mla_decode``,
 ``decode``, ``get_device_error``, ``status_string``.
 """
 from __future__ import annotations
@@ -31,6 +31,7 @@ EXPORTS = (
     "dsa_topk",
     "dsa_topk_noalloc",
     "dsa_dcp_topk_merge",
+    "dsa_lse_combine",
     "dsa_sparse_mla_decode",
     "dsa_decode",
     "dsa_get_device_error",
@@ -100,6 +101,7 @@ def load() -> ctypes.CDLL:
         "dsa_topk": [P, vp, i64, vp, vp, vp, vp, vp, sz, vp],
         "dsa_topk_noalloc": [P, vp, i64, vp, vp, vp, vp, vp],
         "dsa_dcp_topk_merge": [P, vp, i64, vp, ctypes.c_int32, vp, vp, vp, sz, vp],
+        "dsa_lse_combine": [P, ctypes.c_int32, vp, vp, vp, vp, vp],
         "dsa_sparse_mla_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_get_device_error": [vp, vp, ctypes.POINTER(ctypes.c_int32)],
@@ -176,6 +178,12 @@ def dcp_topk_merge(params, scores, score_stride, ctx_lens, world, topk_idx, stat
     _check("dsa_dcp_topk_merge", load().dsa_dcp_topk_merge(
         ctypes.byref(params), _ptr(scores), int(score_stride), _ptr(ctx_lens), int(world), _ptr(topk_idx),
         _ptr(stats), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def lse_combine(params, parts, part_out, part_lse, out, lse, stream=None):
+    """Merge `parts` partial attention results (bf16 out, fp32 lse per shard) by their LSE."""
+    _check("dsa_lse_combine", load().dsa_lse_combine(
+        ctypes.byref(params), int(parts), _ptr(part_out), _ptr(part_lse), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def sparse_mla_decode(params, q, lat_pool, block_table, ctx_lens, topk_idx, out, lse, ws, stream=None):

@@ -12,6 +12,11 @@
 //          whose m candidates were all selected while they hold more; those
 //          send their first K and round 2 selects again. The winners are
 //          written in ascending token order with the round's traffic.
+// and the cross-shard LSE combine of the shards' partial attention outputs
+// (same section: each GPU attends over its own winners, then the partials are
+// merged by their log-sum-exp).
+#include <cuda_bf16.h>
+
 #include "block_select.cuh"
 #include "dsa_internal.cuh"
 
@@ -313,7 +318,67 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- LSE combine
+// out = sum_i e^{lse_i - lse} O_i, lse = ln sum_i e^{lse_i} over the parts; a
+// part with lse_i = -inf (no tokens) adds nothing; all parts empty -> 0, -inf.
+// 64 threads per (row, head), 8 dims (16 B of bf16) per thread per part.
+constexpr int kCombPairs = 4;
+
+__global__ void __launch_bounds__(64 * kCombPairs) dcp_lse_combine_kernel(const __nv_bfloat16* __restrict__ part_out,
+                                                                         const float* __restrict__ part_lse,
+                                                                         int parts, int pairs,
+                                                                         __nv_bfloat16* __restrict__ out,
+                                                                         float* __restrict__ lse) {
+  pdl_wait();
+  const int pair = blockIdx.x * kCombPairs + int(threadIdx.x >> 6);
+  if (pair >= pairs) return;
+  const int d0 = int(threadIdx.x & 63) * 8;
+  float li[kDcpMaxWorld];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kDcpMaxWorld; ++i) {
+    li[i] = i < parts ? __ldg(part_lse + size_t(i) * pairs + pair) : -INFINITY;
+    m = fmaxf(m, li[i]);
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float total = -INFINITY;
+  if (m != -INFINITY) {
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < kDcpMaxWorld; ++i) sum += (li[i] == -INFINITY) ? 0.f : expf(li[i] - m);
+    total = m + logf(sum);
+#pragma unroll
+    for (int i = 0; i < kDcpMaxWorld; ++i) {
+      if (i < parts && li[i] != -INFINITY) {
+        const float wi = expf(li[i] - total);
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(part_out + (size_t(i) * pairs + pair) * kDNope + d0));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 f = __bfloat1622float2(h[u]);
+          acc[2 * u] = fmaf(wi, f.x, acc[2 * u]);
+          acc[2 * u + 1] = fmaf(wi, f.y, acc[2 * u + 1]);
+        }
+      }
+    }
+  }
+  uint4 o;
+  __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) oh[u] = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+  *reinterpret_cast<uint4*>(out + size_t(pair) * kDNope + d0) = o;
+  if (lse && d0 == 0) lse[pair] = total;
+}
+
 }  // namespace
+
+cudaError_t launch_dcp_lse_combine(int rows, int parts, const void* part_out, const float* part_lse, void* out,
+                                   float* lse, cudaStream_t st) {
+  const int pairs = rows * kHeads;
+  return launch_pdl(dcp_lse_combine_kernel, dim3((pairs + kCombPairs - 1) / kCombPairs), dim3(64 * kCombPairs), 0,
+                    st, static_cast<const __nv_bfloat16*>(part_out), part_lse, parts, pairs,
+                    static_cast<__nv_bfloat16*>(out), lse);
+}
 
 cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                              int64_t score_stride, const int32_t* ctx_lens, int world, int32_t* topk_idx,

@@ -115,6 +115,16 @@ dsa_status_t dsa_dcp_topk_merge(const dsa_params_t* params, const float* scores,
                                       topk_idx, stats, stream));
 }
 
+dsa_status_t dsa_lse_combine(const dsa_params_t* params, int32_t parts, const void* part_out,
+                             const float* part_lse, void* out, float* lse, cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if (parts < 1 || parts > dsa::kDcpMaxWorld) return DSA_ERR_INVALID;
+  if (!part_out || !part_lse || !out || !aligned16(part_out) || !aligned16(out)) return DSA_ERR_INVALID;
+  return cuda_status(
+      launch_dcp_lse_combine(params->batch * params->n_q, parts, part_out, part_lse, out, lse, stream));
+}
+
 dsa_status_t dsa_sparse_mla_decode(const dsa_params_t* params, const void* q, const void* lat_pool,
                                    const int32_t* block_table, const int32_t* ctx_lens,
                                    const int32_t* topk_idx, void* out, float* lse, void* ws,

@@ -157,6 +157,8 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
 cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                              int64_t score_stride, const int32_t* ctx_lens, int world, int32_t* topk_idx,
                              int32_t* stats, cudaStream_t st);
+cudaError_t launch_dcp_lse_combine(int rows, int parts, const void* part_out, const float* part_lse, void* out,
+                                   float* lse, cudaStream_t st);
 cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q,
                               const void* lat_pool, const int32_t* block_table,
                               const int32_t* ctx_lens, const int32_t* topk_idx, void* out,

@@ -208,6 +208,21 @@ dsa_status_t dsa_dcp_topk_merge(const dsa_params_t* params, const float* scores,
                                 const int32_t* ctx_lens, int32_t world, int32_t* topk_idx, int32_t* stats,
                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* The cross-shard step of decode context parallelism (same section as
+ * dsa_dcp_topk_merge): each of `parts` shards attended over its own winners
+ * (dsa_sparse_mla_decode with the other shards' slots set to -1), and the
+ * partial results are merged by their log-sum-exp:
+ *   lse[h] = ln sum_i exp(lse_i[h]),  out[h] = sum_i exp(lse_i[h] - lse[h]) * out_i[h]
+ * in fp32, out rounded to bf16 (RNE). A part with lse_i = -inf (no tokens)
+ * adds nothing; if every part is empty, out = 0 and lse = -inf.
+ *   parts    1 .. 16
+ *   part_out bf16 [parts][B * n_q][heads][d_nope] (16-B aligned)
+ *   part_lse fp32 [parts][B * n_q][heads]
+ *   out      bf16 [B * n_q][heads][d_nope] (16-B aligned); lse fp32 [B * n_q][heads] or NULL
+ * No workspace; no device error word. */
+dsa_status_t dsa_lse_combine(const dsa_params_t* params, int32_t parts, const void* part_out,
+                             const float* part_lse, void* out, float* lse, cudaStream_t stream);
+
 /* Stage 2 without a workspace, for callers that cannot allocate device memory
  * when they select tokens (a plugin whose host owns every device byte, a
  * real-time loop that must not enter the allocator, a caller handed only input

@@ -133,3 +133,13 @@ def test_library_missing_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(dsa, "library_path", lambda: str(tmp_path / "libdsa.so"))
     with pytest.raises(RuntimeError, match="not built"):
         dsa.load()
+
+
+def test_lse_combine_arguments_checked(lib):
+    p = _params()
+    L = lib
+    for parts in (0, 17):
+        assert L.dsa_lse_combine(ctypes.byref(p), parts, FAKE, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID
+    assert L.dsa_lse_combine(ctypes.byref(p), 4, None, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID
+    assert L.dsa_lse_combine(ctypes.byref(p), 4, FAKE + 2, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID
+    assert L.dsa_lse_combine(ctypes.byref(p), 4, FAKE, FAKE, FAKE + 8, None, None) == dsa.DSA_ERR_INVALID

@@ -138,3 +138,71 @@ def test_merge_at_full_context():
     idx, st = _check_rows(ctx, mat, 8)
     assert st[3, 0] == 1 << 6
     assert all(st[r, 1] == 8 * 384 for r in range(3))
+
+
+# ----------------------------------------------------------------------------- cross-shard combine
+
+def test_lse_combine_equals_oracle():
+    import torch
+
+    rng = np.random.default_rng(60)
+    B, parts = 3, 5
+    p = dsa.make_params(batch=B, n_q=1, max_pages_per_req=4, num_pages=1, key_page_stride=64 * 132,
+                        lat_page_stride=64 * 576)
+    po = rng.standard_normal((parts, B, 96, 512)).astype(np.float32)
+    pl = (rng.standard_normal((parts, B, 96)) * 3 + 8).astype(np.float32)
+    pl[1, 0, :] = -np.inf                      # a shard with no winners for row 0
+    pl[:, 2, 7] = -np.inf                      # every shard empty for row 2, head 7
+    pl[3, 1, 5] = pl[0, 1, 5] + 60.0           # one shard dominates
+    po_bf = torch.from_numpy(po).to(torch.bfloat16)
+    po_np = po_bf.float().numpy().astype(np.float64)
+    dev_o = po_bf.cuda()
+    dev_l = torch.from_numpy(pl).cuda()
+    out = torch.full((B, 96, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, 96), 7.0, dtype=torch.float32, device="cuda")
+    dsa.lse_combine(p, parts, dev_o, dev_l, out, lse)
+    torch.cuda.synchronize()
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b in range(B):
+        ro, rl = O.lse_combine(po_np[:, b], pl[:, b].astype(np.float64))
+        # fp32 weights and sums, one bf16 rounding of the result
+        assert (np.abs(o[b] - ro) <= 2.0 ** -8 * np.abs(ro) + 1e-5).all(), b
+        fin = np.isfinite(rl)
+        assert (np.isfinite(l[b]) == fin).all()
+        assert np.abs(l[b][fin] - rl[fin]).max() <= 1e-5 * np.abs(rl[fin]).max()
+    assert (o[2, 7] == 0).all() and np.isneginf(l[2, 7])
+
+
+@pytest.mark.parametrize("W", [2, 4, 8])
+def test_dcp_attention_equals_attention_over_the_merged_set(W):
+    """Indexer -> DCP merge -> every shard attends over its own winners -> LSE
+    combine: within the attention bars of the oracle's attention over the merged
+    set."""
+    import torch
+
+    import gen
+    from dsa_testlib import Dev, bf16_to_np, check_attention
+
+    inp = gen.make_inputs(3, 1, [20000, 3000, 1500], seed=61 + W, bt_mode="permuted", holes=True)
+    d = Dev(inp)
+    sc = d.scores()
+    idx = torch.full((3, 2048), -7, dtype=torch.int32, device="cuda")
+    dsa.dcp_topk_merge(d.p, sc, sc.shape[1], d.ctx, W, idx, None, d.ws)
+    outs, lses = [], []
+    for r in range(W):
+        own = torch.where((idx >= 0) & (idx % W == r), idx, torch.full_like(idx, -1))
+        o, l = d.mla(own)
+        outs.append(o)
+        lses.append(l)
+    out = torch.empty((3, 96, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((3, 96), dtype=torch.float32, device="cuda")
+    dsa.lse_combine(d.p, W, torch.stack(outs), torch.stack(lses), out, lse)
+    torch.cuda.synchronize()
+    assert dsa.get_device_error(d.ws) == 0
+    idx_np = idx.cpu().numpy()
+    scores_np = sc.cpu().numpy()
+    for b in range(3):
+        L = inp.ctx[b]
+        assert np.array_equal(idx_np[b], D.merge(scores_np[b, :L], W, 2048)["idx"])
+        ro, rl = O.sparse_mla(inp, b, 0, idx_np[b])
+        check_attention(bf16_to_np(out[b]), lse[b].cpu().numpy(), ro, rl)
