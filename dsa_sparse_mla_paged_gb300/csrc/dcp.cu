@@ -2,7 +2,8 @@
 // token shards ("vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "长上下文：带稀疏
 // indexer 的 decode 上下文并行", "流量减少 10× 的精确 top-k 合并").
 //
-// Shard r of a row holds tokens s with s mod W == r. Two kernels:
+// Shard r of a row holds tokens s with s mod W == r. Three kernels:
+//   keys   the bf16 keys of every shard's tokens, gathered shard by shard
 //   shard  one CTA per (shard, row): the shard's first min(K, L_r) tokens in
 //          the shard's order (bf16 score key desc, token asc), as the lists a
 //          GPU would keep (key, token) by position
@@ -32,6 +33,8 @@ struct DcpArgs {
   int64_t stride;
   const int32_t* ctx_lens;
   int n_q, cap, K, W, m;
+  int64_t S;        // shard row of keys16, in keys (multiple of 8)
+  uint16_t* keys16; // [rows][W][S] key16 by shard position
   uint32_t* lkey;   // [rows][kDcpMaxWorld][K] key16 by position
   int32_t* ltok;    // [rows][kDcpMaxWorld][K] token by position
   int32_t* lcount;  // [rows][kDcpMaxWorld]
@@ -84,7 +87,50 @@ __device__ __forceinline__ int pow2_at_least(int n) {
   return p;
 }
 
+// ---------------------------------------------------------------- shard keys
+// What each shard's GPU would hold: the 16-bit keys of its tokens, contiguous
+// (keys16[row][r][i] = key of token r + i * W). One coalesced pass over the
+// scores, so the shard kernels below read their own tokens densely.
+constexpr int kKeysThreads = 256;
+
+__global__ void __launch_bounds__(kKeysThreads) dcp_keys_kernel(DcpArgs a) {
+  pdl_wait();
+  const int row = blockIdx.y;
+  const int L = dcp_row_len(a, row, false);
+  const int t0 = (blockIdx.x * kKeysThreads + int(threadIdx.x)) * 4;
+  if (t0 >= L) return;
+  // t0 + 3 < score_stride: t0 < L <= stride, both t0 and stride multiples of 4
+  const float4 f = __ldcg(reinterpret_cast<const float4*>(a.scores + size_t(row) * a.stride + t0));
+  const float v[4] = {f.x, f.y, f.z, f.w};
+  uint16_t* base = a.keys16 + size_t(row) * a.W * a.S;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int t = t0 + e;
+    if (t < L) base[size_t(t % a.W) * a.S + t / a.W] = uint16_t(bf16_order_key(v[e]));
+  }
+}
+
 // ---------------------------------------------------------------- shard lists
+constexpr uint32_t kNoKey = 0x10000u;  // a position past the shard's end
+
+// Keys of shard positions [8v, 8v + 8); positions >= Lr read as kNoKey. The
+// 16-byte load stays inside the shard's row: S is a multiple of 8 and 8v < Lr <= S.
+__device__ __forceinline__ void keys8(const uint16_t* src, int v, int Lr, uint32_t (&k)[8]) {
+  uint4 q = make_uint4(0u, 0u, 0u, 0u);
+  if (8 * v < Lr) q = __ldcg(reinterpret_cast<const uint4*>(src) + v);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) k[e] = (8 * v + e < Lr) ? ((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) : kNoKey;
+}
+
+// Histogram add with the lanes of a warp that share a bin combined first (the
+// high byte of bf16 keys takes few values, so plain atomics would serialise).
+// Every lane of the warp calls it; bin >= 256 adds nothing.
+__device__ __forceinline__ void hist_add(int* hist, uint32_t bin) {
+  const unsigned peers = __match_any_sync(0xffffffffu, bin);
+  if (bin < 256u && int(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
 // The n-th largest key16 of the shard (two 8-bit histogram passes), then the
 // tokens above it and the lowest-token ties at it, sorted into the shard order.
 __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
@@ -92,6 +138,7 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
   __shared__ int hist[256];
   __shared__ int s_sel[4];  // high byte, count above it, threshold key, ties wanted
   __shared__ int s_n[2];    // list fill, tie fill
+  __shared__ int smw[64];
   extern __shared__ uint64_t dcp_smem[];
   uint64_t* list = dcp_smem;                                   // [2048] (0xFFFF - key) << 32 | token
   uint32_t* ties = reinterpret_cast<uint32_t*>(list + kMaxTopK);  // [kTieCap] tokens at the threshold
@@ -104,12 +151,17 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
     if (threadIdx.x == 0) *cnt_out = 0;
     return;
   }
-  const float* src = a.scores + size_t(row) * a.stride + r;
+  const uint16_t* src = a.keys16 + (size_t(row) * a.W + r) * a.S;
+  const int nv = (Lr + 7) / 8;
+  uint32_t k[8];
   // pass 1: high byte
   for (int i = threadIdx.x; i < 256; i += kDcpThreads) hist[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < Lr; i += kDcpThreads)
-    atomicAdd(&hist[bf16_order_key(__ldcg(src + size_t(i) * a.W)) >> 8], 1);
+  for (int v0 = 0; v0 < nv; v0 += kDcpThreads) {
+    keys8(src, v0 + int(threadIdx.x), Lr, k);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hist_add(hist, k[e] == kNoKey ? 256u : k[e] >> 8);
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     int above = 0, h = 255;
@@ -126,9 +178,10 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
   // pass 2: low byte within the high byte
   for (int i = threadIdx.x; i < 256; i += kDcpThreads) hist[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < Lr; i += kDcpThreads) {
-    const uint32_t k = bf16_order_key(__ldcg(src + size_t(i) * a.W));
-    if ((k >> 8) == hb) atomicAdd(&hist[k & 255u], 1);
+  for (int v0 = 0; v0 < nv; v0 += kDcpThreads) {
+    keys8(src, v0 + int(threadIdx.x), Lr, k);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hist_add(hist, (k[e] >> 8) == hb ? (k[e] & 255u) : 256u);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -147,12 +200,16 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
   const int need = s_sel[3];
   const int n_ties = hist[tau & 255u];
   // pass 3: tokens above the threshold, and the ties (all of them when they fit)
-  for (int i = threadIdx.x; i < Lr; i += kDcpThreads) {
-    const uint32_t k = bf16_order_key(__ldcg(src + size_t(i) * a.W));
-    if (k > tau) {
-      list[atomicAdd(&s_n[0], 1)] = (uint64_t(0xFFFFu - k) << 32) | uint32_t(r + i * a.W);
-    } else if (k == tau && n_ties <= kTieCap) {
-      ties[atomicAdd(&s_n[1], 1)] = uint32_t(r + i * a.W);
+  for (int v = threadIdx.x; v < nv; v += kDcpThreads) {
+    keys8(src, v, Lr, k);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t tok = uint32_t(r + (8 * v + e) * a.W);
+      if (k[e] != kNoKey && k[e] > tau) {
+        list[atomicAdd(&s_n[0], 1)] = (uint64_t(0xFFFFu - k[e]) << 32) | tok;
+      } else if (k[e] == tau && n_ties <= kTieCap) {
+        ties[atomicAdd(&s_n[1], 1)] = tok;
+      }
     }
   }
   __syncthreads();
@@ -178,16 +235,23 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
     for (int i = threadIdx.x; i < need; i += kDcpThreads)
       list[n_gt + i] = (uint64_t(0xFFFFu - tau) << 32) | ties[i];
   } else {
-    // many equal keys: the ties in token order, chunk by chunk
-    __shared__ int smw[64];
+    // many equal keys: the ties in position (= token) order, 8 positions per
+    // thread, chunk by chunk
     int taken = 0;
-    for (int base = 0; base < Lr && taken < need; base += kDcpThreads) {
-      const int i = base + threadIdx.x;
-      const int is_tie = (i < Lr && bf16_order_key(__ldcg(src + size_t(i) * a.W)) == tau) ? 1 : 0;
+    for (int v0 = 0; v0 < nv && taken < need; v0 += kDcpThreads) {
+      const int v = v0 + int(threadIdx.x);
+      keys8(src, v, Lr, k);
+      int mine = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mine += k[e] == tau ? 1 : 0;
       int tot;
-      const int pre = block_excl_scan<kDcpThreads>(is_tie, &tot, smw);
-      if (is_tie && taken + pre < need)
-        list[n_gt + taken + pre] = (uint64_t(0xFFFFu - tau) << 32) | uint32_t(r + i * a.W);
+      int at = taken + block_excl_scan<kDcpThreads>(mine, &tot, smw);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (k[e] == tau) {
+          if (at < need) list[n_gt + at] = (uint64_t(0xFFFFu - tau) << 32) | uint32_t(r + (8 * v + e) * a.W);
+          ++at;
+        }
       taken += tot;
     }
   }
@@ -224,14 +288,49 @@ __device__ __forceinline__ void round_words(const DcpArgs& a, int row, const int
   }
 }
 
+// One round's selection bookkeeping. The selected words are the ones >= tau.
+// A shard's words fall with its position, so its selected words are a prefix
+// of its candidates; sel[r] is that prefix's length, found by the one selected
+// candidate whose successor (same shard) is not selected. The winners' tokens
+// go to win[] in candidate order (block scan, no contended atomics).
+template <int PER>
+__device__ __forceinline__ void take_round(const DcpArgs& a, int row, const uint32_t (&wd)[PER], uint32_t tau,
+                                           const int* off, uint32_t* selbits, int* sel, uint64_t* win, int* smw,
+                                           bool collect) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int mine = 0;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const bool s_ = wd[u] != 0u && wd[u] >= tau;
+    const unsigned b = __ballot_sync(0xffffffffu, s_);
+    if (lane == 0) selbits[u * (kDcpThreads / 32) + warp] = b;
+    mine += s_ ? 1 : 0;
+  }
+  __syncthreads();
+  int tot;
+  int at = block_excl_scan<kDcpThreads>(mine, &tot, smw);
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    if (wd[u] != 0u && wd[u] >= tau) {
+      const int c = int(threadIdx.x) + u * kDcpThreads;
+      const int r = 15 - int(wd[u] & 15u), j = 4095 - int((wd[u] >> 4) & 4095u);
+      const int nx = c + 1;
+      if (nx >= off[r + 1] || !((selbits[nx >> 5] >> (nx & 31)) & 1u)) sel[r] = j + 1;
+      if (collect) win[at++] = uint32_t(a.ltok[(size_t(row) * kDcpMaxWorld + r) * a.K + j]);
+    }
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
   pdl_wait();
   extern __shared__ uint64_t dcp_smem[];
   int* hist = reinterpret_cast<int*>(dcp_smem);                   // [4096] radix select
   uint64_t* win = dcp_smem + 2048;                                 // [2048] winners (token)
   __shared__ int smw[64];
+  __shared__ uint32_t selbits[32 * kDcpThreads / 32];             // one bit per candidate (32 per thread)
   __shared__ int cnt[kDcpMaxWorld], off[kDcpMaxWorld + 1], held[kDcpMaxWorld], sel[kDcpMaxWorld];
-  __shared__ int s_nwin, s_resend, s_words;
+  __shared__ int s_resend, s_words;
   const int row = blockIdx.x;
   const int L = dcp_row_len(a, row, true);
   int32_t* out = a.topk_idx + size_t(row) * a.K;
@@ -248,9 +347,8 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
     held[threadIdx.x] = a.lcount[size_t(row) * kDcpMaxWorld + threadIdx.x];
     sel[threadIdx.x] = 0;
   }
-  if (threadIdx.x == 0) { s_nwin = 0; s_resend = 0; }
+  if (threadIdx.x == 0) s_resend = 0;
   __syncthreads();
-  uint32_t tau = 0;
   for (int round = 0; round < 2; ++round) {
     if (threadIdx.x == 0) {
       int o = 0, words = round == 0 ? 0 : s_words;
@@ -270,11 +368,8 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
     if (round == 0) {
       uint32_t wd[4];
       round_words<4>(a, row, cnt, off, total, wd);
-      tau = block_kth_key<kDcpThreads, 4>(wd, a.K, hist, smw);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (wd[u] != 0u && wd[u] >= tau) atomicAdd(&sel[15 - int(wd[u] & 15u)], 1);
-      __syncthreads();
+      const uint32_t tau = block_kth_key<kDcpThreads, 4>(wd, a.K, hist, smw);
+      take_round<4>(a, row, wd, tau, off, selbits, sel, win, smw, true);
       if (threadIdx.x == 0) {
         int mask = 0;
         for (int r = 0; r < a.W; ++r)
@@ -282,36 +377,19 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
         s_resend = mask;
       }
       __syncthreads();
-      if (s_resend == 0) {
-        // winners of round 1
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (wd[u] != 0u && wd[u] >= tau) {
-            const int r = 15 - int(wd[u] & 15u), j = 4095 - int((wd[u] >> 4) & 4095u);
-            win[atomicAdd(&s_nwin, 1)] = uint32_t(a.ltok[(size_t(row) * kDcpMaxWorld + r) * a.K + j]);
-          }
-        break;
-      }
+      if (s_resend == 0) break;  // round 1's winners stand
     } else {
       uint32_t wd[32];
       round_words<32>(a, row, cnt, off, total, wd);
-      tau = block_kth_key<kDcpThreads, 32>(wd, a.K, hist, smw);
-#pragma unroll
-      for (int u = 0; u < 32; ++u)
-        if (wd[u] != 0u && wd[u] >= tau) {
-          const int r = 15 - int(wd[u] & 15u), j = 4095 - int((wd[u] >> 4) & 4095u);
-          win[atomicAdd(&s_nwin, 1)] = uint32_t(a.ltok[(size_t(row) * kDcpMaxWorld + r) * a.K + j]);
-        }
+      const uint32_t tau = block_kth_key<kDcpThreads, 32>(wd, a.K, hist, smw);
+      take_round<32>(a, row, wd, tau, off, selbits, sel, win, smw, true);
     }
-    __syncthreads();
   }
-  __syncthreads();
-  // winners in ascending token order
-  const int nwin = s_nwin;
+  // winners in ascending token order (exactly K of them: the words are distinct)
   const int p = pow2_at_least(a.K);
-  for (int i = nwin + threadIdx.x; i < p; i += kDcpThreads) win[i] = ~0ull;
+  for (int i = a.K + threadIdx.x; i < p; i += kDcpThreads) win[i] = ~0ull;
   bitonic_sort_u64<kDcpThreads>(win, p);
-  for (int i = threadIdx.x; i < a.K; i += kDcpThreads) out[i] = i < nwin ? int32_t(win[i]) : -1;
+  for (int i = threadIdx.x; i < a.K; i += kDcpThreads) out[i] = int32_t(win[i]);
   if (a.stats && threadIdx.x == 0) {
     a.stats[2 * row] = s_resend;
     a.stats[2 * row + 1] = s_words;
@@ -392,6 +470,8 @@ cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws,
   a.K = p.topk;
   a.W = world;
   a.m = (3 * p.topk + 2 * world - 1) / (2 * world);  // ceil(1.5 K / W)
+  a.S = ((int64_t(L.cap) + world - 1) / world + 7) / 8 * 8;
+  a.keys16 = reinterpret_cast<uint16_t*>(ws + L.dcp_keys16);
   a.lkey = reinterpret_cast<uint32_t*>(ws + L.dcp_key);
   a.ltok = reinterpret_cast<int32_t*>(ws + L.dcp_tok);
   a.lcount = reinterpret_cast<int32_t*>(ws + L.dcp_cnt);
@@ -403,6 +483,9 @@ cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws,
   cudaError_t e = cudaFuncSetAttribute(dcp_shard_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(shard_smem));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dcp_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(merge_smem));
+  if (e == cudaSuccess)
+    e = launch_pdl(dcp_keys_kernel, dim3((L.cap + 4 * kKeysThreads - 1) / (4 * kKeysThreads), L.rows),
+                   dim3(kKeysThreads), 0, st, a);
   if (e == cudaSuccess)
     e = launch_pdl(dcp_shard_kernel, dim3(world, L.rows), dim3(kDcpThreads), shard_smem, st, a);
   if (e == cudaSuccess) e = launch_pdl(dcp_merge_kernel, dim3(L.rows), dim3(kDcpThreads), merge_smem, st, a);

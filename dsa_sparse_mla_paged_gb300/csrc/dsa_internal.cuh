@@ -53,6 +53,7 @@ struct WsLayout {
   size_t dcp_key;   // uint32 [rows][kDcpMaxWorld][topk] shard lists: bf16 keys by position
   size_t dcp_tok;   // int32 [rows][kDcpMaxWorld][topk] shard lists: tokens by position
   size_t dcp_cnt;   // int32 [rows][kDcpMaxWorld] shard list lengths
+  size_t dcp_keys16;  // uint16 [rows][W][S] shard-major score keys, W * S <= cap + 8 * kDcpMaxWorld
   size_t scores;    // float [rows][cap]
   size_t total;
   int rows, cap, max_chunks, splits;
@@ -83,6 +84,7 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.dcp_key = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * p.topk * 4);
   L.dcp_tok = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * p.topk * 4);
   L.dcp_cnt = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * 4);
+  L.dcp_keys16 = o; o = align256(o + size_t(L.rows) * (size_t(L.cap) + 8 * kDcpMaxWorld) * 2);
   L.scores = o; o = align256(o + size_t(L.rows) * L.cap * 4);
   L.total = o;
   return L;
