@@ -123,20 +123,34 @@ __device__ __forceinline__ void keys8(const uint16_t* src, int v, int Lr, uint32
   for (int e = 0; e < 8; ++e) k[e] = (8 * v + e < Lr) ? ((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) : kNoKey;
 }
 
-// Histogram add with the lanes of a warp that share a bin combined first (the
-// high byte of bf16 keys takes few values, so plain atomics would serialise).
-// Every lane of the warp calls it; bin >= 256 adds nothing.
-__device__ __forceinline__ void hist_add(int* hist, uint32_t bin) {
-  const unsigned peers = __match_any_sync(0xffffffffu, bin);
-  if (bin < 256u && int(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+// The bin of a kHiBins-bin histogram that holds the kk-th largest key, and the
+// number of keys in the bins above it (1 <= kk <= keys counted). Thread t owns
+// the two bins 2047 - 2t and 2046 - 2t; one scan of the per-thread sums finds
+// the owner, which walks its bins.
+constexpr int kHiBits = 11, kHiBins = 1 << kHiBits, kLoBits = 16 - kHiBits;
+static_assert(kHiBins == 2 * kDcpThreads, "two bins per thread");
+
+__device__ __forceinline__ int2 top_bin(const int* H, int kk, int* smw, int* s_out) {
+  const int top = kHiBins - 1 - 2 * int(threadIdx.x);
+  const int c0 = H[top], c1 = H[top - 1];
+  int tot;
+  const int before = block_excl_scan<kDcpThreads>(c0 + c1, &tot, smw);
+  if (before < kk && kk <= before + c0 + c1) {
+    if (kk <= before + c0) { s_out[0] = top; s_out[1] = before; }
+    else { s_out[0] = top - 1; s_out[1] = before + c0; }
+  }
+  __syncthreads();
+  return make_int2(s_out[0], s_out[1]);
 }
 
-// The n-th largest key16 of the shard (two 8-bit histogram passes), then the
-// tokens above it and the lowest-token ties at it, sorted into the shard order.
+// The n-th largest key16 of the shard (an 11-bit and a 5-bit histogram pass:
+// 11 bits spread the keys over enough bins that the shared atomics rarely
+// collide), then the tokens above it and the lowest-token ties at it, sorted
+// into the shard order.
 __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
   pdl_wait();
-  __shared__ int hist[256];
-  __shared__ int s_sel[4];  // high byte, count above it, threshold key, ties wanted
+  __shared__ int hist[kHiBins];
+  __shared__ int s_sel[4];  // high bin, count above it, threshold key, ties wanted
   __shared__ int s_n[2];    // list fill, tie fill
   __shared__ int smw[64];
   extern __shared__ uint64_t dcp_smem[];
@@ -154,43 +168,36 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
   const uint16_t* src = a.keys16 + (size_t(row) * a.W + r) * a.S;
   const int nv = (Lr + 7) / 8;
   uint32_t k[8];
-  // pass 1: high byte
-  for (int i = threadIdx.x; i < 256; i += kDcpThreads) hist[i] = 0;
+  // pass 1: the high 11 bits
+  for (int i = threadIdx.x; i < kHiBins; i += kDcpThreads) hist[i] = 0;
   __syncthreads();
-  for (int v0 = 0; v0 < nv; v0 += kDcpThreads) {
-    keys8(src, v0 + int(threadIdx.x), Lr, k);
+  for (int v = threadIdx.x; v < nv; v += kDcpThreads) {
+    keys8(src, v, Lr, k);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) hist_add(hist, k[e] == kNoKey ? 256u : k[e] >> 8);
+    for (int e = 0; e < 8; ++e)
+      if (k[e] != kNoKey) atomicAdd(&hist[k[e] >> kLoBits], 1);
+  }
+  __syncthreads();
+  const int2 hbin = top_bin(hist, n, smw, s_sel);
+  const uint32_t hb = uint32_t(hbin.x);
+  const int above_hb = hbin.y;
+  // pass 2: the low 5 bits within that bin
+  for (int i = threadIdx.x; i < (1 << kLoBits); i += kDcpThreads) hist[i] = 0;
+  __syncthreads();
+  for (int v = threadIdx.x; v < nv; v += kDcpThreads) {
+    keys8(src, v, Lr, k);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (k[e] != kNoKey && (k[e] >> kLoBits) == hb) atomicAdd(&hist[k[e] & ((1u << kLoBits) - 1)], 1);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int above = 0, h = 255;
-    for (; h > 0; --h) {
-      if (above + hist[h] >= n) break;
-      above += hist[h];
-    }
-    s_sel[0] = h;
-    s_sel[1] = above;
-  }
-  __syncthreads();
-  const uint32_t hb = uint32_t(s_sel[0]);
-  const int above_hb = s_sel[1];
-  // pass 2: low byte within the high byte
-  for (int i = threadIdx.x; i < 256; i += kDcpThreads) hist[i] = 0;
-  __syncthreads();
-  for (int v0 = 0; v0 < nv; v0 += kDcpThreads) {
-    keys8(src, v0 + int(threadIdx.x), Lr, k);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) hist_add(hist, (k[e] >> 8) == hb ? (k[e] & 255u) : 256u);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int above = above_hb, l = 255;
+    int above = above_hb, l = (1 << kLoBits) - 1;
     for (; l > 0; --l) {
       if (above + hist[l] >= n) break;
       above += hist[l];
     }
-    s_sel[2] = int((hb << 8) | uint32_t(l));
+    s_sel[2] = int((hb << kLoBits) | uint32_t(l));
     s_sel[3] = n - above;  // ties at the threshold to take (lowest tokens first)
     s_n[0] = 0;
     s_n[1] = 0;
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
   __syncthreads();
   const uint32_t tau = uint32_t(s_sel[2]);
   const int need = s_sel[3];
-  const int n_ties = hist[tau & 255u];
+  const int n_ties = hist[tau & ((1u << kLoBits) - 1)];
   // pass 3: tokens above the threshold, and the ties (all of them when they fit)
   for (int v = threadIdx.x; v < nv; v += kDcpThreads) {
     keys8(src, v, Lr, k);
