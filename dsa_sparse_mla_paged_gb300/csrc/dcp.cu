@@ -62,22 +62,44 @@ __device__ __forceinline__ uint32_t bf16_order_key(float f) {
   return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
 
-// Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory by
-// the whole CTA.
-template <int NT>
-__device__ void bitonic_sort_u64(uint64_t* v, int n) {
-  for (int size = 2; size <= n; size <<= 1) {
+// Ascending bitonic sort of the 2048 64-bit keys v[0 .. 2048) by the CTA's
+// 1024 threads. Thread t holds elements 2t and 2t + 1 in registers; a partner
+// in the same warp (stride < 64) is read by shuffle, any other through shared
+// memory (15 of the 66 steps). v must be written and synchronised before the
+// call; it holds the sorted keys after.
+__device__ void sort2048_u64(uint64_t* v) {
+  static_assert(kDcpThreads == 1024, "two keys per thread");
+  const int e0 = 2 * int(threadIdx.x);
+  uint64_t x0 = v[e0], x1 = v[e0 + 1];
+  for (int size = 2; size <= 2048; size <<= 1) {
+    const bool up = (e0 & size) == 0;
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < (n >> 1); i += NT) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const uint64_t x = v[lo], y = v[hi];
-        if ((x > y) == up) { v[lo] = y; v[hi] = x; }
+      if (stride == 1) {
+        const uint64_t lo = x0 < x1 ? x0 : x1, hi = x0 < x1 ? x1 : x0;
+        x0 = up ? lo : hi;
+        x1 = up ? hi : lo;
+        continue;
       }
+      uint64_t y0, y1;
+      if (stride < 64) {
+        y0 = __shfl_xor_sync(0xffffffffu, x0, stride >> 1);
+        y1 = __shfl_xor_sync(0xffffffffu, x1, stride >> 1);
+      } else {
+        __syncthreads();  // the previous exchange has been read
+        v[e0] = x0;
+        v[e0 + 1] = x1;
+        __syncthreads();
+        y0 = v[e0 ^ stride];
+        y1 = v[(e0 ^ stride) + 1];
+      }
+      const bool keep_min = ((e0 & stride) == 0) == up;
+      x0 = keep_min ? (x0 < y0 ? x0 : y0) : (x0 < y0 ? y0 : x0);
+      x1 = keep_min ? (x1 < y1 ? x1 : y1) : (x1 < y1 ? y1 : x1);
     }
   }
+  __syncthreads();
+  v[e0] = x0;
+  v[e0 + 1] = x1;
   __syncthreads();
 }
 
@@ -264,9 +286,9 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
   }
   __syncthreads();
   // the shard order: key desc, token asc
-  const int p = pow2_at_least(n);
-  for (int i = n + threadIdx.x; i < p; i += kDcpThreads) list[i] = ~0ull;
-  bitonic_sort_u64<kDcpThreads>(list, p);
+  for (int i = n + threadIdx.x; i < kMaxTopK; i += kDcpThreads) list[i] = ~0ull;
+  __syncthreads();
+  sort2048_u64(list);
   uint32_t* kout = a.lkey + (size_t(row) * kDcpMaxWorld + r) * a.K;
   int32_t* tout = a.ltok + (size_t(row) * kDcpMaxWorld + r) * a.K;
   for (int j = threadIdx.x; j < n; j += kDcpThreads) {
@@ -393,9 +415,9 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
     }
   }
   // winners in ascending token order (exactly K of them: the words are distinct)
-  const int p = pow2_at_least(a.K);
-  for (int i = a.K + threadIdx.x; i < p; i += kDcpThreads) win[i] = ~0ull;
-  bitonic_sort_u64<kDcpThreads>(win, p);
+  for (int i = a.K + threadIdx.x; i < kMaxTopK; i += kDcpThreads) win[i] = ~0ull;
+  __syncthreads();
+  sort2048_u64(win);
   for (int i = threadIdx.x; i < a.K; i += kDcpThreads) out[i] = int32_t(win[i]);
   if (a.stats && threadIdx.x == 0) {
     a.stats[2 * row] = s_resend;
