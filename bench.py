@@ -216,7 +216,9 @@ def run_reference(args, rank):
 
 
 def run_stage(args):
-    """Time one entry point alone (for kernel profiles): `--stage indexer|topk|mla|dcp_merge|dcp_combine`."""
+    """Time one entry point alone (for kernel profiles):
+    `--stage indexer|topk|mla|dcp_merge|dcp_combine|frontend` (the front end with
+    d_c = 1536, d_model = 7168 and its weights rotated through 12 copies, 173 MB > L2)."""
     import torch
 
     import dsa_sparse_mla_paged_gb300 as dsa
@@ -238,12 +240,33 @@ def run_stage(args):
     dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws)
     W = args.world
     stats = torch.zeros((d.rows, 2), dtype=torch.int32, device="cuda")
+    # the front end's weights, in enough copies that the rotation exceeds L2
+    D_C, D_MODEL = 1536, 7168
+    fe_copies = 12 if args.stage == "frontend" else 1
+    gen_ = torch.Generator(device="cuda").manual_seed(9)
+    fe_wq = [torch.randn((4096, D_C), device="cuda", generator=gen_).mul_(D_C ** -0.5).bfloat16()
+             for _ in range(fe_copies)]
+    fe_wk = [torch.randn((128, D_MODEL), device="cuda", generator=gen_).mul_(D_MODEL ** -0.5).bfloat16()
+             for _ in range(fe_copies)]
+    fe_cq = torch.randn((d.rows, D_C), device="cuda", generator=gen_).bfloat16()
+    fe_g = torch.ones(D_C, device="cuda").bfloat16()
+    fe_x = torch.randn((d.rows, D_MODEL), device="cuda", generator=gen_).bfloat16()
+    fe_w = torch.rand((d.rows, 32), device="cuda", generator=gen_)
+    fe_dims = dsa.FrontendDims(d_c=D_C, d_model=D_MODEL, eps=1e-6)
+    fe_i = [0]
+
+    def fe_call():
+        k = fe_i[0] % fe_copies
+        fe_i[0] += 1
+        dsa.indexer_frontend(d.p, fe_dims, fe_cq, fe_g, fe_wq[k], fe_w, fe_x, fe_wk[k], d.key_pool, d.block_table,
+                             d.ctx, d.ws)
     parts_o = torch.zeros((W, d.rows, 96, 512), dtype=torch.bfloat16, device="cuda")
     parts_l = torch.zeros((W, d.rows, 96), dtype=torch.float32, device="cuda")
     calls = {
         "indexer": lambda: dsa.indexer_scores(d.p, d.q_idx, d.w, d.key_pool, d.block_table, d.ctx, sc, d.cap, d.ws),
         "dcp_merge": lambda: dsa.dcp_topk_merge(d.p, sc, d.cap, d.ctx, W, idx, stats, d.ws),
         "dcp_combine": lambda: dsa.lse_combine(d.p, W, parts_o, parts_l, out, lse),
+        "frontend": lambda: fe_call(),
         "topk": lambda: dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws),
         "mla": lambda: dsa.sparse_mla_decode(d.p, d.q, d.lat_pool, d.block_table, d.ctx, idx, out, lse, d.ws),
     }
@@ -263,6 +286,9 @@ def run_stage(args):
               "mla": step_bytes(inp.ctx, inp.n_q, inp.topk) - indexer_bytes(inp.ctx, inp.n_q),
               # every score read once; the partials read once and the result written
               "dcp_merge": score_bytes, "dcp_combine": (W + 1) * d.rows * 96 * 512 * 2 + (W + 1) * d.rows * 96 * 4,
+              # weights once, the rows' inputs, q8 + w' out, one key per row
+              "frontend": (4096 * D_C + 128 * D_MODEL + D_C) * 2 + d.rows * ((D_C + D_MODEL) * 2 + 32 * 4)
+                          + d.rows * (4096 + 32 * 4 + 132),
               }[args.stage]
     assert dsa.get_device_error(d.ws) == 0
     line = {"stage": args.stage, "workload": args.workload, "ms": ms, "bytes": nbytes,
@@ -475,7 +501,8 @@ def main():
     ap.add_argument("--workload", default="b4_ctx1m")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--stage", default="all", choices=["all", "indexer", "topk", "mla", "dcp_merge", "dcp_combine"],
+    ap.add_argument("--stage", default="all",
+                    choices=["all", "indexer", "topk", "mla", "dcp_merge", "dcp_combine", "frontend"],
                     help="time one entry point alone (kernel profiling; the dcp_* stages emulate --world shards)")
     ap.add_argument("--world", type=int, default=8, help="shards of the dcp_* stages")
     args = ap.parse_args()

@@ -5,7 +5,7 @@ module only turns tensors into device pointers and status codes into
 exceptions. There is no fallback: if libdsa.so is missing, ``load()`` raises.
 
 Entry points mirror include/dsa.h: ``workspace_size``, ``indexer_scores``,
-``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``lse_combine``, ``sparse_mla_decode``,
+``indexer_frontend``, ``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``lse_combine``, ``sparse_mla_decode``,
 ``decode``, ``get_device_error``, ``status_string``.
 """
 from __future__ import annotations
@@ -19,6 +19,7 @@ DSA_OK, DSA_ERR_INVALID, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA, D
 DSA_KEY_FP8_132, DSA_KEY_MXFP4_68 = 0, 1
 DSA_LAT_FP8_576, DSA_LAT_NVFP4_352 = 0, 1
 DSA_EMIT_PHYS_ROWS = 0x1
+DSA_Q_PREPARED = 0x2
 DSA_DEVERR_BLOCK_TABLE, DSA_DEVERR_CTX, DSA_DEVERR_TOPK_INDEX = 0x1, 0x2, 0x4
 
 # Kernels one dsa_decode launches (q quantisation, indexer, 3 top-k passes:
@@ -28,6 +29,7 @@ KERNELS_PER_DECODE = 7
 EXPORTS = (
     "dsa_workspace_size",
     "dsa_indexer_scores",
+    "dsa_indexer_frontend",
     "dsa_topk",
     "dsa_topk_noalloc",
     "dsa_dcp_topk_merge",
@@ -37,6 +39,12 @@ EXPORTS = (
     "dsa_get_device_error",
     "dsa_status_string",
 )
+
+
+class FrontendDims(ctypes.Structure):
+    """dsa_frontend_dims_t."""
+
+    _fields_ = [("d_c", ctypes.c_int32), ("d_model", ctypes.c_int32), ("eps", ctypes.c_float)]
 
 
 class Params(ctypes.Structure):
@@ -100,6 +108,8 @@ def load() -> ctypes.CDLL:
         "dsa_indexer_scores": [P, vp, vp, vp, vp, vp, vp, i64, vp, sz, vp],
         "dsa_topk": [P, vp, i64, vp, vp, vp, vp, vp, sz, vp],
         "dsa_topk_noalloc": [P, vp, i64, vp, vp, vp, vp, vp],
+        "dsa_indexer_frontend": [P, ctypes.POINTER(FrontendDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                 sz, vp],
         "dsa_dcp_topk_merge": [P, vp, i64, vp, ctypes.c_int32, vp, vp, vp, sz, vp],
         "dsa_lse_combine": [P, ctypes.c_int32, vp, vp, vp, vp, vp],
         "dsa_sparse_mla_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
@@ -156,6 +166,17 @@ def indexer_scores(params, q_idx, w, key_pool, block_table, ctx_lens, scores, sc
     _check("dsa_indexer_scores", load().dsa_indexer_scores(
         ctypes.byref(params), _ptr(q_idx), _ptr(w), _ptr(key_pool), _ptr(block_table), _ptr(ctx_lens),
         _ptr(scores), int(score_stride), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def indexer_frontend(params, dims, c_q, gamma_q, w_q, w, x, w_k, key_pool, block_table, ctx_lens, ws,
+                     q8_out=None, w_out=None, stream=None):
+    """The fused front end: query norm -> projection -> FP8 q with folded weights
+    (into the workspace, for a following call with DSA_Q_PREPARED) and the new
+    tokens' index keys written into key_pool."""
+    _check("dsa_indexer_frontend", load().dsa_indexer_frontend(
+        ctypes.byref(params), ctypes.byref(dims), _ptr(c_q), _ptr(gamma_q), _ptr(w_q), _ptr(w), _ptr(x),
+        _ptr(w_k), _ptr(key_pool), _ptr(block_table), _ptr(ctx_lens), _ptr(q8_out), _ptr(w_out), _ptr(ws),
+        _nbytes(ws), _stream(stream)))
 
 
 def topk(params, scores, score_stride, ctx_lens, block_table, topk_idx, phys_rows, ws, stream=None):

@@ -1,6 +1,7 @@
 // libdsa C ABI: host-side validation, workspace carving and stage launches.
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 
 #include "dsa_internal.cuh"
 
@@ -28,7 +29,7 @@ dsa_status_t check_params(const dsa_params_t* p) {
   if (p->key_page_stride < key_page || (p->key_page_stride & 15)) return DSA_ERR_INVALID;
   if (p->lat_page_stride < lat_page || (p->lat_page_stride & 15)) return DSA_ERR_INVALID;
   if (!(p->softmax_scale > 0.f) || !(p->latent_scale > 0.f)) return DSA_ERR_INVALID;
-  if (p->flags & ~int32_t(DSA_EMIT_PHYS_ROWS)) return DSA_ERR_INVALID;
+  if (p->flags & ~int32_t(DSA_EMIT_PHYS_ROWS | DSA_Q_PREPARED)) return DSA_ERR_INVALID;
   // keep every index of the kernels inside int32 / the grid limits
   if (int64_t(p->max_pages_per_req) * p->page_size > (int64_t(1) << 28)) return DSA_ERR_UNSUPPORTED;
   if (int64_t(p->batch) * p->n_q > 65535) return DSA_ERR_UNSUPPORTED;
@@ -46,7 +47,9 @@ dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA
 
 dsa_status_t check_indexer_args(const dsa_params_t* p, const void* q_idx, const float* w,
                                 const void* key_pool, const int32_t* bt, const int32_t* ctx) {
-  if (!q_idx || !w || !key_pool || !bt || !ctx) return DSA_ERR_INVALID;
+  if (!key_pool || !bt || !ctx || !aligned16(key_pool)) return DSA_ERR_INVALID;
+  if (p->flags & DSA_Q_PREPARED) return DSA_OK;  // the query is already in the workspace
+  if (!q_idx || !w) return DSA_ERR_INVALID;
   if (!aligned16(q_idx) || !aligned16(key_pool) || (reinterpret_cast<uintptr_t>(w) & 3)) return DSA_ERR_INVALID;
   return DSA_OK;
 }
@@ -81,7 +84,8 @@ dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, c
   WsLayout L;
   if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
   char* w8 = static_cast<char*>(ws);
-  cudaError_t e = launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
+  cudaError_t e = (params->flags & DSA_Q_PREPARED) ? cudaSuccess
+                                                   : launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
   if (e == cudaSuccess)
     e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, score_stride, stream);
   return cuda_status(e);
@@ -99,6 +103,28 @@ dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t s
   if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
   return cuda_status(launch_topk(*params, L, static_cast<char*>(ws), scores, score_stride, ctx_lens,
                                  block_table, topk_idx, phys_rows, stream));
+}
+
+dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend_dims_t* dims, const void* c_q,
+                                  const void* gamma_q, const void* w_q, const float* w, const void* x,
+                                  const void* w_k, void* key_pool, const int32_t* block_table,
+                                  const int32_t* ctx_lens, void* q8_out, float* w_out, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if (!dims) return DSA_ERR_INVALID;
+  for (int d : {dims->d_c, dims->d_model})
+    if (d < 256 || d > 8192 || (d % 256)) return DSA_ERR_UNSUPPORTED;
+  if (!(dims->eps >= 0.f) || !(dims->eps < 1e30f)) return DSA_ERR_INVALID;
+  for (const void* ptr : {c_q, gamma_q, w_q, x, w_k, static_cast<const void*>(key_pool)})
+    if (!ptr || !aligned16(ptr)) return DSA_ERR_INVALID;
+  if (!w || (reinterpret_cast<uintptr_t>(w) & 3) || !block_table || !ctx_lens) return DSA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(q8_out) & 3) || (reinterpret_cast<uintptr_t>(w_out) & 3)) return DSA_ERR_INVALID;
+  WsLayout L;
+  if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
+  FrontendIn in{c_q, gamma_q, w_q, w, x, w_k, key_pool, block_table, ctx_lens, q8_out, w_out,
+                dims->d_c, dims->d_model, dims->eps};
+  return cuda_status(launch_idx_frontend(*params, L, static_cast<char*>(ws), in, stream));
 }
 
 dsa_status_t dsa_dcp_topk_merge(const dsa_params_t* params, const float* scores, int64_t score_stride,
@@ -152,7 +178,8 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
   char* w8 = static_cast<char*>(ws);
   if (!topk_idx_out) topk_idx_out = reinterpret_cast<int32_t*>(w8 + L.topk);
   float* scores = reinterpret_cast<float*>(w8 + L.scores);
-  cudaError_t e = launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
+  cudaError_t e = (params->flags & DSA_Q_PREPARED) ? cudaSuccess
+                                                   : launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
   if (e == cudaSuccess) e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, L.cap, stream);
   if (e == cudaSuccess)
     e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream);

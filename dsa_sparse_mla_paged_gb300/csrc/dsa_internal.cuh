@@ -148,6 +148,40 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int
 // ---------------------------------------------------------------- launchers
 // (each returns cudaGetLastError() of its launches)
 
+// Work plan of the scorer, by one CTA of NT threads: tiles of 128 tokens (two
+// pages) per request, inclusive prefix over the batch. An invalid context
+// length gets no tiles and sets DSA_DEVERR_CTX.
+template <int NT>
+__device__ __forceinline__ void build_tile_plan(const int32_t* __restrict__ ctx_lens, int batch, int n_q, int cap,
+                                                int* __restrict__ tile_prefix, int* err) {
+  constexpr int NW = NT / 32;
+  __shared__ int wsum[NW];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int carry = 0;
+  for (int b0 = 0; b0 < batch; b0 += NT) {
+    const int b = b0 + int(threadIdx.x);
+    int n = 0;
+    if (b < batch) {
+      const int c = ctx_lens[b];
+      if (c < n_q || c > cap) atomicOr(err, DSA_DEVERR_CTX);
+      else n = (c + 127) >> 7;
+    }
+    int x = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int pre = carry;
+    for (int i = 0; i < warp; ++i) pre += wsum[i];
+    if (b < batch) tile_prefix[b] = pre + x;
+    for (int i = 0; i < NW; ++i) carry += wsum[i];
+    __syncthreads();
+  }
+}
+
 cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
                                const float* w, const int32_t* ctx_lens, cudaStream_t st);
 cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
@@ -161,6 +195,23 @@ cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws,
                              int32_t* stats, cudaStream_t st);
 cudaError_t launch_dcp_lse_combine(int rows, int parts, const void* part_out, const float* part_lse, void* out,
                                    float* lse, cudaStream_t st);
+struct FrontendIn {
+  const void* c_q;
+  const void* gamma;
+  const void* w_q;
+  const float* w;
+  const void* x;
+  const void* w_k;
+  void* key_pool;
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  void* q8_out;
+  float* w_out;
+  int d_c, d_model;
+  float eps;
+};
+cudaError_t launch_idx_frontend(const dsa_params_t& p, const WsLayout& L, char* ws, const FrontendIn& in,
+                                cudaStream_t st);
 cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q,
                               const void* lat_pool, const int32_t* block_table,
                               const int32_t* ctx_lens, const int32_t* topk_idx, void* out,

@@ -1,0 +1,295 @@
+// The fused indexer front end of a decode step ("vLLM 为 Kimi K3.1 Pro 提供 Day-0
+// 支持", section "低延迟解码：融合的 DSA 解码路径": the query norm, the indexer's
+// query projection, its FP8 quantisation folded into the head weights and the
+// new token's index key, in one kernel). For query row (b, t):
+//   n  = bf16(c_q / sqrt(mean(c_q^2) + eps) * gamma)       query RMS norm
+//   q  = bf16(n @ W_q^T)                                    32 heads x 128
+//   q8 = E4M3(q * 448 / amax_h), w' = w * (amax_h / 448)    the scorer's inputs
+//   k  = bf16(x @ W_k^T)                                    the new token's key
+// and k goes, FP8 (E4M3 + fp32 scale) or MXFP4 (E2M1 + E8M0 per 32), into the
+// cache slot of token ctx_b - n_q + t.
+//
+// Grid: clusters of 8 CTAs. Cluster j < 32 computes head j, cluster 32 the key,
+// and the first CTA of cluster 33 writes the scorer's tile plan. A CTA owns 16
+// of its cluster's 128 outputs: it streams those 16 weight rows (once per
+// group of 8 query rows) against the group's inputs staged in shared memory,
+// and sends each output, rounded to bf16, to the cluster's first CTA through
+// distributed shared memory; that CTA quantises the 128 values of every row
+// and writes them. A decode step is bound by the weight bytes.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "dsa_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kFeCluster = 8;
+constexpr int kFeThreads = 256;  // 8 warps x 2 outputs
+constexpr int kFeRows = 8;       // query rows per pass
+constexpr int kFeOut = kIdxDim / kFeCluster;
+static_assert(kFeOut == 2 * (kFeThreads / 32), "two outputs per warp");
+
+struct FeArgs {
+  const __nv_bfloat16* c_q;
+  const __nv_bfloat16* gamma;
+  const __nv_bfloat16* w_q;
+  const float* w;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* w_k;
+  uint8_t* key_pool;
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  uint8_t* q8;
+  float* wq;
+  uint8_t* q8_out;
+  float* w_out;
+  int* tile_prefix;
+  int* err;
+  int64_t key_page_stride;
+  int rows, batch, n_q, d_c, d_model, max_pages, num_pages, cap, mx;
+  float eps;
+};
+
+__device__ __forceinline__ void bf16x8(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// E2M1 code of y: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6} with ties to the even
+// code, magnitudes past 6 saturating, the sign bit kept.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  const uint32_t mag = a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u
+                     : a <= 2.5f ? 4u : a < 3.5f ? 5u : a <= 5.0f ? 6u : 7u;
+  return mag | (signbit(y) ? 8u : 0u);
+}
+
+// 2^-e for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float exp2_neg(int e) {
+  return e <= 126 ? __uint_as_float(uint32_t(127 - e) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Rank-0 epilogue of one row: the 128 bf16 outputs of the row (4 per lane).
+__device__ __forceinline__ void head_out(const FeArgs& a, int row, int h, int lane, const float (&v)[4]) {
+  const float m = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+  const float inv = m > 0.f ? __fdiv_rn(448.0f, m) : 1.0f;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    packed |= uint32_t(__nv_cvt_float_to_fp8(__fmul_rn(v[i], inv), __NV_SATFINITE, __NV_E4M3)) << (8 * i);
+  const size_t off = (size_t(row) * kIdxHeads + h) * kIdxDim + lane * 4;
+  *reinterpret_cast<uint32_t*>(a.q8 + off) = packed;
+  if (a.q8_out) *reinterpret_cast<uint32_t*>(a.q8_out + off) = packed;
+  if (lane == 0) {
+    const float wp = __fmul_rn(a.w[size_t(row) * kIdxHeads + h], __fdiv_rn(m, 448.0f));
+    a.wq[size_t(row) * kIdxHeads + h] = wp;
+    if (a.w_out) a.w_out[size_t(row) * kIdxHeads + h] = wp;
+  }
+}
+
+__device__ __forceinline__ void key_out(const FeArgs& a, int row, int lane, const float (&v)[4]) {
+  const int b = row / a.n_q, t = row - b * a.n_q;
+  const int ctx = a.ctx_lens[b];
+  if (ctx < a.n_q || ctx > a.cap) {
+    if (lane == 0) atomicOr(a.err, DSA_DEVERR_CTX);
+    return;
+  }
+  const int pos = ctx - a.n_q + t;
+  const int pg = a.block_table[size_t(b) * a.max_pages + pos / kPage];
+  if (pg < 0 || pg >= a.num_pages) {
+    if (lane == 0) atomicOr(a.err, DSA_DEVERR_BLOCK_TABLE);
+    return;
+  }
+  uint8_t* page = a.key_pool + size_t(pg) * a.key_page_stride;
+  const int slot = pos % kPage;
+  if (!a.mx) {
+    const float m = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+    const float inv = m > 0.f ? __fdiv_rn(448.0f, m) : 1.0f;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      packed |= uint32_t(__nv_cvt_float_to_fp8(__fmul_rn(v[i], inv), __NV_SATFINITE, __NV_E4M3)) << (8 * i);
+    *reinterpret_cast<uint32_t*>(page + slot * kIdxDim + lane * 4) = packed;
+    if (lane == 0) *reinterpret_cast<float*>(page + kPage * kIdxDim + slot * 4) = __fdiv_rn(m, 448.0f);
+  } else {
+    // lanes 8g .. 8g + 7 hold block g (values 32g .. 32g + 31)
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 4; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    int e = 0;
+    if (m > 0.f) {
+      const int ex = int((__float_as_uint(m) >> 23) & 0xFFu);  // floor(log2 m) + 127 for a normal m
+      e = max(-127, min(127, ex - 127 - 2));
+    }
+    const float s = exp2_neg(e);
+    const uint32_t c0 = e2m1_code(__fmul_rn(v[0], s)), c1 = e2m1_code(__fmul_rn(v[1], s));
+    const uint32_t c2 = e2m1_code(__fmul_rn(v[2], s)), c3 = e2m1_code(__fmul_rn(v[3], s));
+    *reinterpret_cast<uint16_t*>(page + slot * 64 + lane * 2) = uint16_t(c0 | c1 << 4 | c2 << 8 | c3 << 12);
+    if ((lane & 7) == 0) page[kPage * 64 + slot * 4 + (lane >> 3)] = uint8_t(e + 127);
+  }
+}
+
+__global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads, 1)
+    idx_frontend_kernel(FeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(16) uint8_t fe_smem[];
+  __shared__ __align__(16) float gath[kFeRows][kIdxDim];  // the first CTA: every output of the pass
+  const int job = blockIdx.y;
+  if (job == kIdxHeads + 1) {  // the tile plan (no cluster traffic in this cluster)
+    if (blockIdx.x == 0) build_tile_plan<kFeThreads>(a.ctx_lens, a.batch, a.n_q, a.cap, a.tile_prefix, a.err);
+    return;
+  }
+  ptx::cluster_sync();  // every CTA of the cluster runs before any remote store
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool is_key = job == kIdxHeads;
+  const int d = is_key ? a.d_model : a.d_c;
+  const int nch = d / 256;  // 16-byte chunks per lane per row
+  __nv_bfloat16* in = reinterpret_cast<__nv_bfloat16*>(fe_smem);  // [kFeRows][d]
+  const int o0 = int(rank) * kFeOut + 2 * warp;                   // this warp's outputs o0, o0 + 1
+  const __nv_bfloat16* w0 = is_key ? a.w_k + size_t(o0) * d : a.w_q + (size_t(job) * kIdxDim + o0) * d;
+  const __nv_bfloat16* w1 = w0 + d;
+  for (int r0 = 0; r0 < a.rows; r0 += kFeRows) {
+    const int nr = min(kFeRows, a.rows - r0);
+    // ---- stage the pass's inputs: warp w prepares row r0 + w
+    if (warp < nr) {
+      const int row = r0 + warp;
+      __nv_bfloat16* dst = in + size_t(warp) * d;
+      if (is_key) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + size_t(row) * d);
+        for (int j = 0; j < nch; ++j) reinterpret_cast<uint4*>(dst)[j * 32 + lane] = __ldg(src + j * 32 + lane);
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(row) * d);
+        float ss = 0.f;
+        for (int j = 0; j < nch; ++j) {
+          float f[8];
+          bf16x8(__ldg(src + j * 32 + lane), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(d)), a.eps)));
+        const uint4* g = reinterpret_cast<const uint4*>(a.gamma);
+        for (int j = 0; j < nch; ++j) {
+          float f[8], gg[8];
+          bf16x8(__ldg(src + j * 32 + lane), f);
+          bf16x8(__ldg(g + j * 32 + lane), gg);
+          uint4 o;
+          __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            oh[i] = __halves2bfloat162(__float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i], rstd), gg[2 * i])),
+                                       __float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], rstd), gg[2 * i + 1])));
+          reinterpret_cast<uint4*>(dst)[j * 32 + lane] = o;
+        }
+      }
+    }
+    __syncthreads();
+    // ---- the warp's two weight rows against the pass's rows
+    float acc0[kFeRows], acc1[kFeRows];
+#pragma unroll
+    for (int rr = 0; rr < kFeRows; ++rr) acc0[rr] = acc1[rr] = 0.f;
+    const uint4* pw0 = reinterpret_cast<const uint4*>(w0);
+    const uint4* pw1 = reinterpret_cast<const uint4*>(w1);
+#pragma unroll 4
+    for (int j = 0; j < nch; ++j) {
+      float f0[8], f1[8];
+      bf16x8(__ldg(pw0 + j * 32 + lane), f0);
+      bf16x8(__ldg(pw1 + j * 32 + lane), f1);
+#pragma unroll
+      for (int rr = 0; rr < kFeRows; ++rr) {
+        float xv[8];
+        bf16x8(reinterpret_cast<const uint4*>(in + size_t(rr) * d)[j * 32 + lane], xv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc0[rr] = fmaf(f0[i], xv[i], acc0[rr]);
+          acc1[rr] = fmaf(f1[i], xv[i], acc1[rr]);
+        }
+      }
+    }
+    // lane 8i + rr keeps output o0 + i of row rr
+    float mine = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < kFeRows; ++rr) {
+      float s0 = acc0[rr], s1 = acc1[rr];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      }
+      if (lane == rr) mine = s0;
+      if (lane == 8 + rr) mine = s1;
+    }
+    if (lane < 16 && (lane & 7) < nr) {
+      const float vb = __bfloat162float(__float2bfloat16_rn(mine));
+      const uint32_t local = ptx::smem_u32(&gath[lane & 7][o0 + (lane >> 3)]);
+      ptx::st_cluster_u32(ptx::mapa_shared(local, 0), __float_as_uint(vb));
+    }
+    ptx::cluster_sync();  // the first CTA holds the pass's outputs
+    if (rank == 0 && warp < nr) {
+      const float4 g4 = *reinterpret_cast<const float4*>(&gath[warp][lane * 4]);
+      const float v[4] = {g4.x, g4.y, g4.z, g4.w};
+      if (is_key) key_out(a, r0 + warp, lane, v);
+      else head_out(a, r0 + warp, job, lane, v);
+    }
+    ptx::cluster_sync();  // read before the next pass writes gath again (and the staged rows)
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_idx_frontend(const dsa_params_t& p, const WsLayout& L, char* ws, const FrontendIn& in,
+                                cudaStream_t st) {
+  FeArgs a;
+  a.c_q = static_cast<const __nv_bfloat16*>(in.c_q);
+  a.gamma = static_cast<const __nv_bfloat16*>(in.gamma);
+  a.w_q = static_cast<const __nv_bfloat16*>(in.w_q);
+  a.w = in.w;
+  a.x = static_cast<const __nv_bfloat16*>(in.x);
+  a.w_k = static_cast<const __nv_bfloat16*>(in.w_k);
+  a.key_pool = static_cast<uint8_t*>(in.key_pool);
+  a.block_table = in.block_table;
+  a.ctx_lens = in.ctx_lens;
+  a.q8 = reinterpret_cast<uint8_t*>(ws + L.q8);
+  a.wq = reinterpret_cast<float*>(ws + L.wq);
+  a.q8_out = static_cast<uint8_t*>(in.q8_out);
+  a.w_out = in.w_out;
+  a.tile_prefix = reinterpret_cast<int*>(ws + L.tiles);
+  a.err = reinterpret_cast<int*>(ws + L.err);
+  a.key_page_stride = p.key_page_stride;
+  a.rows = L.rows;
+  a.batch = p.batch;
+  a.n_q = p.n_q;
+  a.d_c = in.d_c;
+  a.d_model = in.d_model;
+  a.max_pages = p.max_pages_per_req;
+  a.num_pages = p.num_pages;
+  a.cap = L.cap;
+  a.mx = p.key_fmt == DSA_KEY_MXFP4_68;
+  a.eps = in.eps;
+  const size_t smem = size_t(kFeRows) * size_t(std::max(in.d_c, in.d_model)) * 2;
+  cudaError_t e = cudaFuncSetAttribute(idx_frontend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e == cudaSuccess)
+    e = launch_pdl(idx_frontend_kernel, dim3(kFeCluster, kIdxHeads + 2), dim3(kFeThreads), smem, st, a);
+  return e;
+}
+
+}  // namespace dsa

@@ -35,32 +35,7 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (row == gridDim.x - 1) {
-    // Work plan of the scorer: tiles of 128 tokens (two pages) per request,
-    // inclusive prefix over the batch. An invalid context length gets no tiles.
-    __shared__ int wsum[4];
-    int carry = 0;
-    for (int b0 = 0; b0 < batch; b0 += 128) {
-      const int b = b0 + threadIdx.x;
-      int n = 0;
-      if (b < batch) {
-        const int c = ctx_lens[b];
-        if (c < n_q || c > cap) atomicOr(err, DSA_DEVERR_CTX);
-        else n = (c + 127) >> 7;
-      }
-      int x = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (lane == 31) wsum[warp] = x;
-      __syncthreads();
-      int pre = carry;
-      for (int i = 0; i < warp; ++i) pre += wsum[i];
-      if (b < batch) tile_prefix[b] = pre + x;
-      carry += wsum[0] + wsum[1] + wsum[2] + wsum[3];
-      __syncthreads();
-    }
+    build_tile_plan<128>(ctx_lens, batch, n_q, cap, tile_prefix, err);
     return;
   }
   // all eight heads' loads first (independent), then the per-head reductions

@@ -81,6 +81,10 @@ typedef enum { DSA_LAT_FP8_576 = 0, DSA_LAT_NVFP4_352 = 1 } dsa_lat_fmt_t;
 
 /* flags */
 #define DSA_EMIT_PHYS_ROWS 0x1  /* dsa_topk also writes physical cache rows */
+#define DSA_Q_PREPARED 0x2      /* dsa_indexer_scores / dsa_decode take the quantised query,
+                                   the folded weights and the scorer's plan that
+                                   dsa_indexer_frontend left in the same workspace (same
+                                   params and ctx_lens); q_idx and w may be NULL */
 
 /* Device error word bits (dsa_get_device_error). */
 #define DSA_DEVERR_BLOCK_TABLE 0x1  /* a block-table entry outside [0, num_pages) */
@@ -179,6 +183,40 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
                         const int32_t* block_table, const int32_t* ctx_lens, void* out,
                         float* lse, int32_t* topk_idx_out, void* ws, size_t ws_bytes,
                         cudaStream_t stream);
+
+/* Widths of the fused front end's inputs (not fixed by the article). */
+typedef struct {
+  int32_t d_c;      /* query latent width, the query norm's input: 256 .. 8192, a multiple of 256 */
+  int32_t d_model;  /* hidden width, the key projection's input: 256 .. 8192, a multiple of 256 */
+  float eps;        /* RMS norm epsilon, >= 0 */
+} dsa_frontend_dims_t;
+
+/* The fused indexer front end ("低延迟解码：融合的 DSA 解码路径": the query norm,
+ * the indexer's query projection, its FP8 quantisation folded into the head
+ * weights and the new token's index key, in one kernel). For row (b, t):
+ *   n  = bf16(c_q / sqrt(mean(c_q^2) + eps) * gamma_q)     (fp32 arithmetic)
+ *   q  = bf16(n @ w_q^T), q[h] = q[128 h .. 128 h + 127]   (fp32 accumulation)
+ *   q8[h] = E4M3_rne_satfinite(q[h] * (448 / amax_h)), w'[h] = w[h] * (amax_h / 448)
+ *        (the recipe of dsa_indexer_scores' own quantisation)
+ *   k  = bf16(x @ w_k^T), quantised to the key format (FP8: one fp32 scale
+ *        amax / 448 per token, codes E4M3(k * 448 / amax); MXFP4: per 32 values
+ *        E8M0 exponent e = floor(log2 amax) - 2 and E2M1(v / 2^e), nearest-even,
+ *        saturating) and written to the cache slot of token ctx_b - n_q + t.
+ * The quantised query, w' and the scorer's plan go to the workspace, where a
+ * following dsa_indexer_scores / dsa_decode with DSA_Q_PREPARED reads them.
+ *   c_q     bf16 [B * n_q, d_c]          gamma_q bf16 [d_c]
+ *   w_q     bf16 [32 * 128, d_c]         (a linear layer's [out, in] weight)
+ *   w       fp32 [B * n_q, 32]           head weights
+ *   x       bf16 [B * n_q, d_model]      w_k bf16 [128, d_model]
+ *   key_pool written at one slot per row (16-B aligned, like every bf16 input)
+ *   q8_out  E4M3 [B * n_q, 32, 128] or NULL; w_out fp32 [B * n_q, 32] or NULL (copies)
+ * Errors: a row with an invalid ctx_b or block-table entry writes no key and
+ * sets DSA_DEVERR_CTX / DSA_DEVERR_BLOCK_TABLE in the workspace. */
+dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend_dims_t* dims, const void* c_q,
+                                  const void* gamma_q, const void* w_q, const float* w, const void* x,
+                                  const void* w_k, void* key_pool, const int32_t* block_table,
+                                  const int32_t* ctx_lens, void* q8_out, float* w_out, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream);
 
 /* Stage 2 as W decode-context-parallel GPUs would run it, emulated on one GPU
  * ("vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "长上下文：带稀疏 indexer 的

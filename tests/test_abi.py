@@ -143,3 +143,33 @@ def test_lse_combine_arguments_checked(lib):
     assert L.dsa_lse_combine(ctypes.byref(p), 4, None, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID
     assert L.dsa_lse_combine(ctypes.byref(p), 4, FAKE + 2, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID
     assert L.dsa_lse_combine(ctypes.byref(p), 4, FAKE, FAKE, FAKE + 8, None, None) == dsa.DSA_ERR_INVALID
+
+
+def test_frontend_arguments_checked(lib):
+    p = _params()
+    need = dsa.workspace_size(p)
+    L = lib
+    ok = dsa.FrontendDims(d_c=1536, d_model=7168, eps=1e-6)
+    args = lambda dims, cq=FAKE, w=FAKE: (ctypes.byref(p), ctypes.byref(dims), cq, FAKE, FAKE, w, FAKE, FAKE, FAKE,
+                                          FAKE, FAKE, None, None, FAKE, need, None)
+    for bad in (dsa.FrontendDims(d_c=1000, d_model=7168), dsa.FrontendDims(d_c=1536, d_model=16384),
+                dsa.FrontendDims(d_c=0, d_model=256)):
+        assert L.dsa_indexer_frontend(*args(bad)) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_indexer_frontend(*args(dsa.FrontendDims(d_c=256, d_model=256, eps=-1.0))) == dsa.DSA_ERR_INVALID
+    assert L.dsa_indexer_frontend(*args(ok, cq=None)) == dsa.DSA_ERR_INVALID
+    assert L.dsa_indexer_frontend(*args(ok, cq=FAKE + 8)) == dsa.DSA_ERR_INVALID
+    assert L.dsa_indexer_frontend(*args(ok, w=FAKE + 2)) == dsa.DSA_ERR_INVALID
+    a = list(args(ok))
+    a[14] = need - 1
+    assert L.dsa_indexer_frontend(*a) == dsa.DSA_ERR_WORKSPACE
+
+
+def test_prepared_flag_lets_the_query_be_null(lib):
+    p = _params(flags=dsa.DSA_Q_PREPARED)
+    need = dsa.workspace_size(p)
+    # passes validation up to the workspace size check (no launch)
+    st = lib.dsa_indexer_scores(ctypes.byref(p), None, None, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need - 1, None)
+    assert st == dsa.DSA_ERR_WORKSPACE
+    q = _params()
+    st = lib.dsa_indexer_scores(ctypes.byref(q), None, None, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need, None)
+    assert st == dsa.DSA_ERR_INVALID
