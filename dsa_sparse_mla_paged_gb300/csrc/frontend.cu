@@ -11,8 +11,10 @@
 //
 // Grid: clusters of 8 CTAs. Cluster j < 32 computes head j, cluster 32 the key,
 // and the first CTA of cluster 33 writes the scorer's tile plan. A CTA owns 16
-// of its cluster's 128 outputs: it streams those 16 weight rows (once per
-// group of 8 query rows) against the group's inputs staged in shared memory,
+// of its cluster's 128 outputs: it prefetches those 16 weight rows into L2 at
+// launch, then streams them (once per group of 8 query rows) against the
+// group's inputs, staged in shared memory 2,048 columns at a time (32 KB, so
+// two CTAs fit an SM and the 272 CTAs run in one wave),
 // and sends each output, rounded to bf16, to the cluster's first CTA through
 // distributed shared memory; that CTA quantises the 128 values of every row
 // and writes them. A decode step is bound by the weight bytes.
@@ -32,6 +34,7 @@ constexpr int kFeCluster = 8;
 constexpr int kFeThreads = 256;  // 8 warps x 2 outputs
 constexpr int kFeRows = 8;       // query rows per pass
 constexpr int kFeOut = kIdxDim / kFeCluster;
+constexpr int kFeBlk = 8;        // 16-byte chunks per lane per staged block: 2,048 inputs per row
 static_assert(kFeOut == 2 * (kFeThreads / 32), "two outputs per warp");
 
 struct FeArgs {
@@ -148,7 +151,6 @@ __device__ __forceinline__ void key_out(const FeArgs& a, int row, int lane, cons
 __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads, 1)
     idx_frontend_kernel(FeArgs a) {
   pdl_trigger();
-  pdl_wait();
   extern __shared__ __align__(16) uint8_t fe_smem[];
   __shared__ __align__(16) float gath[kFeRows][kIdxDim];  // the first CTA: every output of the pass
   const int job = blockIdx.y;
@@ -156,72 +158,87 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
     if (blockIdx.x == 0) build_tile_plan<kFeThreads>(a.ctx_lens, a.batch, a.n_q, a.cap, a.tile_prefix, a.err);
     return;
   }
-  ptx::cluster_sync();  // every CTA of the cluster runs before any remote store
   const uint32_t rank = ptx::cluster_ctarank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_key = job == kIdxHeads;
   const int d = is_key ? a.d_model : a.d_c;
   const int nch = d / 256;  // 16-byte chunks per lane per row
-  __nv_bfloat16* in = reinterpret_cast<__nv_bfloat16*>(fe_smem);  // [kFeRows][d]
+  __nv_bfloat16* in = reinterpret_cast<__nv_bfloat16*>(fe_smem);  // [kFeRows][kFeBlk * 256]
   const int o0 = int(rank) * kFeOut + 2 * warp;                   // this warp's outputs o0, o0 + 1
   const __nv_bfloat16* w0 = is_key ? a.w_k + size_t(o0) * d : a.w_q + (size_t(job) * kIdxDim + o0) * d;
   const __nv_bfloat16* w1 = w0 + d;
+  // The weights are constants of the model, not outputs of the previous
+  // kernel: start pulling this CTA's 16 rows into L2 before waiting on it.
+  const __nv_bfloat16* wcta = w0 - size_t(2 * warp) * d;  // the CTA's first weight row
+  if (threadIdx.x < kFeOut) ptx::prefetch_l2_bulk(wcta + size_t(threadIdx.x) * d, uint32_t(d) * 2);
+  pdl_wait();
+  ptx::cluster_sync();  // every CTA of the cluster runs before any remote store
+  __shared__ float s_rstd[kFeRows];
   for (int r0 = 0; r0 < a.rows; r0 += kFeRows) {
     const int nr = min(kFeRows, a.rows - r0);
-    // ---- stage the pass's inputs: warp w prepares row r0 + w
-    if (warp < nr) {
-      const int row = r0 + warp;
-      __nv_bfloat16* dst = in + size_t(warp) * d;
-      if (is_key) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.x + size_t(row) * d);
-        for (int j = 0; j < nch; ++j) reinterpret_cast<uint4*>(dst)[j * 32 + lane] = __ldg(src + j * 32 + lane);
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(row) * d);
-        float ss = 0.f;
-        for (int j = 0; j < nch; ++j) {
-          float f[8];
-          bf16x8(__ldg(src + j * 32 + lane), f);
+    // ---- the query rows' 1 / RMS (warp w: row r0 + w)
+    if (!is_key && warp < nr) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(r0 + warp) * d);
+      float ss = 0.f;
+      for (int j = 0; j < nch; ++j) {
+        float f[8];
+        bf16x8(__ldg(src + j * 32 + lane), f);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(d)), a.eps)));
-        const uint4* g = reinterpret_cast<const uint4*>(a.gamma);
-        for (int j = 0; j < nch; ++j) {
-          float f[8], gg[8];
-          bf16x8(__ldg(src + j * 32 + lane), f);
-          bf16x8(__ldg(g + j * 32 + lane), gg);
-          uint4 o;
-          __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            oh[i] = __halves2bfloat162(__float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i], rstd), gg[2 * i])),
-                                       __float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], rstd), gg[2 * i + 1])));
-          reinterpret_cast<uint4*>(dst)[j * 32 + lane] = o;
-        }
+        for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
       }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_rstd[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(d)), a.eps)));
     }
-    __syncthreads();
-    // ---- the warp's two weight rows against the pass's rows
     float acc0[kFeRows], acc1[kFeRows];
 #pragma unroll
     for (int rr = 0; rr < kFeRows; ++rr) acc0[rr] = acc1[rr] = 0.f;
-    const uint4* pw0 = reinterpret_cast<const uint4*>(w0);
-    const uint4* pw1 = reinterpret_cast<const uint4*>(w1);
+    for (int jb = 0; jb < nch; jb += kFeBlk) {
+      const int nj = min(kFeBlk, nch - jb);
+      __syncthreads();  // the previous block's inputs are consumed (and s_rstd is written)
+      // ---- stage the block's inputs: warp w prepares row r0 + w, chunks jb .. jb + nj - 1
+      if (warp < nr) {
+        const int row = r0 + warp;
+        uint4* dst = reinterpret_cast<uint4*>(in) + size_t(warp) * kFeBlk * 32;
+        if (is_key) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.x + size_t(row) * d) + jb * 32;
+          for (int j = 0; j < nj; ++j) dst[j * 32 + lane] = __ldg(src + j * 32 + lane);
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(row) * d) + jb * 32;
+          const uint4* g = reinterpret_cast<const uint4*>(a.gamma) + jb * 32;
+          const float rstd = s_rstd[warp];
+          for (int j = 0; j < nj; ++j) {
+            float f[8], gg[8];
+            bf16x8(__ldg(src + j * 32 + lane), f);
+            bf16x8(__ldg(g + j * 32 + lane), gg);
+            uint4 o;
+            __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              oh[i] = __halves2bfloat162(__float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i], rstd), gg[2 * i])),
+                                         __float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], rstd), gg[2 * i + 1])));
+            dst[j * 32 + lane] = o;
+          }
+        }
+      }
+      __syncthreads();
+      // ---- the warp's two weight rows against the block's rows
+      const uint4* pw0 = reinterpret_cast<const uint4*>(w0) + jb * 32;
+      const uint4* pw1 = reinterpret_cast<const uint4*>(w1) + jb * 32;
 #pragma unroll 4
-    for (int j = 0; j < nch; ++j) {
-      float f0[8], f1[8];
-      bf16x8(__ldg(pw0 + j * 32 + lane), f0);
-      bf16x8(__ldg(pw1 + j * 32 + lane), f1);
+      for (int j = 0; j < nj; ++j) {
+        float f0[8], f1[8];
+        bf16x8(__ldg(pw0 + j * 32 + lane), f0);
+        bf16x8(__ldg(pw1 + j * 32 + lane), f1);
 #pragma unroll
-      for (int rr = 0; rr < kFeRows; ++rr) {
-        float xv[8];
-        bf16x8(reinterpret_cast<const uint4*>(in + size_t(rr) * d)[j * 32 + lane], xv);
+        for (int rr = 0; rr < kFeRows; ++rr) {
+          float xv[8];
+          bf16x8(reinterpret_cast<const uint4*>(in)[(size_t(rr) * kFeBlk + j) * 32 + lane], xv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc0[rr] = fmaf(f0[i], xv[i], acc0[rr]);
-          acc1[rr] = fmaf(f1[i], xv[i], acc1[rr]);
+          for (int i = 0; i < 8; ++i) {
+            acc0[rr] = fmaf(f0[i], xv[i], acc0[rr]);
+            acc1[rr] = fmaf(f1[i], xv[i], acc1[rr]);
+          }
         }
       }
     }
@@ -285,7 +302,7 @@ cudaError_t launch_idx_frontend(const dsa_params_t& p, const WsLayout& L, char* 
   a.cap = L.cap;
   a.mx = p.key_fmt == DSA_KEY_MXFP4_68;
   a.eps = in.eps;
-  const size_t smem = size_t(kFeRows) * size_t(std::max(in.d_c, in.d_model)) * 2;
+  const size_t smem = size_t(kFeRows) * kFeBlk * 256 * 2;
   cudaError_t e = cudaFuncSetAttribute(idx_frontend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e == cudaSuccess)
     e = launch_pdl(idx_frontend_kernel, dim3(kFeCluster, kIdxHeads + 2), dim3(kFeThreads), smem, st, a);
