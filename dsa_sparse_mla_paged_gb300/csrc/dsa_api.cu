@@ -116,6 +116,7 @@ dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend
   for (int d : {dims->d_c, dims->d_model})
     if (d < 256 || d > 8192 || (d % 256)) return DSA_ERR_UNSUPPORTED;
   if (!(dims->eps >= 0.f) || !(dims->eps < 1e30f)) return DSA_ERR_INVALID;
+  if (int64_t(params->batch) * params->n_q > kFeMaxRows) return DSA_ERR_UNSUPPORTED;
   for (const void* ptr : {c_q, gamma_q, w_q, x, w_k, static_cast<const void*>(key_pool)})
     if (!ptr || !aligned16(ptr)) return DSA_ERR_INVALID;
   if (!w || (reinterpret_cast<uintptr_t>(w) & 3) || !block_table || !ctx_lens) return DSA_ERR_INVALID;

@@ -38,6 +38,10 @@ constexpr int kMaxSplits = (kMaxTopK + kSplitTok - 1) / kSplitTok;
 // emulated decode context parallelism: at most this many token shards
 constexpr int kDcpMaxWorld = 16;
 
+// the fused front end handles at most this many query rows (64 passes of 8)
+constexpr int kFeMaxRows = 512;
+constexpr int kFeMaxPasses = kFeMaxRows / 4;
+
 // Byte offsets of the workspace regions (all 256-B aligned).
 struct WsLayout {
   size_t err;       // int32 error word
@@ -53,6 +57,8 @@ struct WsLayout {
   size_t dcp_key;   // uint32 [rows][kDcpMaxWorld][topk] shard lists: bf16 keys by position
   size_t dcp_tok;   // int32 [rows][kDcpMaxWorld][topk] shard lists: tokens by position
   size_t dcp_cnt;   // int32 [rows][kDcpMaxWorld] shard list lengths
+  size_t fe_part;   // fp32 [4][rows][128] the front end's key partial sums
+  size_t fe_cnt;    // int32 [kFeMaxPasses] the front end's per-pass arrival counters
   size_t dcp_keys16;  // uint16 [rows][W][S] shard-major score keys, W * S <= cap + 8 * kDcpMaxWorld
   size_t scores;    // float [rows][cap]
   size_t total;
@@ -84,6 +90,8 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.dcp_key = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * p.topk * 4);
   L.dcp_tok = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * p.topk * 4);
   L.dcp_cnt = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * 4);
+  L.fe_part = o; o = align256(o + size_t(4) * L.rows * kIdxDim * 4);
+  L.fe_cnt = o; o = align256(o + size_t(kFeMaxPasses) * 4);
   L.dcp_keys16 = o; o = align256(o + size_t(L.rows) * (size_t(L.cap) + 8 * kDcpMaxWorld) * 2);
   L.scores = o; o = align256(o + size_t(L.rows) * L.cap * 4);
   L.total = o;

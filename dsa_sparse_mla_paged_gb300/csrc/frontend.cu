@@ -9,15 +9,18 @@
 // and k goes, FP8 (E4M3 + fp32 scale) or MXFP4 (E2M1 + E8M0 per 32), into the
 // cache slot of token ctx_b - n_q + t.
 //
-// Grid: clusters of 8 CTAs. Cluster j < 32 computes head j, cluster 32 the key,
-// and the first CTA of cluster 33 writes the scorer's tile plan. A CTA owns 16
-// of its cluster's 128 outputs: it prefetches those 16 weight rows into L2 at
-// launch, then streams them (once per group of 8 query rows) against the
-// group's inputs, staged in shared memory 2,048 columns at a time (32 KB, so
-// two CTAs fit an SM and the 272 CTAs run in one wave),
-// and sends each output, rounded to bf16, to the cluster's first CTA through
-// distributed shared memory; that CTA quantises the 128 values of every row
-// and writes them. A decode step is bound by the weight bytes.
+// Grid: clusters of 8 CTAs. Cluster j < 32 computes head j, clusters 32..35
+// a quarter of the key's hidden width each, and the first CTA of cluster 36
+// writes the scorer's tile plan. A CTA owns 16 of its cluster's 128 outputs:
+// it prefetches those 16 weight rows into L2 at launch, then streams them
+// (once per group of R = 4 or 8 query rows) against the group's inputs,
+// staged as fp32 in shared memory 2,048 columns at a time (two CTAs fit an
+// SM and the 296 CTAs run in one wave). A head's CTAs send each output,
+// rounded to bf16, to the cluster's first CTA through distributed shared
+// memory, and that CTA quantises the 128 values of every row. The key's
+// clusters leave fp32 partial sums in the workspace; the last of their CTAs
+// to finish a pass adds the quarters in order, rounds, quantises and writes
+// the keys. A decode step is bound by the weight bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -32,9 +35,11 @@ namespace {
 
 constexpr int kFeCluster = 8;
 constexpr int kFeThreads = 256;  // 8 warps x 2 outputs
-constexpr int kFeRows = 8;       // query rows per pass
+constexpr int kFeKeyParts = 4;   // the key's hidden width is split over 4 clusters
+constexpr int kFeJobs = kIdxHeads + kFeKeyParts + 1;  // head clusters, key clusters, the plan
 constexpr int kFeOut = kIdxDim / kFeCluster;
 constexpr int kFeBlk = 8;        // 16-byte chunks per lane per staged block: 2,048 inputs per row
+static_assert(kFeMaxRows % 8 == 0, "whole passes");
 static_assert(kFeOut == 2 * (kFeThreads / 32), "two outputs per warp");
 
 struct FeArgs {
@@ -53,6 +58,8 @@ struct FeArgs {
   float* w_out;
   int* tile_prefix;
   int* err;
+  float* fe_part;  // [kFeKeyParts][rows][128] the key's partial sums
+  int* fe_cnt;     // [kFeMaxPasses] arrivals per pass (0 between calls)
   int64_t key_page_stride;
   int rows, batch, n_q, d_c, d_model, max_pages, num_pages, cap, mx;
   float eps;
@@ -148,34 +155,40 @@ __device__ __forceinline__ void key_out(const FeArgs& a, int row, int lane, cons
   }
 }
 
-__global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads, 1)
+template <int R>
+__global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads, 2)
     idx_frontend_kernel(FeArgs a) {
   pdl_trigger();
-  extern __shared__ __align__(16) uint8_t fe_smem[];
-  __shared__ __align__(16) float gath[kFeRows][kIdxDim];  // the first CTA: every output of the pass
+  extern __shared__ __align__(16) float fe_in[];           // [R][kFeBlk * 256] staged inputs (fp32)
+  __shared__ __align__(16) float gath[R][kIdxDim];         // the first CTA: a head's outputs of the pass
+  __shared__ float s_rstd[R];
+  __shared__ int s_last;
   const int job = blockIdx.y;
-  if (job == kIdxHeads + 1) {  // the tile plan (no cluster traffic in this cluster)
+  if (job == kFeJobs - 1) {  // the tile plan (no cluster traffic in this cluster)
     if (blockIdx.x == 0) build_tile_plan<kFeThreads>(a.ctx_lens, a.batch, a.n_q, a.cap, a.tile_prefix, a.err);
     return;
   }
   const uint32_t rank = ptx::cluster_ctarank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool is_key = job == kIdxHeads;
+  const bool is_key = job >= kIdxHeads;
+  const int part = job - kIdxHeads;  // key: which quarter of the hidden width
   const int d = is_key ? a.d_model : a.d_c;
-  const int nch = d / 256;  // 16-byte chunks per lane per row
-  __nv_bfloat16* in = reinterpret_cast<__nv_bfloat16*>(fe_smem);  // [kFeRows][kFeBlk * 256]
-  const int o0 = int(rank) * kFeOut + 2 * warp;                   // this warp's outputs o0, o0 + 1
+  const int nch = d / 256;           // 16-byte chunks per lane per row
+  const int cj0 = is_key ? part * nch / kFeKeyParts : 0;
+  const int cj1 = is_key ? (part + 1) * nch / kFeKeyParts : nch;
+  const int o0 = int(rank) * kFeOut + 2 * warp;  // this warp's outputs o0, o0 + 1
   const __nv_bfloat16* w0 = is_key ? a.w_k + size_t(o0) * d : a.w_q + (size_t(job) * kIdxDim + o0) * d;
   const __nv_bfloat16* w1 = w0 + d;
   // The weights are constants of the model, not outputs of the previous
-  // kernel: start pulling this CTA's 16 rows into L2 before waiting on it.
-  const __nv_bfloat16* wcta = w0 - size_t(2 * warp) * d;  // the CTA's first weight row
-  if (threadIdx.x < kFeOut) ptx::prefetch_l2_bulk(wcta + size_t(threadIdx.x) * d, uint32_t(d) * 2);
+  // kernel: start pulling this CTA's 16 row segments into L2 before waiting.
+  if (threadIdx.x < kFeOut) {
+    const __nv_bfloat16* row = w0 + (int(threadIdx.x) - 2 * warp) * size_t(d) + size_t(cj0) * 256;
+    ptx::prefetch_l2_bulk(row, uint32_t(cj1 - cj0) * 512u);
+  }
   pdl_wait();
   ptx::cluster_sync();  // every CTA of the cluster runs before any remote store
-  __shared__ float s_rstd[kFeRows];
-  for (int r0 = 0; r0 < a.rows; r0 += kFeRows) {
-    const int nr = min(kFeRows, a.rows - r0);
+  for (int r0 = 0, pass = 0; r0 < a.rows; r0 += R, ++pass) {
+    const int nr = min(R, a.rows - r0);
     // ---- the query rows' 1 / RMS (warp w: row r0 + w)
     if (!is_key && warp < nr) {
       const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(r0 + warp) * d);
@@ -190,34 +203,37 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0) s_rstd[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(d)), a.eps)));
     }
-    float acc0[kFeRows], acc1[kFeRows];
+    float acc0[R], acc1[R];
 #pragma unroll
-    for (int rr = 0; rr < kFeRows; ++rr) acc0[rr] = acc1[rr] = 0.f;
-    for (int jb = 0; jb < nch; jb += kFeBlk) {
-      const int nj = min(kFeBlk, nch - jb);
+    for (int rr = 0; rr < R; ++rr) acc0[rr] = acc1[rr] = 0.f;
+    for (int jb = cj0; jb < cj1; jb += kFeBlk) {
+      const int nj = min(kFeBlk, cj1 - jb);
       __syncthreads();  // the previous block's inputs are consumed (and s_rstd is written)
-      // ---- stage the block's inputs: warp w prepares row r0 + w, chunks jb .. jb + nj - 1
+      // ---- stage the block's inputs as fp32: warp w prepares row r0 + w
       if (warp < nr) {
         const int row = r0 + warp;
-        uint4* dst = reinterpret_cast<uint4*>(in) + size_t(warp) * kFeBlk * 32;
+        float4* dst = reinterpret_cast<float4*>(fe_in) + size_t(warp) * kFeBlk * 64;
         if (is_key) {
           const uint4* src = reinterpret_cast<const uint4*>(a.x + size_t(row) * d) + jb * 32;
-          for (int j = 0; j < nj; ++j) dst[j * 32 + lane] = __ldg(src + j * 32 + lane);
+          for (int j = 0; j < nj; ++j) {
+            float f[8];
+            bf16x8(__ldg(src + j * 32 + lane), f);
+            dst[(j * 32 + lane) * 2] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[(j * 32 + lane) * 2 + 1] = make_float4(f[4], f[5], f[6], f[7]);
+          }
         } else {
           const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(row) * d) + jb * 32;
           const uint4* g = reinterpret_cast<const uint4*>(a.gamma) + jb * 32;
           const float rstd = s_rstd[warp];
           for (int j = 0; j < nj; ++j) {
-            float f[8], gg[8];
+            float f[8], gg[8], n[8];
             bf16x8(__ldg(src + j * 32 + lane), f);
             bf16x8(__ldg(g + j * 32 + lane), gg);
-            uint4 o;
-            __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              oh[i] = __halves2bfloat162(__float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i], rstd), gg[2 * i])),
-                                         __float2bfloat16_rn(__fmul_rn(__fmul_rn(f[2 * i + 1], rstd), gg[2 * i + 1])));
-            dst[j * 32 + lane] = o;
+            for (int i = 0; i < 8; ++i)
+              n[i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(f[i], rstd), gg[i])));
+            dst[(j * 32 + lane) * 2] = make_float4(n[0], n[1], n[2], n[3]);
+            dst[(j * 32 + lane) * 2 + 1] = make_float4(n[4], n[5], n[6], n[7]);
           }
         }
       }
@@ -231,9 +247,10 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
         bf16x8(__ldg(pw0 + j * 32 + lane), f0);
         bf16x8(__ldg(pw1 + j * 32 + lane), f1);
 #pragma unroll
-        for (int rr = 0; rr < kFeRows; ++rr) {
-          float xv[8];
-          bf16x8(reinterpret_cast<const uint4*>(in)[(size_t(rr) * kFeBlk + j) * 32 + lane], xv);
+        for (int rr = 0; rr < R; ++rr) {
+          const float4* xr = reinterpret_cast<const float4*>(fe_in) + (size_t(rr) * kFeBlk * 32 + j * 32 + lane) * 2;
+          const float4 xa = xr[0], xb = xr[1];
+          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             acc0[rr] = fmaf(f0[i], xv[i], acc0[rr]);
@@ -242,10 +259,10 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
         }
       }
     }
-    // lane 8i + rr keeps output o0 + i of row rr
+    // lane 8i + rr (rr < R) keeps output o0 + i of row rr
     float mine = 0.f;
 #pragma unroll
-    for (int rr = 0; rr < kFeRows; ++rr) {
+    for (int rr = 0; rr < R; ++rr) {
       float s0 = acc0[rr], s1 = acc1[rr];
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
@@ -255,19 +272,50 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
       if (lane == rr) mine = s0;
       if (lane == 8 + rr) mine = s1;
     }
-    if (lane < 16 && (lane & 7) < nr) {
-      const float vb = __bfloat162float(__float2bfloat16_rn(mine));
-      const uint32_t local = ptx::smem_u32(&gath[lane & 7][o0 + (lane >> 3)]);
-      ptx::st_cluster_u32(ptx::mapa_shared(local, 0), __float_as_uint(vb));
+    const bool holds = lane < 16 && (lane & 7) < nr;
+    const int hr = lane & 7, ho = o0 + (lane >> 3);
+    if (!is_key) {
+      if (holds) {
+        const float vb = __bfloat162float(__float2bfloat16_rn(mine));
+        ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_u32(&gath[hr][ho]), 0), __float_as_uint(vb));
+      }
+      ptx::cluster_sync();  // the first CTA holds the pass's outputs
+      if (rank == 0 && warp < nr) {
+        const float4 g4 = *reinterpret_cast<const float4*>(&gath[warp][lane * 4]);
+        const float v[4] = {g4.x, g4.y, g4.z, g4.w};
+        head_out(a, r0 + warp, job, lane, v);
+      }
+      ptx::cluster_sync();  // read before the next pass writes gath again
+    } else {
+      // the key: each quarter's partial sums go to the workspace; the last of
+      // the quarters' 32 CTAs to finish the pass adds them (in quarter order),
+      // rounds to bf16, quantises and writes the keys
+      if (holds) a.fe_part[(size_t(part) * a.rows + r0 + hr) * kIdxDim + ho] = mine;
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int ticket = atomicAdd(a.fe_cnt + pass, 1);
+        s_last = ticket == kFeKeyParts * kFeCluster - 1;
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        if (warp < nr) {
+          float v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float t = 0.f;
+#pragma unroll
+            for (int q = 0; q < kFeKeyParts; ++q)
+              t = __fadd_rn(t, __ldcg(a.fe_part + (size_t(q) * a.rows + r0 + warp) * kIdxDim + lane * 4 + i));
+            v[i] = __bfloat162float(__float2bfloat16_rn(t));
+          }
+          key_out(a, r0 + warp, lane, v);
+        }
+        if (threadIdx.x == 0) a.fe_cnt[pass] = 0;  // ready for the next call
+      }
+      __syncthreads();  // the staged inputs are read before the next pass
     }
-    ptx::cluster_sync();  // the first CTA holds the pass's outputs
-    if (rank == 0 && warp < nr) {
-      const float4 g4 = *reinterpret_cast<const float4*>(&gath[warp][lane * 4]);
-      const float v[4] = {g4.x, g4.y, g4.z, g4.w};
-      if (is_key) key_out(a, r0 + warp, lane, v);
-      else head_out(a, r0 + warp, job, lane, v);
-    }
-    ptx::cluster_sync();  // read before the next pass writes gath again (and the staged rows)
   }
 }
 
@@ -302,10 +350,14 @@ cudaError_t launch_idx_frontend(const dsa_params_t& p, const WsLayout& L, char* 
   a.cap = L.cap;
   a.mx = p.key_fmt == DSA_KEY_MXFP4_68;
   a.eps = in.eps;
-  const size_t smem = size_t(kFeRows) * kFeBlk * 256 * 2;
-  cudaError_t e = cudaFuncSetAttribute(idx_frontend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e == cudaSuccess)
-    e = launch_pdl(idx_frontend_kernel, dim3(kFeCluster, kIdxHeads + 2), dim3(kFeThreads), smem, st, a);
+  a.fe_part = reinterpret_cast<float*>(ws + L.fe_part);
+  a.fe_cnt = reinterpret_cast<int*>(ws + L.fe_cnt);
+  // four query rows per pass when the batch has at most four, else eight
+  const bool small = L.rows <= 4;
+  const size_t smem = size_t(small ? 4 : 8) * kFeBlk * 256 * 4;
+  auto kern = small ? idx_frontend_kernel<4> : idx_frontend_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e == cudaSuccess) e = launch_pdl(kern, dim3(kFeCluster, kFeJobs), dim3(kFeThreads), smem, st, a);
   return e;
 }
 

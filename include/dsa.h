@@ -210,6 +210,7 @@ typedef struct {
  *   x       bf16 [B * n_q, d_model]      w_k bf16 [128, d_model]
  *   key_pool written at one slot per row (16-B aligned, like every bf16 input)
  *   q8_out  E4M3 [B * n_q, 32, 128] or NULL; w_out fp32 [B * n_q, 32] or NULL (copies)
+ * Limits: B * n_q <= 512 (else DSA_ERR_UNSUPPORTED).
  * Errors: a row with an invalid ctx_b or block-table entry writes no key and
  * sets DSA_DEVERR_CTX / DSA_DEVERR_BLOCK_TABLE in the workspace. */
 dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend_dims_t* dims, const void* c_q,

@@ -173,3 +173,12 @@ def test_prepared_flag_lets_the_query_be_null(lib):
     q = _params()
     st = lib.dsa_indexer_scores(ctypes.byref(q), None, None, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need, None)
     assert st == dsa.DSA_ERR_INVALID
+
+
+def test_frontend_row_limit(lib):
+    p = _params(batch=513)
+    need = dsa.workspace_size(p)
+    dims = dsa.FrontendDims(d_c=1536, d_model=7168, eps=1e-6)
+    st = lib.dsa_indexer_frontend(ctypes.byref(p), ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, FAKE, None, None, FAKE, need, None)
+    assert st == dsa.DSA_ERR_UNSUPPORTED
