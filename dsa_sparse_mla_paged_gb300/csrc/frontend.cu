@@ -189,26 +189,45 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
   ptx::cluster_sync();  // every CTA of the cluster runs before any remote store
   for (int r0 = 0, pass = 0; r0 < a.rows; r0 += R, ++pass) {
     const int nr = min(R, a.rows - r0);
-    // ---- the query rows' 1 / RMS (warp w: row r0 + w)
+    // ---- the query rows' 1 / RMS (warp w: row r0 + w); the first block's raw
+    // values stay in shared memory for the staging below
+    __syncthreads();  // the previous pass's inputs are consumed
     if (!is_key && warp < nr) {
       const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(r0 + warp) * d);
+      float4* raw = reinterpret_cast<float4*>(fe_in) + size_t(warp) * kFeBlk * 64;
       float ss = 0.f;
       for (int j = 0; j < nch; ++j) {
         float f[8];
         bf16x8(__ldg(src + j * 32 + lane), f);
+        if (j < kFeBlk) {
+          raw[(j * 32 + lane) * 2] = make_float4(f[0], f[1], f[2], f[3]);
+          raw[(j * 32 + lane) * 2 + 1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0) s_rstd[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(d)), a.eps)));
+      __syncwarp();  // the warp's staging reads it
     }
     float acc0[R], acc1[R];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) acc0[rr] = acc1[rr] = 0.f;
     for (int jb = cj0; jb < cj1; jb += kFeBlk) {
       const int nj = min(kFeBlk, cj1 - jb);
-      __syncthreads();  // the previous block's inputs are consumed (and s_rstd is written)
+      const uint4* pw0 = reinterpret_cast<const uint4*>(w0) + jb * 32;
+      const uint4* pw1 = reinterpret_cast<const uint4*>(w1) + jb * 32;
+      // the block's first four weight chunks, loaded before the staging so
+      // that their latency overlaps it
+      uint4 wa[4], wb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (u < nj) {
+          wa[u] = __ldg(pw0 + u * 32 + lane);
+          wb[u] = __ldg(pw1 + u * 32 + lane);
+        }
+      if (jb != cj0) __syncthreads();  // the previous block's inputs are consumed
       // ---- stage the block's inputs as fp32: warp w prepares row r0 + w
       if (warp < nr) {
         const int row = r0 + warp;
@@ -224,10 +243,16 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
         } else {
           const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(row) * d) + jb * 32;
           const uint4* g = reinterpret_cast<const uint4*>(a.gamma) + jb * 32;
-          const float rstd = s_rstd[warp];
+          const float rstd = s_rstd[warp];  // written by this warp's lane 0
           for (int j = 0; j < nj; ++j) {
             float f[8], gg[8], n[8];
-            bf16x8(__ldg(src + j * 32 + lane), f);
+            if (jb == 0) {  // the raw values are already here (this lane wrote them)
+              const float4 ra = dst[(j * 32 + lane) * 2], rb = dst[(j * 32 + lane) * 2 + 1];
+              f[0] = ra.x; f[1] = ra.y; f[2] = ra.z; f[3] = ra.w;
+              f[4] = rb.x; f[5] = rb.y; f[6] = rb.z; f[7] = rb.w;
+            } else {
+              bf16x8(__ldg(src + j * 32 + lane), f);
+            }
             bf16x8(__ldg(g + j * 32 + lane), gg);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -238,23 +263,33 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
         }
       }
       __syncthreads();
-      // ---- the warp's two weight rows against the block's rows
-      const uint4* pw0 = reinterpret_cast<const uint4*>(w0) + jb * 32;
-      const uint4* pw1 = reinterpret_cast<const uint4*>(w1) + jb * 32;
-#pragma unroll 4
-      for (int j = 0; j < nj; ++j) {
-        float f0[8], f1[8];
-        bf16x8(__ldg(pw0 + j * 32 + lane), f0);
-        bf16x8(__ldg(pw1 + j * 32 + lane), f1);
+      // ---- the warp's two weight rows against the block's rows, four chunks at a time
+      for (int jg = 0; jg < nj; jg += 4) {
+        if (jg > 0) {
 #pragma unroll
-        for (int rr = 0; rr < R; ++rr) {
-          const float4* xr = reinterpret_cast<const float4*>(fe_in) + (size_t(rr) * kFeBlk * 32 + j * 32 + lane) * 2;
-          const float4 xa = xr[0], xb = xr[1];
-          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          for (int u = 0; u < 4; ++u)
+            if (jg + u < nj) {
+              wa[u] = __ldg(pw0 + (jg + u) * 32 + lane);
+              wb[u] = __ldg(pw1 + (jg + u) * 32 + lane);
+            }
+        }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            acc0[rr] = fmaf(f0[i], xv[i], acc0[rr]);
-            acc1[rr] = fmaf(f1[i], xv[i], acc1[rr]);
+        for (int u = 0; u < 4; ++u) {
+          if (jg + u >= nj) break;
+          float f0[8], f1[8];
+          bf16x8(wa[u], f0);
+          bf16x8(wb[u], f1);
+#pragma unroll
+          for (int rr = 0; rr < R; ++rr) {
+            const float4* xr =
+                reinterpret_cast<const float4*>(fe_in) + (size_t(rr) * kFeBlk * 32 + (jg + u) * 32 + lane) * 2;
+            const float4 xa = xr[0], xb = xr[1];
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc0[rr] = fmaf(f0[i], xv[i], acc0[rr]);
+              acc1[rr] = fmaf(f1[i], xv[i], acc1[rr]);
+            }
           }
         }
       }
