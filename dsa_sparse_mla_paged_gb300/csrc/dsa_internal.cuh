@@ -58,7 +58,8 @@ struct WsLayout {
   size_t dcp_tok;   // int32 [rows][kDcpMaxWorld][topk] shard lists: tokens by position
   size_t dcp_cnt;   // int32 [rows][kDcpMaxWorld] shard list lengths
   size_t fe_part;   // fp32 [4][rows][128] the front end's key partial sums
-  size_t fe_cnt;    // int32 [kFeMaxPasses] the front end's per-pass arrival counters
+  size_t fe_q;      // fp32 [rows][32][128] the front end's head outputs
+  size_t fe_cnt;    // int32 [33][kFeMaxPasses] the front end's arrival counters
   size_t dcp_keys16;  // uint16 [rows][W][S] shard-major score keys, W * S <= cap + 8 * kDcpMaxWorld
   size_t scores;    // float [rows][cap]
   size_t total;
@@ -91,7 +92,8 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.dcp_tok = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * p.topk * 4);
   L.dcp_cnt = o; o = align256(o + size_t(L.rows) * kDcpMaxWorld * 4);
   L.fe_part = o; o = align256(o + size_t(4) * L.rows * kIdxDim * 4);
-  L.fe_cnt = o; o = align256(o + size_t(kFeMaxPasses) * 4);
+  L.fe_q = o; o = align256(o + size_t(L.rows) * kIdxHeads * kIdxDim * 4);
+  L.fe_cnt = o; o = align256(o + size_t(kIdxHeads + 1) * kFeMaxPasses * 4);
   L.dcp_keys16 = o; o = align256(o + size_t(L.rows) * (size_t(L.cap) + 8 * kDcpMaxWorld) * 2);
   L.scores = o; o = align256(o + size_t(L.rows) * L.cap * 4);
   L.total = o;

@@ -9,18 +9,17 @@
 // and k goes, FP8 (E4M3 + fp32 scale) or MXFP4 (E2M1 + E8M0 per 32), into the
 // cache slot of token ctx_b - n_q + t.
 //
-// Grid: clusters of 8 CTAs. Cluster j < 32 computes head j, clusters 32..35
-// a quarter of the key's hidden width each, and the first CTA of cluster 36
-// writes the scorer's tile plan. A CTA owns 16 of its cluster's 128 outputs:
-// it prefetches those 16 weight rows into L2 at launch, then streams them
-// (once per group of R = 4 or 8 query rows) against the group's inputs,
-// staged as fp32 in shared memory 2,048 columns at a time (two CTAs fit an
-// SM and the 296 CTAs run in one wave). A head's CTAs send each output,
-// rounded to bf16, to the cluster's first CTA through distributed shared
-// memory, and that CTA quantises the 128 values of every row. The key's
-// clusters leave fp32 partial sums in the workspace; the last of their CTAs
-// to finish a pass adds the quarters in order, rounds, quantises and writes
-// the keys. A decode step is bound by the weight bytes.
+// Grid: 8 x 37 CTAs. Row j < 32 computes head j, rows 32..35 a quarter of
+// the key's hidden width each, and the first CTA of row 36 writes the
+// scorer's tile plan. A CTA owns 16 of the 128 outputs of its head (or key
+// quarter): it prefetches those 16 weight rows into L2 at launch, then streams
+// them (once per group of R = 4 or 8 query rows) against the group's inputs,
+// staged as fp32 in shared memory 2,048 columns at a time (two CTAs fit an SM,
+// so the 296 CTAs run in one wave). Each CTA leaves its outputs in the
+// workspace; the last CTA of a head (or of the key) to finish a pass, found by
+// an arrival counter, reads them back, rounds and quantises the rows and
+// writes them (the key's quarters are added in order). A decode step is bound
+// by the weight bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -33,11 +32,11 @@ namespace dsa {
 
 namespace {
 
-constexpr int kFeCluster = 8;
+constexpr int kFeSplit = 8;      // CTAs per 128 outputs (16 outputs each)
 constexpr int kFeThreads = 256;  // 8 warps x 2 outputs
-constexpr int kFeKeyParts = 4;   // the key's hidden width is split over 4 clusters
-constexpr int kFeJobs = kIdxHeads + kFeKeyParts + 1;  // head clusters, key clusters, the plan
-constexpr int kFeOut = kIdxDim / kFeCluster;
+constexpr int kFeKeyParts = 4;   // the key's hidden width is split in quarters
+constexpr int kFeJobs = kIdxHeads + kFeKeyParts + 1;  // heads, key quarters, the plan
+constexpr int kFeOut = kIdxDim / kFeSplit;
 constexpr int kFeBlk = 8;        // 16-byte chunks per lane per staged block: 2,048 inputs per row
 static_assert(kFeMaxRows % 8 == 0, "whole passes");
 static_assert(kFeOut == 2 * (kFeThreads / 32), "two outputs per warp");
@@ -59,7 +58,8 @@ struct FeArgs {
   int* tile_prefix;
   int* err;
   float* fe_part;  // [kFeKeyParts][rows][128] the key's partial sums
-  int* fe_cnt;     // [kFeMaxPasses] arrivals per pass (0 between calls)
+  float* fe_q;     // [rows][32][128] the heads' bf16-rounded outputs
+  int* fe_cnt;     // [33][kFeMaxPasses] arrivals per (head or key, pass); 0 between calls
   int64_t key_page_stride;
   int rows, batch, n_q, d_c, d_model, max_pages, num_pages, cap, mx;
   float eps;
@@ -156,19 +156,18 @@ __device__ __forceinline__ void key_out(const FeArgs& a, int row, int lane, cons
 }
 
 template <int R>
-__global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads, 2)
+__global__ void __launch_bounds__(kFeThreads, 2)
     idx_frontend_kernel(FeArgs a) {
   pdl_trigger();
   extern __shared__ __align__(16) float fe_in[];           // [R][kFeBlk * 256] staged inputs (fp32)
-  __shared__ __align__(16) float gath[R][kIdxDim];         // the first CTA: a head's outputs of the pass
   __shared__ float s_rstd[R];
   __shared__ int s_last;
   const int job = blockIdx.y;
-  if (job == kFeJobs - 1) {  // the tile plan (no cluster traffic in this cluster)
+  if (job == kFeJobs - 1) {  // the tile plan
     if (blockIdx.x == 0) build_tile_plan<kFeThreads>(a.ctx_lens, a.batch, a.n_q, a.cap, a.tile_prefix, a.err);
     return;
   }
-  const uint32_t rank = ptx::cluster_ctarank();
+  const int rank = blockIdx.x;  // which 16 outputs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_key = job >= kIdxHeads;
   const int part = job - kIdxHeads;  // key: which quarter of the hidden width
@@ -176,7 +175,7 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
   const int nch = d / 256;           // 16-byte chunks per lane per row
   const int cj0 = is_key ? part * nch / kFeKeyParts : 0;
   const int cj1 = is_key ? (part + 1) * nch / kFeKeyParts : nch;
-  const int o0 = int(rank) * kFeOut + 2 * warp;  // this warp's outputs o0, o0 + 1
+  const int o0 = rank * kFeOut + 2 * warp;  // this warp's outputs o0, o0 + 1
   const __nv_bfloat16* w0 = is_key ? a.w_k + size_t(o0) * d : a.w_q + (size_t(job) * kIdxDim + o0) * d;
   const __nv_bfloat16* w1 = w0 + d;
   // The weights are constants of the model, not outputs of the previous
@@ -186,7 +185,6 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
     ptx::prefetch_l2_bulk(row, uint32_t(cj1 - cj0) * 512u);
   }
   pdl_wait();
-  ptx::cluster_sync();  // every CTA of the cluster runs before any remote store
   for (int r0 = 0, pass = 0; r0 < a.rows; r0 += R, ++pass) {
     const int nr = min(R, a.rows - r0);
     // ---- the query rows' 1 / RMS (warp w: row r0 + w); the first block's raw
@@ -307,49 +305,42 @@ __global__ void __cluster_dims__(kFeCluster, 1, 1) __launch_bounds__(kFeThreads,
       if (lane == rr) mine = s0;
       if (lane == 8 + rr) mine = s1;
     }
-    const bool holds = lane < 16 && (lane & 7) < nr;
-    const int hr = lane & 7, ho = o0 + (lane >> 3);
-    if (!is_key) {
-      if (holds) {
-        const float vb = __bfloat162float(__float2bfloat16_rn(mine));
-        ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_u32(&gath[hr][ho]), 0), __float_as_uint(vb));
-      }
-      ptx::cluster_sync();  // the first CTA holds the pass's outputs
-      if (rank == 0 && warp < nr) {
-        const float4 g4 = *reinterpret_cast<const float4*>(&gath[warp][lane * 4]);
-        const float v[4] = {g4.x, g4.y, g4.z, g4.w};
-        head_out(a, r0 + warp, job, lane, v);
-      }
-      ptx::cluster_sync();  // read before the next pass writes gath again
-    } else {
-      // the key: each quarter's partial sums go to the workspace; the last of
-      // the quarters' 32 CTAs to finish the pass adds them (in quarter order),
-      // rounds to bf16, quantises and writes the keys
-      if (holds) a.fe_part[(size_t(part) * a.rows + r0 + hr) * kIdxDim + ho] = mine;
+    // Every CTA leaves its outputs in the workspace (a head's bf16-rounded
+    // values; the key's fp32 partial sums); the last CTA of the group to finish
+    // the pass (a ticket) reads them back, finishes and quantises the rows.
+    if (lane < 16 && (lane & 7) < nr) {
+      const int hr = lane & 7, ho = o0 + (lane >> 3);
+      if (is_key) a.fe_part[(size_t(part) * a.rows + r0 + hr) * kIdxDim + ho] = mine;
+      else a.fe_q[(size_t(r0 + hr) * kIdxHeads + job) * kIdxDim + ho] = __bfloat162float(__float2bfloat16_rn(mine));
+    }
+    __threadfence();
+    __syncthreads();
+    const int group = is_key ? kIdxHeads : job;
+    int* cnt = a.fe_cnt + size_t(group) * kFeMaxPasses + pass;
+    if (threadIdx.x == 0) s_last = atomicAdd(cnt, 1) == (is_key ? kFeKeyParts : 1) * kFeSplit - 1;
+    __syncthreads();
+    if (s_last) {
       __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const int ticket = atomicAdd(a.fe_cnt + pass, 1);
-        s_last = ticket == kFeKeyParts * kFeCluster - 1;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        if (warp < nr) {
-          float v[4];
+      if (warp < nr) {
+        const int row = r0 + warp;
+        float v[4];
+        if (is_key) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float t = 0.f;
 #pragma unroll
             for (int q = 0; q < kFeKeyParts; ++q)
-              t = __fadd_rn(t, __ldcg(a.fe_part + (size_t(q) * a.rows + r0 + warp) * kIdxDim + lane * 4 + i));
+              t = __fadd_rn(t, __ldcg(a.fe_part + (size_t(q) * a.rows + row) * kIdxDim + lane * 4 + i));
             v[i] = __bfloat162float(__float2bfloat16_rn(t));
           }
-          key_out(a, r0 + warp, lane, v);
+          key_out(a, row, lane, v);
+        } else {
+          const float4 g4 = __ldcg(reinterpret_cast<const float4*>(a.fe_q + (size_t(row) * kIdxHeads + job) * kIdxDim) + lane);
+          v[0] = g4.x; v[1] = g4.y; v[2] = g4.z; v[3] = g4.w;
+          head_out(a, row, job, lane, v);
         }
-        if (threadIdx.x == 0) a.fe_cnt[pass] = 0;  // ready for the next call
       }
-      __syncthreads();  // the staged inputs are read before the next pass
+      if (threadIdx.x == 0) *cnt = 0;  // ready for the next call
     }
   }
 }
@@ -387,12 +378,13 @@ cudaError_t launch_idx_frontend(const dsa_params_t& p, const WsLayout& L, char* 
   a.eps = in.eps;
   a.fe_part = reinterpret_cast<float*>(ws + L.fe_part);
   a.fe_cnt = reinterpret_cast<int*>(ws + L.fe_cnt);
+  a.fe_q = reinterpret_cast<float*>(ws + L.fe_q);
   // four query rows per pass when the batch has at most four, else eight
   const bool small = L.rows <= 4;
   const size_t smem = size_t(small ? 4 : 8) * kFeBlk * 256 * 4;
   auto kern = small ? idx_frontend_kernel<4> : idx_frontend_kernel<8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e == cudaSuccess) e = launch_pdl(kern, dim3(kFeCluster, kFeJobs), dim3(kFeThreads), smem, st, a);
+  if (e == cudaSuccess) e = launch_pdl(kern, dim3(kFeSplit, kFeJobs), dim3(kFeThreads), smem, st, a);
   return e;
 }
 
