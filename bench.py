@@ -217,8 +217,9 @@ def run_reference(args, rank):
 
 def run_stage(args):
     """Time one entry point alone (for kernel profiles):
-    `--stage indexer|topk|mla|dcp_merge|dcp_combine|frontend` (the front end with
-    d_c = 1536, d_model = 7168 and its weights rotated through 12 copies, 173 MB > L2)."""
+    `--stage indexer|topk|mla|dcp_merge|dcp_combine|frontend|prefill` (the front end with
+    d_c = 1536, d_model = 7168 and its weights rotated through 12 copies, 173 MB > L2;
+    prefill: rank --rank of --world token slices, e.g. on --workload b1_prefill2k_ctx150k)."""
     import torch
 
     import dsa_sparse_mla_paged_gb300 as dsa
@@ -267,10 +268,31 @@ def run_stage(args):
         "dcp_merge": lambda: dsa.dcp_topk_merge(d.p, sc, d.cap, d.ctx, W, idx, stats, d.ws),
         "dcp_combine": lambda: dsa.lse_combine(d.p, W, parts_o, parts_l, out, lse),
         "frontend": lambda: fe_call(),
+        "prefill": lambda: dsa.indexer_prefill_scores(d.p, W, max(args.rank, 0), d.q_idx, d.w, d.key_pool,
+                                                      d.block_table, d.ctx, sc, d.cap, d.ws),
         "topk": lambda: dsa.topk(d.p, sc, d.cap, d.ctx, d.block_table, idx, None, d.ws),
         "mla": lambda: dsa.sparse_mla_decode(d.p, d.q, d.lat_pool, d.block_table, d.ctx, idx, out, lse, d.ws),
     }
     f = calls[args.stage]
+    if args.stage == "prefill" and args.rank < 0:
+        # every rank of the token split in turn: the balance of the r / 2W-1-r pairing
+        per_rank = []
+        for r in range(W):
+            args.rank = r
+            for _ in range(args.warmup):
+                f()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(args.steps):
+                f()
+            e1.record()
+            torch.cuda.synchronize()
+            per_rank.append(e0.elapsed_time(e1) / args.steps)
+        args.rank = -1
+        print(json.dumps({"stage": "prefill", "workload": args.workload, "world": W,
+                          "ms_per_rank": per_rank, "max_over_min": max(per_rank) / min(per_rank)}), flush=True)
+        return
     for _ in range(args.warmup):
         f()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -289,10 +311,20 @@ def run_stage(args):
               # weights once, the rows' inputs, q8 + w' out, one key per row
               "frontend": (4096 * D_C + 128 * D_MODEL + D_C) * 2 + d.rows * ((D_C + D_MODEL) * 2 + 32 * 4)
                           + d.rows * (4096 + 32 * 4 + 132),
+              "prefill": 0,
               }[args.stage]
     assert dsa.get_device_error(d.ws) == 0
     line = {"stage": args.stage, "workload": args.workload, "ms": ms, "bytes": nbytes,
             "gbs": nbytes / (ms * 1e-3) / 1e9}
+    if args.stage == "prefill":
+        # useful work of the scored rows: every visible key of every row, 32 heads x 128 dims
+        rows = list(range(inp.n_q)) if W == 1 else [int(t) for t in _rank_rows(inp.n_q, W, max(args.rank, 0))]
+        keys = sum(max(0, int(c) - inp.n_q + t + 1) for c in inp.ctx for t in rows)
+        flops = 2.0 * 32 * 128 * keys
+        byts = 132 * sum(int(c) for c in inp.ctx) + 4 * keys + len(rows) * inp.batch * (32 * 128 * 2 + 32 * 4)
+        line.update({"world": W, "rank": max(args.rank, 0), "rows_scored": len(rows) * inp.batch,
+                     "keys_scored": keys, "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9,
+                     "tflops": flops / (ms * 1e-3) / 1e12})
     if args.stage == "dcp_merge":
         from oracle import dcp as D
 
@@ -308,6 +340,12 @@ def run_stage(args):
         line["oracle_ms_per_row"] = (time.perf_counter() - t0) * 1e3
         line["row0_equals_oracle"] = bool(np.array_equal(idx[0].cpu().numpy(), res["idx"]))
     print(json.dumps(line), flush=True)
+
+
+def _rank_rows(n_q, world, rank):
+    """Rows of one request that rank `rank` of `world` scores (slices r and 2W - 1 - r of 2W)."""
+    ss = n_q // (2 * world)
+    return list(range(rank * ss, (rank + 1) * ss)) + list(range((2 * world - 1 - rank) * ss, (2 * world - rank) * ss))
 
 
 def run_ours(args, rank, world):
@@ -502,9 +540,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage", default="all",
-                    choices=["all", "indexer", "topk", "mla", "dcp_merge", "dcp_combine", "frontend"],
+                    choices=["all", "indexer", "topk", "mla", "dcp_merge", "dcp_combine", "frontend", "prefill"],
                     help="time one entry point alone (kernel profiling; the dcp_* stages emulate --world shards)")
-    ap.add_argument("--world", type=int, default=8, help="shards of the dcp_* stages")
+    ap.add_argument("--world", type=int, default=8, help="shards of the dcp_* stages, ranks of the prefill stage")
+    ap.add_argument("--rank", type=int, default=0, help="prefill stage: this rank's slices (-1: every rank in turn)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     rank = int(os.environ.get("RANK", "0"))

@@ -5,7 +5,7 @@ module only turns tensors into device pointers and status codes into
 exceptions. There is no fallback: if libdsa.so is missing, ``load()`` raises.
 
 Entry points mirror include/dsa.h: ``workspace_size``, ``indexer_scores``,
-``indexer_frontend``, ``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``lse_combine``, ``sparse_mla_decode``,
+``indexer_frontend``, ``indexer_prefill_scores``, ``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``lse_combine``, ``sparse_mla_decode``,
 ``decode``, ``get_device_error``, ``status_string``.
 """
 from __future__ import annotations
@@ -30,6 +30,7 @@ EXPORTS = (
     "dsa_workspace_size",
     "dsa_indexer_scores",
     "dsa_indexer_frontend",
+    "dsa_indexer_prefill_scores",
     "dsa_topk",
     "dsa_topk_noalloc",
     "dsa_dcp_topk_merge",
@@ -110,6 +111,7 @@ def load() -> ctypes.CDLL:
         "dsa_topk_noalloc": [P, vp, i64, vp, vp, vp, vp, vp],
         "dsa_indexer_frontend": [P, ctypes.POINTER(FrontendDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                  sz, vp],
+        "dsa_indexer_prefill_scores": [P, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp, vp, vp, i64, vp, sz, vp],
         "dsa_dcp_topk_merge": [P, vp, i64, vp, ctypes.c_int32, vp, vp, vp, sz, vp],
         "dsa_lse_combine": [P, ctypes.c_int32, vp, vp, vp, vp, vp],
         "dsa_sparse_mla_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
@@ -177,6 +179,14 @@ def indexer_frontend(params, dims, c_q, gamma_q, w_q, w, x, w_k, key_pool, block
         ctypes.byref(params), ctypes.byref(dims), _ptr(c_q), _ptr(gamma_q), _ptr(w_q), _ptr(w), _ptr(x),
         _ptr(w_k), _ptr(key_pool), _ptr(block_table), _ptr(ctx_lens), _ptr(q8_out), _ptr(w_out), _ptr(ws),
         _nbytes(ws), _stream(stream)))
+
+
+def indexer_prefill_scores(params, world, rank, q_idx, w, key_pool, block_table, ctx_lens, scores, score_stride, ws,
+                           stream=None):
+    """Scores of rank's two token slices of every request (2 * world slices)."""
+    _check("dsa_indexer_prefill_scores", load().dsa_indexer_prefill_scores(
+        ctypes.byref(params), int(world), int(rank), _ptr(q_idx), _ptr(w), _ptr(key_pool), _ptr(block_table),
+        _ptr(ctx_lens), _ptr(scores), int(score_stride), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def topk(params, scores, score_stride, ctx_lens, block_table, topk_idx, phys_rows, ws, stream=None):

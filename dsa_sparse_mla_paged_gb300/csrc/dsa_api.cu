@@ -15,7 +15,7 @@ dsa_status_t check_params(const dsa_params_t* p) {
   if (!p) return DSA_ERR_INVALID;
   if (p->batch < 1 || p->n_q < 1 || p->max_pages_per_req < 1 || p->num_pages < 1) return DSA_ERR_INVALID;
   if (p->topk < 1) return DSA_ERR_INVALID;
-  if (p->n_q > kMaxNQ || p->topk > kMaxTopK) return DSA_ERR_UNSUPPORTED;
+  if (p->topk > kMaxTopK) return DSA_ERR_UNSUPPORTED;
   if (p->page_size != kPage || p->idx_heads != kIdxHeads || p->idx_dim != kIdxDim ||
       p->heads != kHeads || p->d_nope != kDNope || p->d_rope != kDRope)
     return DSA_ERR_UNSUPPORTED;
@@ -91,6 +91,26 @@ dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, c
   return cuda_status(e);
 }
 
+dsa_status_t dsa_indexer_prefill_scores(const dsa_params_t* params, int32_t world, int32_t rank, const void* q_idx,
+                                        const float* w, const void* key_pool, const int32_t* block_table,
+                                        const int32_t* ctx_lens, float* scores, int64_t score_stride, void* ws,
+                                        size_t ws_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_params(params);
+  if (s != DSA_OK) return s;
+  if (world < 1 || rank < 0 || rank >= world) return DSA_ERR_INVALID;
+  if (world > 1 && params->n_q % (2 * world * kMaxNQ)) return DSA_ERR_INVALID;
+  if (params->flags & DSA_Q_PREPARED) return DSA_ERR_INVALID;
+  if ((s = check_indexer_args(params, q_idx, w, key_pool, block_table, ctx_lens)) != DSA_OK) return s;
+  if (!scores || !aligned16(scores) || score_stride < 1 || (score_stride & 3)) return DSA_ERR_INVALID;
+  WsLayout L;
+  if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
+  char* w8 = static_cast<char*>(ws);
+  cudaError_t e = launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream, world, rank);
+  if (e == cudaSuccess)
+    e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, score_stride, stream, world, rank);
+  return cuda_status(e);
+}
+
 dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t score_stride,
                       const int32_t* ctx_lens, const int32_t* block_table, int32_t* topk_idx,
                       int32_t* phys_rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -116,7 +136,7 @@ dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend
   for (int d : {dims->d_c, dims->d_model})
     if (d < 256 || d > 8192 || (d % 256)) return DSA_ERR_UNSUPPORTED;
   if (!(dims->eps >= 0.f) || !(dims->eps < 1e30f)) return DSA_ERR_INVALID;
-  if (int64_t(params->batch) * params->n_q > kFeMaxRows) return DSA_ERR_UNSUPPORTED;
+  if (int64_t(params->batch) * params->n_q > kFeMaxRows || params->n_q > kMaxNQ) return DSA_ERR_UNSUPPORTED;
   for (const void* ptr : {c_q, gamma_q, w_q, x, w_k, static_cast<const void*>(key_pool)})
     if (!ptr || !aligned16(ptr)) return DSA_ERR_INVALID;
   if (!w || (reinterpret_cast<uintptr_t>(w) & 3) || !block_table || !ctx_lens) return DSA_ERR_INVALID;

@@ -47,7 +47,7 @@ struct WsLayout {
   size_t err;       // int32 error word
   size_t q8;        // uint8 [rows][32][128] quantised indexer query
   size_t wq;        // float [rows][32] folded head weights
-  size_t tiles;     // int32 [batch] inclusive prefix of 128-token tiles per request
+  size_t tiles;     // int32 [rows] inclusive prefix of 128-token tiles per scorer unit
   size_t state;     // int32 [rows][kRowState]
   size_t chunkinfo; // int32 [rows][max_chunks][2] (offset, count) of each chunk's candidates
   size_t cand;      // uint64 [rows][kCandCap] top-k candidates (key << 32 | token)
@@ -81,7 +81,7 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.err = o; o = align256(o + 256);
   L.q8 = o; o = align256(o + size_t(L.rows) * kIdxHeads * kIdxDim);
   L.wq = o; o = align256(o + size_t(L.rows) * kIdxHeads * 4);
-  L.tiles = o; o = align256(o + size_t(p.batch) * 4);
+  L.tiles = o; o = align256(o + size_t(L.rows) * 4);
   L.state = o; o = align256(o + size_t(L.rows) * kRowState * 4);
   L.chunkinfo = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
   L.cand = o; o = align256(o + size_t(L.rows) * kCandCap * 8);
@@ -158,23 +158,63 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int
 // ---------------------------------------------------------------- launchers
 // (each returns cudaGetLastError() of its launches)
 
+// The scorer's work units: the query rows of a request in groups of at most
+// kMaxNQ (decode: one group per request; prefill: many). With token sharding
+// ("预填充：按 token 而非按头分片注意力": each request cut into 2W slices, rank r
+// taking slices r and 2W - 1 - r), a call covers only its rank's groups.
+struct UnitMap {
+  int rows_per_req;      // n_q
+  int gsz;               // query rows per group: min(n_q, kMaxNQ)
+  int groups;            // groups per request in this call
+  int slice_groups;      // groups of the first slice (all of them without sharding)
+  int slice_a, slice_b;  // first group of each slice
+};
+
+__host__ __device__ inline UnitMap unit_map(int n_q, int world, int rank) {
+  UnitMap m;
+  m.rows_per_req = n_q;
+  m.gsz = n_q < kMaxNQ ? n_q : kMaxNQ;
+  if (world <= 1) {
+    m.groups = m.slice_groups = (n_q + m.gsz - 1) / m.gsz;
+    m.slice_a = m.slice_b = 0;
+  } else {  // n_q is a multiple of 2W x kMaxNQ
+    m.slice_groups = n_q / (2 * world) / m.gsz;
+    m.groups = 2 * m.slice_groups;
+    m.slice_a = rank * m.slice_groups;
+    m.slice_b = (2 * world - 1 - rank) * m.slice_groups;
+  }
+  return m;
+}
+
+__host__ __device__ __forceinline__ int unit_first_row(const UnitMap& m, int gl) {
+  const int g = gl < m.slice_groups ? m.slice_a + gl : m.slice_b + (gl - m.slice_groups);
+  return g * m.gsz;
+}
+
 // Work plan of the scorer, by one CTA of NT threads: tiles of 128 tokens (two
-// pages) per request, inclusive prefix over the batch. An invalid context
-// length gets no tiles and sets DSA_DEVERR_CTX.
+// pages) per unit, inclusive prefix over the units. A unit's context is its
+// last row's: ctx_b - n_q + first + valid. An invalid context length gets no
+// tiles and sets DSA_DEVERR_CTX.
 template <int NT>
-__device__ __forceinline__ void build_tile_plan(const int32_t* __restrict__ ctx_lens, int batch, int n_q, int cap,
+__device__ __forceinline__ void build_tile_plan(const int32_t* __restrict__ ctx_lens, int units, UnitMap m, int cap,
                                                 int* __restrict__ tile_prefix, int* err) {
   constexpr int NW = NT / 32;
   __shared__ int wsum[NW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int carry = 0;
-  for (int b0 = 0; b0 < batch; b0 += NT) {
-    const int b = b0 + int(threadIdx.x);
+  for (int u0 = 0; u0 < units; u0 += NT) {
+    const int u = u0 + int(threadIdx.x);
     int n = 0;
-    if (b < batch) {
+    if (u < units) {
+      const int b = u / m.groups;
       const int c = ctx_lens[b];
-      if (c < n_q || c > cap) atomicOr(err, DSA_DEVERR_CTX);
-      else n = (c + 127) >> 7;
+      if (c < m.rows_per_req || c > cap) {
+        atomicOr(err, DSA_DEVERR_CTX);
+      } else {
+        const int first = unit_first_row(m, u - b * m.groups);
+        const int valid = min(m.gsz, m.rows_per_req - first);
+        n = (c - m.rows_per_req + first + valid + 127) >> 7;
+      }
     }
     int x = n;
 #pragma unroll
@@ -186,17 +226,18 @@ __device__ __forceinline__ void build_tile_plan(const int32_t* __restrict__ ctx_
     __syncthreads();
     int pre = carry;
     for (int i = 0; i < warp; ++i) pre += wsum[i];
-    if (b < batch) tile_prefix[b] = pre + x;
+    if (u < units) tile_prefix[u] = pre + x;
     for (int i = 0; i < NW; ++i) carry += wsum[i];
     __syncthreads();
   }
 }
 
 cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
-                               const float* w, const int32_t* ctx_lens, cudaStream_t st);
+                               const float* w, const int32_t* ctx_lens, cudaStream_t st, int world = 1,
+                               int rank = 0);
 cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
                            const int32_t* block_table, const int32_t* ctx_lens, float* scores,
-                           int64_t score_stride, cudaStream_t st);
+                           int64_t score_stride, cudaStream_t st, int world = 1, int rank = 0);
 cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                         int64_t score_stride, const int32_t* ctx_lens, const int32_t* block_table,
                         int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st);

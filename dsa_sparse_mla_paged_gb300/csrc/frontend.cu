@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(kFeThreads, 2)
   __shared__ int s_last;
   const int job = blockIdx.y;
   if (job == kFeJobs - 1) {  // the tile plan
-    if (blockIdx.x == 0) build_tile_plan<kFeThreads>(a.ctx_lens, a.batch, a.n_q, a.cap, a.tile_prefix, a.err);
+    if (blockIdx.x == 0)  // decode rows (n_q <= 8): one unit per request
+      build_tile_plan<kFeThreads>(a.ctx_lens, a.batch, unit_map(a.n_q, 1, 0), a.cap, a.tile_prefix, a.err);
     return;
   }
   const int rank = blockIdx.x;  // which 16 outputs

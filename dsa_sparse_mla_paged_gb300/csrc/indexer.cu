@@ -27,15 +27,15 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
                                                           const float* __restrict__ w,
                                                           uint8_t* __restrict__ q8,
                                                           float* __restrict__ wq,
-                                                          const int32_t* __restrict__ ctx_lens, int batch,
-                                                          int n_q, int cap, int* __restrict__ tile_prefix,
+                                                          const int32_t* __restrict__ ctx_lens, int units,
+                                                          UnitMap map, int cap, int* __restrict__ tile_prefix,
                                                           int* err) {
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (row == gridDim.x - 1) {
-    build_tile_plan<128>(ctx_lens, batch, n_q, cap, tile_prefix, err);
+    build_tile_plan<128>(ctx_lens, units, map, cap, tile_prefix, err);
     return;
   }
   // all eight heads' loads first (independent), then the per-head reductions
@@ -68,10 +68,11 @@ __global__ void __launch_bounds__(128) idx_q_quant_kernel(const __nv_bfloat16* _
 }
 
 cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
-                               const float* w, const int32_t* ctx_lens, cudaStream_t st) {
+                               const float* w, const int32_t* ctx_lens, cudaStream_t st, int world, int rank) {
+  const UnitMap map = unit_map(p.n_q, world, rank);
   return launch_pdl(idx_q_quant_kernel, dim3(L.rows + 1), dim3(128), 0, st,
                     static_cast<const __nv_bfloat16*>(q_idx), w, reinterpret_cast<uint8_t*>(ws + L.q8),
-                    reinterpret_cast<float*>(ws + L.wq), ctx_lens, p.batch, p.n_q, L.cap,
+                    reinterpret_cast<float*>(ws + L.wq), ctx_lens, p.batch * map.groups, map, L.cap,
                     reinterpret_cast<int*>(ws + L.tiles), reinterpret_cast<int*>(ws + L.err));
 }
 
@@ -112,10 +113,29 @@ struct IdxTc {
   float* scores;
   int64_t score_stride;
   int64_t key_page_stride;
-  int batch, n_q, max_pages, num_pages, stages, nacc, group, ncol, tmem_cols;
+  int units, n_q, max_pages, num_pages, stages, nacc, group, ncol, tmem_cols;  // n_q: rows per unit
   int raw_slots;  // MXFP4: raw page-pair slots
+  UnitMap map;
   int* err;
 };
+
+// Unit u: request, first query row (global), valid rows, and context (that of
+// its last row; the rows before it see fewer tokens).
+struct UnitInfo {
+  int b, row0, valid, ctx;
+};
+
+__device__ __forceinline__ int unit_req(const IdxTc& a, int u) { return u / a.map.groups; }
+
+__device__ __forceinline__ UnitInfo unit_info(const IdxTc& a, int u) {
+  UnitInfo x;
+  x.b = u / a.map.groups;
+  const int first = unit_first_row(a.map, u - x.b * a.map.groups);
+  x.row0 = x.b * a.map.rows_per_req + first;
+  x.valid = min(a.map.gsz, a.map.rows_per_req - first);
+  x.ctx = a.ctx_lens[x.b] - a.map.rows_per_req + first + x.valid;
+  return x;
+}
 
 struct TileWalk {
   int b, j;        // request, tile within the request
@@ -124,7 +144,7 @@ struct TileWalk {
 };
 
 __device__ __forceinline__ void walk_start(const IdxTc& a, long long t0, TileWalk& w) {
-  int lo = 0, hi = a.batch - 1;
+  int lo = 0, hi = a.units - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
     if (a.tile_prefix[mid] > t0) hi = mid; else lo = mid + 1;
@@ -138,7 +158,7 @@ __device__ __forceinline__ void walk_start(const IdxTc& a, long long t0, TileWal
 __device__ __forceinline__ void walk_next(const IdxTc& a, TileWalk& w) {
   ++w.t;
   ++w.j;
-  while (w.t >= w.end_b && w.b + 1 < a.batch) {
+  while (w.t >= w.end_b && w.b + 1 < a.units) {
     ++w.b;
     w.j = 0;
     w.end_b = a.tile_prefix[w.b];
@@ -165,12 +185,12 @@ __device__ __forceinline__ void advance_walk(const IdxTc& a, TileWalk& w, int& n
   w.j += n;
   if (w.t >= w.end_b) {
     const int b0 = w.b;
-    while (w.t >= w.end_b && w.b + 1 < a.batch) {
+    while (w.t >= w.end_b && w.b + 1 < a.units) {
       ++w.b;
       w.end_b = a.tile_prefix[w.b];
     }
     w.j = int(w.t - (w.b ? a.tile_prefix[w.b - 1] : 0));
-    if (w.b != b0) np = (a.ctx_lens[w.b] + kPage - 1) / kPage;
+    if (w.b != b0) np = (unit_info(a, w.b).ctx + kPage - 1) / kPage;
   }
 }
 
@@ -184,7 +204,7 @@ __device__ __forceinline__ TilePages tile_pages(const IdxTc& a, const TileWalk& 
   if (lane) advance_walk(a, x, xnp, lane);
   tp.b = x.b;
   const int lp0 = 2 * x.j;
-  const int32_t* row = a.block_table + size_t(x.b) * a.max_pages;
+  const int32_t* row = a.block_table + size_t(unit_req(a, x.b)) * a.max_pages;
   tp.pg0 = row[lp0];
   tp.two = lp0 + 1 < xnp;
   if (tp.two) tp.pg1 = row[lp0 + 1];
@@ -199,13 +219,13 @@ struct EpiState {
 // Reduce one 32-column accumulator block (tile e.g, query row e.t) of this
 // thread's token row and store the score, then step to the next block.
 __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
-                                          int lane, TileWalk& w, EpiState& e, int& cur_b, int& ctx,
+                                          int lane, TileWalk& w, EpiState& e, int& cur_b, UnitInfo& ui,
                                           float (&wl)[kMaxNQ], float (&wr)[kIdxHeads]) {
   if (e.t == 0 && w.b != cur_b) {
     cur_b = w.b;
-    ctx = a.ctx_lens[w.b];
+    ui = unit_info(a, w.b);
     if (a.n_q == 1) {
-      const float4* src = reinterpret_cast<const float4*>(a.wq + size_t(w.b) * kIdxHeads);
+      const float4* src = reinterpret_cast<const float4*>(a.wq + size_t(ui.row0) * kIdxHeads);
 #pragma unroll
       for (int i = 0; i < kIdxHeads / 4; ++i) {
         const float4 f = src[i];
@@ -213,7 +233,7 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
       }
     } else {
 #pragma unroll
-      for (int t = 0; t < kMaxNQ; ++t) wl[t] = t < a.n_q ? a.wq[(size_t(w.b) * a.n_q + t) * kIdxHeads + lane] : 0.f;
+      for (int t = 0; t < kMaxNQ; ++t) wl[t] = t < ui.valid ? a.wq[(size_t(ui.row0) + t) * kIdxHeads + lane] : 0.f;
     }
   }
   float scale = sc[0], wt = wl[0];
@@ -237,8 +257,8 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
   }
   const float sum = (part[0] + part[1]) + (part[2] + part[3]);
   const int tok = w.j * kTileTok + rowt;
-  const int Lt = ctx - a.n_q + e.t + 1;
-  if (tok < Lt && tok < a.score_stride) a.scores[(size_t(w.b) * a.n_q + e.t) * a.score_stride + tok] = sum;
+  const int Lt = ui.ctx - ui.valid + e.t + 1;  // rows past `valid` (a short last group) get Lt <= 0
+  if (tok < Lt && tok < a.score_stride) a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
   if (++e.t == a.n_q) {
     e.t = 0;
     ++e.g;
@@ -331,7 +351,7 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the tile plan and the query come from the previous kernel
-  const long long T = a.tile_prefix[a.batch - 1];
+  const long long T = a.tile_prefix[a.units - 1];
   const long long t_begin = T * blockIdx.x / gridDim.x;
   const long long t_end = T * (blockIdx.x + 1) / gridDim.x;
 
@@ -359,7 +379,7 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
       const uint64_t pol = ptx::policy_evict_first();
       TileWalk base;
       walk_start(a, t_begin, base);
-      int base_np = (a.ctx_lens[base.b] + kPage - 1) / kPage;
+      int base_np = (unit_info(a, base.b).ctx + kPage - 1) / kPage;
       TilePages cur = tile_pages(a, base, base_np, t_end, lane);
       int cur_b = -1, nq = -1;
       int s = 0;          // ring stage
@@ -434,7 +454,7 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
               if (!ptx::mbar_wait(qempty + slot, (uint32_t(nq >> 1) & 1u) ^ 1u)) { fail(); ok = false; }
               if (ok) {
                 ptx::mbar_arrive_expect_tx(qfull + slot, qbytes);
-                ptx::tma_load_2d(qbuf + slot * qbytes, &qmap, qfull + slot, 0, b * a.n_q * kIdxHeads);
+                ptx::tma_load_2d(qbuf + slot * qbytes, &qmap, qfull + slot, 0, unit_info(a, b).row0 * kIdxHeads);
                 cur_b = b;
               }
             }
@@ -522,7 +542,8 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
       const int rowt = quad * 32 + lane;
       TileWalk w;
       walk_start(a, t_begin, w);
-      int cur_b = -1, ctx = 0;
+      int cur_b = -1;
+      UnitInfo ui{0, 0, 0, 0};
       float wl[kMaxNQ];  // lane h holds w'_h of each query row of the current request
       float wr[kIdxHeads];  // one query row: all head weights
       int s = 0, acc = 0;
@@ -549,11 +570,11 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
 #pragma unroll 1
         for (int c = 0; c < nb; c += 2) {
           if (c + 1 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 1) * 32), vb);
-          epi_block(a, va, sc, rowt, lane, w, e, cur_b, ctx, wl, wr);
+          epi_block(a, va, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
           if (c + 1 < nb) {
             ptx::tmem_ld_wait(vb);
             if (c + 2 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 2) * 32), va);
-            epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ctx, wl, wr);
+            epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
             if (c + 2 < nb) ptx::tmem_ld_wait(va);
           }
         }
@@ -614,7 +635,9 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int
 
 cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
                            const int32_t* block_table, const int32_t* ctx_lens, float* scores,
-                           int64_t score_stride, cudaStream_t st) {
+                           int64_t score_stride, cudaStream_t st, int world, int rank) {
+  const UnitMap map = unit_map(p.n_q, world, rank);
+  const int gsz = map.gsz;
   const uint8_t* q8 = reinterpret_cast<const uint8_t*>(ws + L.q8);
   const float* wq = reinterpret_cast<const float*>(ws + L.wq);
   int* err = reinterpret_cast<int*>(ws + L.err);
@@ -630,7 +653,7 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   {
     const uint64_t dims[2] = {uint64_t(kIdxDim), uint64_t(L.rows) * kIdxHeads};
     const uint64_t strides[1] = {uint64_t(kIdxDim)};
-    const uint32_t box[2] = {uint32_t(kIdxDim), uint32_t(p.n_q * kIdxHeads)};
+    const uint32_t box[2] = {uint32_t(kIdxDim), uint32_t(gsz * kIdxHeads)};
     if (!encode_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q8, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   IdxTc a;
@@ -642,16 +665,17 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   a.scores = scores;
   a.score_stride = score_stride;
   a.key_page_stride = p.key_page_stride;
-  a.batch = p.batch;
-  a.n_q = p.n_q;
+  a.units = p.batch * map.groups;
+  a.n_q = gsz;
+  a.map = map;
   a.max_pages = p.max_pages_per_req;
   a.num_pages = p.num_pages;
-  a.ncol = p.n_q * kIdxHeads;
+  a.ncol = gsz * kIdxHeads;
   // FP8 keys, one query row: two CTAs per SM, each with half of the shared
   // memory and TMEM (two independent pipelines per SM measured 4% faster than
   // one with twice the tiles per stage). Tiles per stage: as many as fit 256
   // accumulator columns, at most 2 (4 with one CTA per SM).
-  const int cps = (!mx && p.n_q == 1) ? 2 : 1;
+  const int cps = (!mx && gsz == 1) ? 2 : 1;
   a.group = std::max(1, std::min(cps == 2 || mx ? 2 : 4, 256 / a.ncol));
   const int slot_cols = a.group * a.ncol;
   a.nacc = std::max(1, std::min(4, 512 / cps / slot_cols));
@@ -659,7 +683,7 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   while (cols < a.nacc * slot_cols) cols <<= 1;
   a.tmem_cols = cols;
   const size_t stage_bytes = size_t(a.group) * (kKeyTileBytes + kScaleTileBytes);
-  const size_t fixed = 1024 + 2 * size_t(p.n_q) * kIdxHeads * kIdxDim + 512;
+  const size_t fixed = 1024 + 2 * size_t(gsz) * kIdxHeads * kIdxDim + 512;
   const size_t budget = (cps == 2 ? 113 * 1024 : 227 * 1024) - fixed;
   if (mx) {
     // three key stages; the rest of shared memory holds raw page pairs in flight
@@ -676,7 +700,7 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   // enough tiles for every SM is the common case; with fewer, one CTA per tile
-  const long long max_tiles = (long long)p.batch * ((L.cap + kTileTok - 1) / kTileTok);
+  const long long max_tiles = (long long)a.units * ((L.cap + kTileTok - 1) / kTileTok);
   const int grid = int(std::min<long long>(cps * sm_count(), std::max<long long>(1, max_tiles)));
   if (mx) return launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(kMxThreads), smem, st, kmap, qmap, a);
   return launch_pdl(indexer_tc_kernel<false>, dim3(grid), dim3(kTcThreads), smem, st, kmap, qmap, a);

@@ -382,6 +382,8 @@ WORKLOADS = {
     "b4_ctx1m": dict(batch=4, n_q=1, ctx=1 << 20, seed=3, bt_mode="permuted"),
     "b32x6_ctx256k_fp4": dict(batch=32, n_q=6, ctx=1 << 18, seed=4, bt_mode="permuted",
                               key_fmt="mxfp4", lat_fmt="nvfp4"),
+    # a prefill chunk: 2,048 new tokens appended to a 150K-token cached prefix
+    "b1_prefill2k_ctx150k": dict(batch=1, n_q=2048, ctx=150 * 1024 + 2048, seed=7, bt_mode="permuted"),
     # small cases for kernel profiles: each kernel's own inputs still exceed the 129 MB L2
     "b4_ctx256k": dict(batch=4, n_q=1, ctx=1 << 18, seed=5, bt_mode="permuted"),
     "b64_ctx16k": dict(batch=64, n_q=1, ctx=1 << 14, seed=6, bt_mode="permuted"),

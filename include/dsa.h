@@ -94,7 +94,8 @@ typedef enum { DSA_LAT_FP8_576 = 0, DSA_LAT_NVFP4_352 = 1 } dsa_lat_fmt_t;
 
 typedef struct {
   int32_t batch;              /* B >= 1 */
-  int32_t n_q;                /* query tokens per request, 1..8 */
+  int32_t n_q;                /* query tokens per request (decode 1..8, a prefill chunk more;
+                                 batch * n_q <= 65535); the scorer takes them 8 at a time */
   int32_t topk;               /* K, 1..2048 (the article's K is 2048) */
   int32_t page_size;          /* tokens per page; this build: 64 */
   int32_t max_pages_per_req;  /* row stride of block_table (entries); ctx_b <= this * page_size */
@@ -151,6 +152,21 @@ dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, c
  *   phys_rows int32 [B * n_q, K] or NULL: page * page_size + slot of each
  *            selected token ("融合的 indexer ... 输出注意力读取的物理 KV 行"),
  *            -1 padded; needs DSA_EMIT_PHYS_ROWS and block_table. */
+/* Stage 1 for a prefill chunk with token sharding ("预填充：按 token 而非按头分片注意力":
+ * every GPU scores its own query tokens against the whole context; each request
+ * is cut into 16 slices and GPU r of 8 takes slices r and 15 - r, which balances
+ * the causal work). Here: the n_q rows of each request are cut into 2 * world
+ * equal slices and the call scores only rank's two slices, r and
+ * 2 * world - 1 - r, exactly as dsa_indexer_scores would (scores of the other
+ * rows are not written). world = 1 scores every row (= dsa_indexer_scores).
+ *   world, rank  1 <= world, 0 <= rank < world; world > 1 needs n_q to be a
+ *                multiple of 16 * world (slices of whole 8-row groups)
+ * Other arguments, layouts and errors as dsa_indexer_scores (no DSA_Q_PREPARED). */
+dsa_status_t dsa_indexer_prefill_scores(const dsa_params_t* params, int32_t world, int32_t rank, const void* q_idx,
+                                        const float* w, const void* key_pool, const int32_t* block_table,
+                                        const int32_t* ctx_lens, float* scores, int64_t score_stride, void* ws,
+                                        size_t ws_bytes, cudaStream_t stream);
+
 dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t score_stride,
                       const int32_t* ctx_lens, const int32_t* block_table, int32_t* topk_idx,
                       int32_t* phys_rows, void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -210,7 +226,7 @@ typedef struct {
  *   x       bf16 [B * n_q, d_model]      w_k bf16 [128, d_model]
  *   key_pool written at one slot per row (16-B aligned, like every bf16 input)
  *   q8_out  E4M3 [B * n_q, 32, 128] or NULL; w_out fp32 [B * n_q, 32] or NULL (copies)
- * Limits: B * n_q <= 512 (else DSA_ERR_UNSUPPORTED).
+ * Limits: n_q <= 8 and B * n_q <= 512 (else DSA_ERR_UNSUPPORTED).
  * Errors: a row with an invalid ctx_b or block-table entry writes no key and
  * sets DSA_DEVERR_CTX / DSA_DEVERR_BLOCK_TABLE in the workspace. */
 dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend_dims_t* dims, const void* c_q,

@@ -47,7 +47,7 @@ def test_workspace_size_and_layout(lib):
 @pytest.mark.parametrize("kw,status", [
     (dict(batch=0), dsa.DSA_ERR_INVALID),
     (dict(n_q=0), dsa.DSA_ERR_INVALID),
-    (dict(n_q=9), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(batch=2, n_q=40000), dsa.DSA_ERR_UNSUPPORTED),
     (dict(topk=4096), dsa.DSA_ERR_UNSUPPORTED),
     (dict(topk=0), dsa.DSA_ERR_INVALID),
     (dict(page_size=32), dsa.DSA_ERR_UNSUPPORTED),
