@@ -257,8 +257,10 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
   }
   const float sum = (part[0] + part[1]) + (part[2] + part[3]);
   const int tok = w.j * kTileTok + rowt;
-  const int Lt = ui.ctx - ui.valid + e.t + 1;  // rows past `valid` (a short last group) get Lt <= 0
-  if (tok < Lt && tok < a.score_stride) a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
+  const int Lt = ui.ctx - ui.valid + e.t + 1;
+  // a short last group computes padding rows past `valid`: never stored
+  if (e.t < ui.valid && tok < Lt && tok < a.score_stride)
+    a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
   if (++e.t == a.n_q) {
     e.t = 0;
     ++e.g;
