@@ -216,12 +216,31 @@ struct EpiState {
   int g, t;
 };
 
+// Step the epilogue position past one block (another warpgroup reduces it).
+__device__ __forceinline__ void epi_skip(const IdxTc& a, TileWalk& w, EpiState& e) {
+  if (++e.t == a.n_q) {
+    e.t = 0;
+    ++e.g;
+    walk_next(a, w);
+  }
+}
+
+__device__ __forceinline__ void epi_store(const IdxTc& a, float sum, int rowt, TileWalk& w, EpiState& e,
+                                          const UnitInfo& ui) {
+  const int tok = w.j * kTileTok + rowt;
+  const int Lt = ui.ctx - ui.valid + e.t + 1;
+  // a short last group computes padding rows past `valid`: never stored
+  if (e.t < ui.valid && tok < Lt && tok < a.score_stride)
+    a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
+  epi_skip(a, w, e);
+}
+
 // Reduce one 32-column accumulator block (tile e.g, query row e.t) of this
 // thread's token row and store the score, then step to the next block.
 __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
                                           int lane, TileWalk& w, EpiState& e, int& cur_b, UnitInfo& ui,
                                           float (&wl)[kMaxNQ], float (&wr)[kIdxHeads]) {
-  if (e.t == 0 && w.b != cur_b) {
+  if (w.b != cur_b) {
     cur_b = w.b;
     ui = unit_info(a, w.b);
     if (a.n_q == 1) {
@@ -256,17 +275,9 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
       part[h & 3] = fmaf(__shfl_sync(0xffffffffu, wt, h), fmaxf(scale * v[h], 0.f), part[h & 3]);
   }
   const float sum = (part[0] + part[1]) + (part[2] + part[3]);
-  const int tok = w.j * kTileTok + rowt;
-  const int Lt = ui.ctx - ui.valid + e.t + 1;
-  // a short last group computes padding rows past `valid`: never stored
-  if (e.t < ui.valid && tok < Lt && tok < a.score_stride)
-    a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
-  if (++e.t == a.n_q) {
-    e.t = 0;
-    ++e.g;
-    walk_next(a, w);
-  }
+  epi_store(a, sum, rowt, w, e, ui);
 }
+
 
 // One MXFP4 token (64 B of E2M1 pairs, element 2i in the low nibble; 4 E8M0
 // exponents) -> 128 E4M3 values into its 128-B swizzled row, and its scale.
@@ -310,9 +321,13 @@ __device__ __forceinline__ void mx_convert_row(const uint8_t* vals, uint32_t e4,
   }
 }
 
-template <bool kMx>
-__global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
+// kEwg epilogue warpgroups (FP8 keys): 1 for one query row, where the kernel
+// is bound by HBM; 2 when a unit has several rows (decode with n_q > 1,
+// prefill), where the reduction of 32 x rows columns per token is the work.
+template <bool kMx, int kEwg>
+__global__ void __launch_bounds__(kMx ? kMxThreads : 64 + 128 * kEwg, (kMx || kEwg > 1) ? 1 : 2)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, IdxTc a) {
+  static_assert(!kMx || kEwg == 1, "the MXFP4 kernel's warps 6..9 convert keys");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages, NA = a.nacc, G = a.group;
@@ -337,9 +352,9 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) { ptx::mbar_init(full + i, kMx ? 4 : 1); ptx::mbar_init(empty + i, 1 + 4); }
+    for (int i = 0; i < S; ++i) { ptx::mbar_init(full + i, kMx ? 4 : 1); ptx::mbar_init(empty + i, 1 + 4 * kEwg); }
     for (int i = 0; i < R; ++i) { ptx::mbar_init(rfull + i, 1); ptx::mbar_init(rempty + i, 4); }
-    for (int i = 0; i < NA; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, 4); }
+    for (int i = 0; i < NA; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, 4 * kEwg); }
     for (int i = 0; i < 2; ++i) { ptx::mbar_init(qfull + i, 1); ptx::mbar_init(qempty + i, 1); }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -538,9 +553,10 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
           if (++s == S) { s = 0; ph ^= 1u; }
         }
       }
-    } else if (warp >= 2 && warp < 6) {
+    } else if (warp >= 2 && warp < 2 + 4 * kEwg) {
       // ------------------------------------------------------------ epilogue
-      const int quad = warp & 3;
+      const int quad = warp & 3;      // TMEM lanes 32 quad .. 32 quad + 31
+      const int eg = (warp - 2) >> 2;  // warpgroup: reduces blocks eg, eg + kEwg, ...
       const int rowt = quad * 32 + lane;
       TileWalk w;
       walk_start(a, t_begin, w);
@@ -561,25 +577,35 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : kTcThreads, kMx ? 1 : 2)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty + s);
         // the stage's accumulators are nb = ng * n_q blocks of 32 columns,
-        // block (g, t) = tile g, query row t; the load of block c + 1 is in
-        // flight while block c is reduced
+        // block (g, t) = tile g, query row t; this warpgroup reduces blocks
+        // eg, eg + kEwg, ... and steps over the others; the load of its next
+        // block is in flight while the current one is reduced
         const uint32_t col0 = tmem + (uint32_t(quad * 32) << 16) + uint32_t(acc * G * a.ncol);
         const int nb = ng * a.n_q;
         EpiState e{0, 0};
+        int pos = 0;  // block the epilogue position e / w points at
         float va[32], vb[32];
-        ptx::tmem_ld32_nowait(col0, va);
-        ptx::tmem_ld_wait(va);
+        if (eg < nb) {
+          ptx::tmem_ld32_nowait(col0 + uint32_t(eg * 32), va);
+          ptx::tmem_ld_wait(va);
+        }
 #pragma unroll 1
-        for (int c = 0; c < nb; c += 2) {
-          if (c + 1 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 1) * 32), vb);
+        for (int c = eg; c < nb; c += 2 * kEwg) {
+          const int c1 = c + kEwg, c2 = c + 2 * kEwg;
+          if (c1 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t(c1 * 32), vb);
+          for (; pos < c; ++pos) epi_skip(a, w, e);
           epi_block(a, va, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
-          if (c + 1 < nb) {
+          ++pos;
+          if (c1 < nb) {
             ptx::tmem_ld_wait(vb);
-            if (c + 2 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t((c + 2) * 32), va);
+            if (c2 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t(c2 * 32), va);
+            for (; pos < c1; ++pos) epi_skip(a, w, e);
             epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
-            if (c + 2 < nb) ptx::tmem_ld_wait(va);
+            ++pos;
+            if (c2 < nb) ptx::tmem_ld_wait(va);
           }
         }
+        for (; pos < nb; ++pos) epi_skip(a, w, e);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tempty + acc);
@@ -697,15 +723,18 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   }
   a.err = err;
   const size_t smem = fixed + size_t(a.stages) * stage_bytes + size_t(a.raw_slots) * kMxRawTile;
-  const void* fn = mx ? reinterpret_cast<const void*>(indexer_tc_kernel<true>)
-                      : reinterpret_cast<const void*>(indexer_tc_kernel<false>);
+  const bool wide = !mx && gsz > 1;  // two epilogue warpgroups
+  const void* fn = mx ? reinterpret_cast<const void*>(indexer_tc_kernel<true, 1>)
+                 : wide ? reinterpret_cast<const void*>(indexer_tc_kernel<false, 2>)
+                        : reinterpret_cast<const void*>(indexer_tc_kernel<false, 1>);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   // enough tiles for every SM is the common case; with fewer, one CTA per tile
   const long long max_tiles = (long long)a.units * ((L.cap + kTileTok - 1) / kTileTok);
   const int grid = int(std::min<long long>(cps * sm_count(), std::max<long long>(1, max_tiles)));
-  if (mx) return launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(kMxThreads), smem, st, kmap, qmap, a);
-  return launch_pdl(indexer_tc_kernel<false>, dim3(grid), dim3(kTcThreads), smem, st, kmap, qmap, a);
+  if (mx) return launch_pdl(indexer_tc_kernel<true, 1>, dim3(grid), dim3(kMxThreads), smem, st, kmap, qmap, a);
+  if (wide) return launch_pdl(indexer_tc_kernel<false, 2>, dim3(grid), dim3(64 + 256), smem, st, kmap, qmap, a);
+  return launch_pdl(indexer_tc_kernel<false, 1>, dim3(grid), dim3(kTcThreads), smem, st, kmap, qmap, a);
 }
 
 }  // namespace dsa
