@@ -384,6 +384,7 @@ WORKLOADS = {
                               key_fmt="mxfp4", lat_fmt="nvfp4"),
     # a prefill chunk: 2,048 new tokens appended to a 150K-token cached prefix
     "b1_prefill2k_ctx150k": dict(batch=1, n_q=2048, ctx=150 * 1024 + 2048, seed=7, bt_mode="permuted"),
+    "b1_prefill512_ctx32k": dict(batch=1, n_q=512, ctx=32768, seed=8, bt_mode="permuted"),
     # small cases for kernel profiles: each kernel's own inputs still exceed the 129 MB L2
     "b4_ctx256k": dict(batch=4, n_q=1, ctx=1 << 18, seed=5, bt_mode="permuted"),
     "b64_ctx16k": dict(batch=64, n_q=1, ctx=1 << 14, seed=6, bt_mode="permuted"),
