@@ -235,6 +235,66 @@ __device__ __forceinline__ void epi_store(const IdxTc& a, float sum, int rowt, T
   epi_skip(a, w, e);
 }
 
+// Packed fp32 pairs (one instruction for two lanes of work; each half rounds
+// as its scalar op would).
+__device__ __forceinline__ unsigned long long f2_pack(float x, float y) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Several query rows with two epilogue warpgroups: the warp keeps the current
+// unit's head weights in its own shared-memory copy (wme[t][h]), read four at a
+// time by every lane, and reduces in packed pairs -- the same operations, in the
+// same order, as the scalar loop of epi_block, so the same bits.
+__device__ __forceinline__ void epi_block_wide(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
+                                               int lane, TileWalk& w, EpiState& e, int& cur_b, UnitInfo& ui,
+                                               float* wme) {
+  if (w.b != cur_b) {
+    cur_b = w.b;
+    ui = unit_info(a, w.b);
+    __syncwarp();  // every lane is done with the previous unit's weights
+#pragma unroll
+    for (int t = 0; t < kMaxNQ; ++t)
+      wme[t * kIdxHeads + lane] = t < ui.valid ? a.wq[(size_t(ui.row0) + t) * kIdxHeads + lane] : 0.f;
+    __syncwarp();
+  }
+  float scale = sc[0];
+#pragma unroll
+  for (int g = 1; g < 4; ++g)
+    if (e.g == g) scale = sc[g];
+  const float4* wrow = reinterpret_cast<const float4*>(wme + e.t * kIdxHeads);
+  const unsigned long long s2 = f2_pack(scale, scale);
+  unsigned long long p01 = f2_pack(0.f, 0.f), p23 = p01;  // partial sums of heads 4i + {0, 1} and 4i + {2, 3}
+#pragma unroll
+  for (int i = 0; i < kIdxHeads / 4; ++i) {
+    const float4 w4 = wrow[i];
+    float2 x = f2_unpack(f2_mul(s2, f2_pack(v[4 * i], v[4 * i + 1])));
+    float2 y = f2_unpack(f2_mul(s2, f2_pack(v[4 * i + 2], v[4 * i + 3])));
+    p01 = f2_fma(f2_pack(w4.x, w4.y), f2_pack(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), p01);
+    p23 = f2_fma(f2_pack(w4.z, w4.w), f2_pack(fmaxf(y.x, 0.f), fmaxf(y.y, 0.f)), p23);
+  }
+  const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
+  const float sum = (a01.x + a01.y) + (a23.x + a23.y);
+  epi_store(a, sum, rowt, w, e, ui);
+}
+
 // Reduce one 32-column accumulator block (tile e.g, query row e.t) of this
 // thread's token row and store the score, then step to the next block.
 __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
@@ -334,7 +394,8 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : 64 + 128 * kEwg, (kMx || kE
   const int qbytes = a.n_q * kIdxHeads * kIdxDim;
   uint8_t* keys = smem;                                           // S x G x 16 KB
   uint8_t* qbuf = keys + size_t(S) * G * kKeyTileBytes;           // 2 x qbytes
-  float* scl = reinterpret_cast<float*>(qbuf + 2 * qbytes);       // S x G x 128
+  float* wsm = reinterpret_cast<float*>(qbuf + 2 * qbytes);       // wide epilogue: 8 warps x 8 rows x 32 heads
+  float* scl = wsm + (kEwg > 1 ? 4 * kEwg * kMaxNQ * kIdxHeads : 0);  // S x G x 128
   uint8_t* raw = reinterpret_cast<uint8_t*>(scl + size_t(S) * G * kTileTok);  // MXFP4: R x 8,704 B
   const int R = kMx ? a.raw_slots : 0;
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw + size_t(R) * kMxRawTile);
@@ -563,6 +624,7 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : 64 + 128 * kEwg, (kMx || kE
       int cur_b = -1;
       UnitInfo ui{0, 0, 0, 0};
       float wl[kMaxNQ];  // lane h holds w'_h of each query row of the current request
+      float* wme = wsm + (warp - 2) * (kMaxNQ * kIdxHeads);  // wide epilogue: this warp's weights
       float wr[kIdxHeads];  // one query row: all head weights
       int s = 0, acc = 0;
       uint32_t aph = 0;
@@ -594,13 +656,15 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : 64 + 128 * kEwg, (kMx || kE
           const int c1 = c + kEwg, c2 = c + 2 * kEwg;
           if (c1 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t(c1 * 32), vb);
           for (; pos < c; ++pos) epi_skip(a, w, e);
-          epi_block(a, va, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
+          if constexpr (kEwg > 1) epi_block_wide(a, va, sc, rowt, lane, w, e, cur_b, ui, wme);
+          else epi_block(a, va, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
           ++pos;
           if (c1 < nb) {
             ptx::tmem_ld_wait(vb);
             if (c2 < nb) ptx::tmem_ld32_nowait(col0 + uint32_t(c2 * 32), va);
             for (; pos < c1; ++pos) epi_skip(a, w, e);
-            epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
+            if constexpr (kEwg > 1) epi_block_wide(a, vb, sc, rowt, lane, w, e, cur_b, ui, wme);
+            else epi_block(a, vb, sc, rowt, lane, w, e, cur_b, ui, wl, wr);
             ++pos;
             if (c2 < nb) ptx::tmem_ld_wait(va);
           }
@@ -711,7 +775,9 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   while (cols < a.nacc * slot_cols) cols <<= 1;
   a.tmem_cols = cols;
   const size_t stage_bytes = size_t(a.group) * (kKeyTileBytes + kScaleTileBytes);
-  const size_t fixed = 1024 + 2 * size_t(gsz) * kIdxHeads * kIdxDim + 512;
+  const bool wide = !mx && gsz > 1;  // two epilogue warpgroups
+  const size_t fixed = 1024 + 2 * size_t(gsz) * kIdxHeads * kIdxDim + 512 +
+                       (wide ? size_t(8) * kMaxNQ * kIdxHeads * 4 : 0);
   const size_t budget = (cps == 2 ? 113 * 1024 : 227 * 1024) - fixed;
   if (mx) {
     // three key stages; the rest of shared memory holds raw page pairs in flight
@@ -723,7 +789,6 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   }
   a.err = err;
   const size_t smem = fixed + size_t(a.stages) * stage_bytes + size_t(a.raw_slots) * kMxRawTile;
-  const bool wide = !mx && gsz > 1;  // two epilogue warpgroups
   const void* fn = mx ? reinterpret_cast<const void*>(indexer_tc_kernel<true, 1>)
                  : wide ? reinterpret_cast<const void*>(indexer_tc_kernel<false, 2>)
                         : reinterpret_cast<const void*>(indexer_tc_kernel<false, 1>);
