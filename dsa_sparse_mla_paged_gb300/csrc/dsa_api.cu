@@ -48,7 +48,8 @@ dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA
 dsa_status_t check_indexer_args(const dsa_params_t* p, const void* q_idx, const float* w,
                                 const void* key_pool, const int32_t* bt, const int32_t* ctx) {
   if (!key_pool || !bt || !ctx || !aligned16(key_pool)) return DSA_ERR_INVALID;
-  if (p->flags & DSA_Q_PREPARED) return DSA_OK;  // the query is already in the workspace
+  if (p->flags & DSA_Q_PREPARED)  // the query is already in the workspace (decode rows only)
+    return p->n_q > kMaxNQ ? DSA_ERR_UNSUPPORTED : DSA_OK;
   if (!q_idx || !w) return DSA_ERR_INVALID;
   if (!aligned16(q_idx) || !aligned16(key_pool) || (reinterpret_cast<uintptr_t>(w) & 3)) return DSA_ERR_INVALID;
   return DSA_OK;

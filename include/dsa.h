@@ -84,7 +84,8 @@ typedef enum { DSA_LAT_FP8_576 = 0, DSA_LAT_NVFP4_352 = 1 } dsa_lat_fmt_t;
 #define DSA_Q_PREPARED 0x2      /* dsa_indexer_scores / dsa_decode take the quantised query,
                                    the folded weights and the scorer's plan that
                                    dsa_indexer_frontend left in the same workspace (same
-                                   params and ctx_lens); q_idx and w may be NULL */
+                                   params and ctx_lens); q_idx and w may be NULL;
+                                   n_q <= 8 (else DSA_ERR_UNSUPPORTED) */
 
 /* Device error word bits (dsa_get_device_error). */
 #define DSA_DEVERR_BLOCK_TABLE 0x1  /* a block-table entry outside [0, num_pages) */

@@ -182,3 +182,23 @@ def test_frontend_row_limit(lib):
     st = lib.dsa_indexer_frontend(ctypes.byref(p), ctypes.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                   FAKE, FAKE, None, None, FAKE, need, None)
     assert st == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_prepared_query_needs_decode_rows(lib):
+    p = _params(n_q=16, flags=dsa.DSA_Q_PREPARED)
+    need = dsa.workspace_size(p)
+    st = lib.dsa_indexer_scores(ctypes.byref(p), None, None, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need, None)
+    assert st == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_prefill_world_and_rank_checked(lib):
+    p = _params(n_q=64)
+    need = dsa.workspace_size(p)
+    call = lambda world, rank: lib.dsa_indexer_prefill_scores(ctypes.byref(p), world, rank, FAKE, FAKE, FAKE, FAKE,
+                                                              FAKE, FAKE, 640, FAKE, need, None)
+    assert call(0, 0) == dsa.DSA_ERR_INVALID
+    assert call(2, 2) == dsa.DSA_ERR_INVALID
+    assert call(2, -1) == dsa.DSA_ERR_INVALID
+    assert call(3, 0) == dsa.DSA_ERR_INVALID       # 64 rows are not 6 slices of whole 8-row groups
+    a = list((ctypes.byref(p), 4, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need - 1, None))
+    assert lib.dsa_indexer_prefill_scores(*a) == dsa.DSA_ERR_WORKSPACE
