@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kFeThreads, 2)
     idx_frontend_kernel(FeArgs a) {
   pdl_trigger();
   extern __shared__ __align__(16) float fe_in[];           // [R][kFeBlk * 256] staged inputs (fp32)
-  __shared__ float s_ss[R][(kFeThreads / 32) / R];
+  __shared__ float s_rstd[R];
   __shared__ int s_last;
   const int job = blockIdx.y;
   if (job == kFeJobs - 1) {  // the tile plan
@@ -188,18 +188,14 @@ __global__ void __launch_bounds__(kFeThreads, 2)
   pdl_wait();
   for (int r0 = 0, pass = 0; r0 < a.rows; r0 += R, ++pass) {
     const int nr = min(R, a.rows - r0);
-    // ---- staging work: warp w serves row rw = w % R and the chunks j = w / R
-    // (mod kWpr) of it, so every warp stages (R = 4: two warps per row)
-    constexpr int kWpr = (kFeThreads / 32) / R;
-    const int rw = warp % R, wk = warp / R;
-    // the query rows' sums of squares, in kWpr parts; the first block's raw
+    // ---- the query rows' 1 / RMS (warp w: row r0 + w); the first block's raw
     // values stay in shared memory for the staging below
     __syncthreads();  // the previous pass's inputs are consumed
-    if (!is_key && rw < nr) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(r0 + rw) * d);
-      float4* raw = reinterpret_cast<float4*>(fe_in) + size_t(rw) * kFeBlk * 64;
+    if (!is_key && warp < nr) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(r0 + warp) * d);
+      float4* raw = reinterpret_cast<float4*>(fe_in) + size_t(warp) * kFeBlk * 64;
       float ss = 0.f;
-      for (int j = wk; j < nch; j += kWpr) {
+      for (int j = 0; j < nch; ++j) {
         float f[8];
         bf16x8(__ldg(src + j * 32 + lane), f);
         if (j < kFeBlk) {
@@ -211,9 +207,9 @@ __global__ void __launch_bounds__(kFeThreads, 2)
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) s_ss[rw][wk] = ss;
+      if (lane == 0) s_rstd[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(d)), a.eps)));
+      __syncwarp();  // the warp's staging reads it
     }
-    __syncthreads();
     float acc0[R], acc1[R];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) acc0[rr] = acc1[rr] = 0.f;
@@ -231,13 +227,13 @@ __global__ void __launch_bounds__(kFeThreads, 2)
           wb[u] = __ldg(pw1 + u * 32 + lane);
         }
       if (jb != cj0) __syncthreads();  // the previous block's inputs are consumed
-      // ---- stage the block's inputs as fp32 (warp w: row rw, chunks wk mod kWpr)
-      if (rw < nr) {
-        const int row = r0 + rw;
-        float4* dst = reinterpret_cast<float4*>(fe_in) + size_t(rw) * kFeBlk * 64;
+      // ---- stage the block's inputs as fp32: warp w prepares row r0 + w
+      if (warp < nr) {
+        const int row = r0 + warp;
+        float4* dst = reinterpret_cast<float4*>(fe_in) + size_t(warp) * kFeBlk * 64;
         if (is_key) {
           const uint4* src = reinterpret_cast<const uint4*>(a.x + size_t(row) * d) + jb * 32;
-          for (int j = wk; j < nj; j += kWpr) {
+          for (int j = 0; j < nj; ++j) {
             float f[8];
             bf16x8(__ldg(src + j * 32 + lane), f);
             dst[(j * 32 + lane) * 2] = make_float4(f[0], f[1], f[2], f[3]);
@@ -246,11 +242,8 @@ __global__ void __launch_bounds__(kFeThreads, 2)
         } else {
           const uint4* src = reinterpret_cast<const uint4*>(a.c_q + size_t(row) * d) + jb * 32;
           const uint4* g = reinterpret_cast<const uint4*>(a.gamma) + jb * 32;
-          float ss = s_ss[rw][0];
-#pragma unroll
-          for (int k = 1; k < kWpr; ++k) ss += s_ss[rw][k];
-          const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(d)), a.eps)));
-          for (int j = wk; j < nj; j += kWpr) {
+          const float rstd = s_rstd[warp];  // written by this warp's lane 0
+          for (int j = 0; j < nj; ++j) {
             float f[8], gg[8], n[8];
             if (jb == 0) {  // the raw values are already here (this lane wrote them)
               const float4 ra = dst[(j * 32 + lane) * 2], rb = dst[(j * 32 + lane) * 2 + 1];
