@@ -8,14 +8,15 @@
 //          the shard's order (bf16 score key desc, token asc), as the lists a
 //          GPU would keep (key, token) by position
 //   merge  one CTA per row: round 1 packs each shard's first m = ceil(1.5 K / W)
-//          candidates into 32-bit words (key16 << 16 | (4095 - position) << 4 |
-//          (15 - shard)), radix-selects the K largest, and finds the shards
-//          whose m candidates were all selected while they hold more; those
-//          send their first K and round 2 selects again. The winners are
-//          written in ascending token order with the round's traffic.
-// and the cross-shard LSE combine of the shards' partial attention outputs
-// (same section: each GPU attends over its own winners, then the partials are
-// merged by their log-sum-exp).
+//          candidates (at most K) into 32-bit words (key16 << 16 |
+//          (4095 - position) << 4 | (15 - shard)), radix-selects the K largest,
+//          and finds the shards whose m candidates were all selected while they
+//          hold more among their first K; those send their first K and round 2
+//          selects again. The winners are written in ascending token order,
+//          with the re-sent shard mask and the words exchanged.
+// Then a fourth kernel, the cross-shard LSE combine of the shards' partial
+// attention outputs (same section: each GPU attends over its own winners,
+// then the partials are merged by their log-sum-exp).
 #include <cuda_bf16.h>
 
 #include "block_select.cuh"
