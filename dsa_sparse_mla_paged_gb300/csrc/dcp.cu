@@ -21,6 +21,7 @@
 
 #include "block_select.cuh"
 #include "dsa_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace dsa {
 
@@ -166,83 +167,134 @@ __device__ __forceinline__ int2 top_bin(const int* H, int kk, int* smw, int* s_o
   return make_int2(s_out[0], s_out[1]);
 }
 
+// Distributed shared memory of the shard cluster (addresses from mapa).
+__device__ __forceinline__ uint32_t dsm_ld_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void dsm_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void dsm_st_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t dsm_atom_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void dsm_red_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+constexpr int kShardCluster = 4;  // CTAs per (row, shard)
+
 // The n-th largest key16 of the shard (an 11-bit and a 5-bit histogram pass:
 // 11 bits spread the keys over enough bins that the shared atomics rarely
 // collide), then the tokens above it and the lowest-token ties at it, sorted
-// into the shard order.
-__global__ void __launch_bounds__(kDcpThreads, 1) dcp_shard_kernel(DcpArgs a) {
+// into the shard order. A cluster of kShardCluster CTAs shares the shard's
+// positions: each counts its quarter into its own histogram and adds it into
+// the first CTA's, which picks the bins; the tokens found go to the first
+// CTA's list, which sorts and writes it.
+__global__ void __cluster_dims__(kShardCluster, 1, 1) __launch_bounds__(kDcpThreads, 1)
+    dcp_shard_kernel(DcpArgs a) {
   pdl_wait();
-  __shared__ int hist[kHiBins];
-  __shared__ int s_sel[4];  // high bin, count above it, threshold key, ties wanted
-  __shared__ int s_n[2];    // list fill, tie fill
+  __shared__ int hist[kHiBins];     // this CTA's counts
+  __shared__ int hsum[kHiBins];     // first CTA: the cluster's pass-1 counts
+  __shared__ int hsum2[1 << kLoBits];  // first CTA: the cluster's pass-2 counts
+  __shared__ int s_sel[4];          // first CTA: high bin, count above it, threshold key, ties wanted
+  __shared__ int s_n[3];            // first CTA: list fill, tie fill, ties at the threshold
   __shared__ int smw[64];
   extern __shared__ uint64_t dcp_smem[];
-  uint64_t* list = dcp_smem;                                   // [2048] (0xFFFF - key) << 32 | token
-  uint32_t* ties = reinterpret_cast<uint32_t*>(list + kMaxTopK);  // [kTieCap] tokens at the threshold
-  const int r = blockIdx.x, row = blockIdx.y;
+  uint64_t* list = dcp_smem;                                   // first CTA: [2048] (0xFFFF - key) << 32 | token
+  uint32_t* ties = reinterpret_cast<uint32_t*>(list + kMaxTopK);  // first CTA: [kTieCap] tokens at the threshold
+  const uint32_t q = ptx::cluster_ctarank();
+  const int r = blockIdx.x / kShardCluster, row = blockIdx.y;
   const int L = dcp_row_len(a, row, false);
   const int Lr = L > r ? (L - 1 - r) / a.W + 1 : 0;
   const int n = min(a.K, Lr);
   int32_t* cnt_out = a.lcount + size_t(row) * kDcpMaxWorld + r;
-  if (n == 0) {
-    if (threadIdx.x == 0) *cnt_out = 0;
+  if (n == 0) {  // the whole cluster
+    if (q == 0 && threadIdx.x == 0) *cnt_out = 0;
     return;
   }
   const uint16_t* src = a.keys16 + (size_t(row) * a.W + r) * a.S;
   const int nv = (Lr + 7) / 8;
+  const int per = (nv + kShardCluster - 1) / kShardCluster;
+  const int v0 = int(q) * per, v1 = min(nv, v0 + per);  // this CTA's vectors of 8 positions
+  const auto first = [](const void* p) { return ptx::mapa_shared(ptx::smem_u32(p), 0); };
   uint32_t k[8];
+  for (int i = threadIdx.x; i < kHiBins; i += kDcpThreads) {
+    hist[i] = 0;
+    hsum[i] = 0;
+  }
+  if (threadIdx.x < (1 << kLoBits)) hsum2[threadIdx.x] = 0;
+  ptx::cluster_sync();  // every CTA runs and the first CTA's sums are zero
   // pass 1: the high 11 bits
-  for (int i = threadIdx.x; i < kHiBins; i += kDcpThreads) hist[i] = 0;
-  __syncthreads();
-  for (int v = threadIdx.x; v < nv; v += kDcpThreads) {
+  for (int v = v0 + int(threadIdx.x); v < v1; v += kDcpThreads) {
     keys8(src, v, Lr, k);
 #pragma unroll
     for (int e = 0; e < 8; ++e)
       if (k[e] != kNoKey) atomicAdd(&hist[k[e] >> kLoBits], 1);
   }
   __syncthreads();
-  const int2 hbin = top_bin(hist, n, smw, s_sel);
-  const uint32_t hb = uint32_t(hbin.x);
-  const int above_hb = hbin.y;
+  for (int i = threadIdx.x; i < kHiBins; i += kDcpThreads) {
+    if (hist[i]) dsm_red_add(first(&hsum[i]), uint32_t(hist[i]));
+    hist[i] = 0;
+  }
+  ptx::cluster_sync();  // the first CTA holds the cluster's counts
+  if (q == 0) top_bin(hsum, n, smw, s_sel);
+  ptx::cluster_sync();
+  const uint32_t hb = dsm_ld_u32(first(&s_sel[0]));
+  const int above_hb = int(dsm_ld_u32(first(&s_sel[1])));
   // pass 2: the low 5 bits within that bin
-  for (int i = threadIdx.x; i < (1 << kLoBits); i += kDcpThreads) hist[i] = 0;
-  __syncthreads();
-  for (int v = threadIdx.x; v < nv; v += kDcpThreads) {
+  for (int v = v0 + int(threadIdx.x); v < v1; v += kDcpThreads) {
     keys8(src, v, Lr, k);
 #pragma unroll
     for (int e = 0; e < 8; ++e)
       if (k[e] != kNoKey && (k[e] >> kLoBits) == hb) atomicAdd(&hist[k[e] & ((1u << kLoBits) - 1)], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < (1 << kLoBits) && hist[threadIdx.x])
+    dsm_red_add(first(&hsum2[threadIdx.x]), uint32_t(hist[threadIdx.x]));
+  ptx::cluster_sync();
+  if (q == 0 && threadIdx.x == 0) {
     int above = above_hb, l = (1 << kLoBits) - 1;
     for (; l > 0; --l) {
-      if (above + hist[l] >= n) break;
-      above += hist[l];
+      if (above + hsum2[l] >= n) break;
+      above += hsum2[l];
     }
     s_sel[2] = int((hb << kLoBits) | uint32_t(l));
     s_sel[3] = n - above;  // ties at the threshold to take (lowest tokens first)
     s_n[0] = 0;
     s_n[1] = 0;
+    s_n[2] = hsum2[l];
   }
-  __syncthreads();
-  const uint32_t tau = uint32_t(s_sel[2]);
-  const int need = s_sel[3];
-  const int n_ties = hist[tau & ((1u << kLoBits) - 1)];
-  // pass 3: tokens above the threshold, and the ties (all of them when they fit)
-  for (int v = threadIdx.x; v < nv; v += kDcpThreads) {
-    keys8(src, v, Lr, k);
+  ptx::cluster_sync();
+  const uint32_t tau = dsm_ld_u32(first(&s_sel[2]));
+  const int n_ties = int(dsm_ld_u32(first(&s_n[2])));
+  // pass 3: tokens above the threshold, and the ties (all of them when they fit), into the first CTA
+  {
+    const uint32_t list0 = first(list), ties0 = first(ties), nl0 = first(&s_n[0]), nt0 = first(&s_n[1]);
+    for (int v = v0 + int(threadIdx.x); v < v1; v += kDcpThreads) {
+      keys8(src, v, Lr, k);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t tok = uint32_t(r + (8 * v + e) * a.W);
-      if (k[e] != kNoKey && k[e] > tau) {
-        list[atomicAdd(&s_n[0], 1)] = (uint64_t(0xFFFFu - k[e]) << 32) | tok;
-      } else if (k[e] == tau && n_ties <= kTieCap) {
-        ties[atomicAdd(&s_n[1], 1)] = tok;
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t tok = uint32_t(r + (8 * v + e) * a.W);
+        if (k[e] != kNoKey && k[e] > tau) {
+          const uint32_t at = dsm_atom_add(nl0, 1u);
+          dsm_st_u64(list0 + 8u * at, (uint64_t(0xFFFFu - k[e]) << 32) | tok);
+        } else if (k[e] == tau && n_ties <= kTieCap) {
+          const uint32_t at = dsm_atom_add(nt0, 1u);
+          dsm_st_u32(ties0 + 4u * at, tok);
+        }
       }
     }
   }
-  __syncthreads();
+  ptx::cluster_sync();  // the first CTA holds every token found
+  if (q != 0) return;
+  const int need = s_sel[3];
   const int n_gt = s_n[0];
   if (n_ties <= kTieCap) {
     // lowest `need` tokens among the ties
@@ -517,7 +569,7 @@ cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws,
     e = launch_pdl(dcp_keys_kernel, dim3((L.cap + 4 * kKeysThreads - 1) / (4 * kKeysThreads), L.rows),
                    dim3(kKeysThreads), 0, st, a);
   if (e == cudaSuccess)
-    e = launch_pdl(dcp_shard_kernel, dim3(world, L.rows), dim3(kDcpThreads), shard_smem, st, a);
+    e = launch_pdl(dcp_shard_kernel, dim3(world * kShardCluster, L.rows), dim3(kDcpThreads), shard_smem, st, a);
   if (e == cudaSuccess) e = launch_pdl(dcp_merge_kernel, dim3(L.rows), dim3(kDcpThreads), merge_smem, st, a);
   return e;
 }
