@@ -64,39 +64,43 @@ __device__ __forceinline__ uint32_t bf16_order_key(float f) {
   return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
 
-// Ascending bitonic sort of the 2048 64-bit keys v[0 .. 2048) by the CTA's
-// 1024 threads. Thread t holds elements 2t and 2t + 1 in registers; a partner
-// in the same warp (stride < 64) is read by shuffle, any other through shared
-// memory (15 of the 66 steps). v must be written and synchronised before the
-// call; it holds the sorted keys after.
-__device__ void sort2048_u64(uint64_t* v) {
+// Ascending bitonic sort of the 2048 keys v[0 .. 2048) (32- or 64-bit) by
+// the CTA's 1024 threads, the network unrolled at compile time. Thread t holds
+// elements 2t and 2t + 1 in registers; a partner in the same warp (stride < 64)
+// is read by shuffle, any other through shared memory (15 of the 66 steps).
+// v must be written and synchronised before the call; it holds the sorted keys
+// after.
+template <typename T>
+__device__ __forceinline__ void sort2048(T* v) {
   static_assert(kDcpThreads == 1024, "two keys per thread");
   const int e0 = 2 * int(threadIdx.x);
-  uint64_t x0 = v[e0], x1 = v[e0 + 1];
+  T x0 = v[e0], x1 = v[e0 + 1];
+#pragma unroll
   for (int size = 2; size <= 2048; size <<= 1) {
     const bool up = (e0 & size) == 0;
+#pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       if (stride == 1) {
-        const uint64_t lo = x0 < x1 ? x0 : x1, hi = x0 < x1 ? x1 : x0;
+        const T lo = x0 < x1 ? x0 : x1, hi = x0 < x1 ? x1 : x0;
         x0 = up ? lo : hi;
         x1 = up ? hi : lo;
-        continue;
-      }
-      uint64_t y0, y1;
-      if (stride < 64) {
-        y0 = __shfl_xor_sync(0xffffffffu, x0, stride >> 1);
-        y1 = __shfl_xor_sync(0xffffffffu, x1, stride >> 1);
       } else {
-        __syncthreads();  // the previous exchange has been read
-        v[e0] = x0;
-        v[e0 + 1] = x1;
-        __syncthreads();
-        y0 = v[e0 ^ stride];
-        y1 = v[(e0 ^ stride) + 1];
+        T y0, y1;
+        if (stride < 64) {
+          y0 = __shfl_xor_sync(0xffffffffu, x0, stride >> 1);
+          y1 = __shfl_xor_sync(0xffffffffu, x1, stride >> 1);
+        } else {
+          __syncthreads();  // the previous exchange has been read
+          v[e0] = x0;
+          v[e0 + 1] = x1;
+          __syncthreads();
+          y0 = v[e0 ^ stride];
+          y1 = v[(e0 ^ stride) + 1];
+        }
+        const bool keep_min = ((e0 & stride) == 0) == up;
+        x0 = keep_min ? (x0 < y0 ? x0 : y0) : (x0 < y0 ? y0 : x0);
+        x1 = keep_min ? (x1 < y1 ? x1 : y1) : (x1 < y1 ? y1 : x1);
       }
-      const bool keep_min = ((e0 & stride) == 0) == up;
-      x0 = keep_min ? (x0 < y0 ? x0 : y0) : (x0 < y0 ? y0 : x0);
-      x1 = keep_min ? (x1 < y1 ? x1 : y1) : (x1 < y1 ? y1 : x1);
     }
   }
   __syncthreads();
@@ -341,7 +345,7 @@ __global__ void __cluster_dims__(kShardCluster, 1, 1) __launch_bounds__(kDcpThre
   // the shard order: key desc, token asc
   for (int i = n + threadIdx.x; i < kMaxTopK; i += kDcpThreads) list[i] = ~0ull;
   __syncthreads();
-  sort2048_u64(list);
+  sort2048<uint64_t>(list);
   uint32_t* kout = a.lkey + (size_t(row) * kDcpMaxWorld + r) * a.K;
   int32_t* tout = a.ltok + (size_t(row) * kDcpMaxWorld + r) * a.K;
   for (int j = threadIdx.x; j < n; j += kDcpThreads) {
@@ -377,7 +381,7 @@ __device__ __forceinline__ void round_words(const DcpArgs& a, int row, const int
 // go to win[] in candidate order (block scan, no contended atomics).
 template <int PER>
 __device__ __forceinline__ void take_round(const DcpArgs& a, int row, const uint32_t (&wd)[PER], uint32_t tau,
-                                           const int* off, uint32_t* selbits, int* sel, uint64_t* win, int* smw,
+                                           const int* off, uint32_t* selbits, int* sel, uint32_t* win, int* smw,
                                            bool collect) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int mine = 0;
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
   pdl_wait();
   extern __shared__ uint64_t dcp_smem[];
   int* hist = reinterpret_cast<int*>(dcp_smem);                   // [4096] radix select
-  uint64_t* win = dcp_smem + 2048;                                 // [2048] winners (token)
+  uint32_t* win = reinterpret_cast<uint32_t*>(dcp_smem + 2048);  // [2048] winners (token)
   __shared__ int smw[64];
   __shared__ uint32_t selbits[32 * kDcpThreads / 32];             // one bit per candidate (32 per thread)
   __shared__ int cnt[kDcpMaxWorld], off[kDcpMaxWorld + 1], held[kDcpMaxWorld], sel[kDcpMaxWorld];
@@ -468,9 +472,9 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
     }
   }
   // winners in ascending token order (exactly K of them: the words are distinct)
-  for (int i = a.K + threadIdx.x; i < kMaxTopK; i += kDcpThreads) win[i] = ~0ull;
+  for (int i = a.K + threadIdx.x; i < kMaxTopK; i += kDcpThreads) win[i] = 0xFFFFFFFFu;
   __syncthreads();
-  sort2048_u64(win);
+  sort2048<uint32_t>(win);
   for (int i = threadIdx.x; i < a.K; i += kDcpThreads) out[i] = int32_t(win[i]);
   if (a.stats && threadIdx.x == 0) {
     a.stats[2 * row] = s_resend;
