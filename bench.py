@@ -502,7 +502,7 @@ def run_ours(args, rank, world):
         bufs.append({"d_in": d_in, "d_out": d_out, "h_out": h_out, "views": views,
                      "out": piece(d_out, 0, out), "lse": piece(d_out, o_off, lse)})
     h2d, d2h = int(h_in.numel()), int(bufs[0]["h_out"].numel())
-    copy_st = torch.cuda.Stream()
+    in_st, out_st = torch.cuda.Stream(), torch.cuda.Stream()
 
     def decode_into(bf, s_):
         e_q_idx, e_w, e_q, e_bt, e_ctx = bf["views"]
@@ -517,27 +517,31 @@ def run_ours(args, rank, world):
             bf["graph"] = torch.cuda.CUDAGraph()
             with torch.cuda.graph(bf["graph"], stream=stream):
                 decode_into(bf, torch.cuda.current_stream())
-        bf["ev_in"], bf["ev_done"] = torch.cuda.Event(), torch.cuda.Event()
+        bf["ev_in"], bf["ev_done"], bf["ev_out"] = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
 
     def run_e2e(n):
+        # inputs in on in_st, the step on `stream`, results out on out_st
         for i in range(n):
             bf = bufs[i & 1]
-            copy_st.wait_event(bf["ev_done"])  # step i - 2 has read these inputs and its results left
-            with torch.cuda.stream(copy_st):
+            in_st.wait_event(bf["ev_done"])  # step i - 2 has read these inputs
+            with torch.cuda.stream(in_st):
                 bf["d_in"].copy_(h_in, non_blocking=True)
-            bf["ev_in"].record(copy_st)
+            bf["ev_in"].record(in_st)
             stream.wait_event(bf["ev_in"])
+            stream.wait_event(bf["ev_out"])  # step i - 2's results have left
             with torch.cuda.stream(stream):
                 bf["graph"].replay()
             bf["ev_done"].record(stream)
-            copy_st.wait_event(bf["ev_done"])
-            with torch.cuda.stream(copy_st):
+            out_st.wait_event(bf["ev_done"])
+            with torch.cuda.stream(out_st):
                 bf["h_out"].copy_(bf["d_out"], non_blocking=True)
-        stream.wait_stream(copy_st)
+            bf["ev_out"].record(out_st)
+        stream.wait_stream(out_st)
 
     torch.cuda.synchronize()
     for bf in bufs:
         bf["ev_done"].record(stream)
+        bf["ev_out"].record(stream)
     run_e2e(4)
     torch.cuda.synchronize()
     for bf in bufs:
@@ -545,7 +549,7 @@ def run_ours(args, rank, world):
     ke2e = max(6, min(args.steps, 100))
     barrier()
     ev[0].record(stream)
-    copy_st.wait_event(ev[0])
+    in_st.wait_event(ev[0])
     run_e2e(ke2e)
     ev[1].record(stream)
     barrier()
