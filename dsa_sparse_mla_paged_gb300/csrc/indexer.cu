@@ -777,7 +777,7 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   const size_t stage_bytes = size_t(a.group) * (kKeyTileBytes + kScaleTileBytes);
   const bool wide = !mx && gsz > 1;  // two epilogue warpgroups
   const size_t fixed = 1024 + 2 * size_t(gsz) * kIdxHeads * kIdxDim + 512 +
-                       (wide ? size_t(8) * kMaxNQ * kIdxHeads * 4 : 0);
+                       (wide ? size_t(12) * kMaxNQ * kIdxHeads * 4 : 0);
   const size_t budget = (cps == 2 ? 113 * 1024 : 227 * 1024) - fixed;
   if (mx) {
     // three key stages; the rest of shared memory holds raw page pairs in flight
@@ -790,7 +790,7 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   a.err = err;
   const size_t smem = fixed + size_t(a.stages) * stage_bytes + size_t(a.raw_slots) * kMxRawTile;
   const void* fn = mx ? reinterpret_cast<const void*>(indexer_tc_kernel<true, 1>)
-                 : wide ? reinterpret_cast<const void*>(indexer_tc_kernel<false, 2>)
+                 : wide ? reinterpret_cast<const void*>(indexer_tc_kernel<false, 3>)
                         : reinterpret_cast<const void*>(indexer_tc_kernel<false, 1>);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
@@ -798,7 +798,7 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   const long long max_tiles = (long long)a.units * ((L.cap + kTileTok - 1) / kTileTok);
   const int grid = int(std::min<long long>(cps * sm_count(), std::max<long long>(1, max_tiles)));
   if (mx) return launch_pdl(indexer_tc_kernel<true, 1>, dim3(grid), dim3(kMxThreads), smem, st, kmap, qmap, a);
-  if (wide) return launch_pdl(indexer_tc_kernel<false, 2>, dim3(grid), dim3(64 + 256), smem, st, kmap, qmap, a);
+  if (wide) return launch_pdl(indexer_tc_kernel<false, 3>, dim3(grid), dim3(64 + 384), smem, st, kmap, qmap, a);
   return launch_pdl(indexer_tc_kernel<false, 1>, dim3(grid), dim3(kTcThreads), smem, st, kmap, qmap, a);
 }
 
