@@ -12,9 +12,9 @@
  *   3. MLA attention runs exactly over those tokens only, reading each one's
  *      576-B FP8 latent (512 "nope" + 64 "rope" values) shared by all 96
  *      query heads.
- * The caches are paged; the kernels reach them through a block table (section
- * "面向三种状态的 KV 缓存": "the block table and cache slots are turned into
- * kernel page addresses before each step").
+ * The caches are paged; the kernels reach them through a block table, which
+ * maps each request's logical pages to physical pages (section "面向三种状态的
+ * KV 缓存" describes the translation to page addresses done before each step).
  *
  * Conventions shared by every call
  * --------------------------------
