@@ -1,7 +1,8 @@
 // The fused indexer front end of a decode step ("vLLM 为 Kimi K3.1 Pro 提供 Day-0
-// 支持", section "低延迟解码：融合的 DSA 解码路径": the query norm, the indexer's
-// query projection, its FP8 quantisation folded into the head weights and the
-// new token's index key, in one kernel). For query row (b, t):
+// 支持", section "低延迟解码：融合的 DSA 解码路径": a single kernel normalises the
+// query latent, projects it onto the indexer heads, makes it FP8 with the scale
+// moved into the head weights, and produces the new token's index key).
+// For query row (b, t):
 //   n  = bf16(c_q / sqrt(mean(c_q^2) + eps) * gamma)       query RMS norm
 //   q  = bf16(n @ W_q^T)                                    32 heads x 128
 //   q8 = E4M3(q * 448 / amax_h), w' = w * (amax_h / 448)    the scorer's inputs

@@ -154,9 +154,9 @@ dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, c
  *            selected token ("融合的 indexer ... 输出注意力读取的物理 KV 行"),
  *            -1 padded; needs DSA_EMIT_PHYS_ROWS and block_table. */
 /* Stage 1 for a prefill chunk with token sharding ("预填充：按 token 而非按头分片注意力":
- * every GPU scores its own query tokens against the whole context; each request
- * is cut into 16 slices and GPU r of 8 takes slices r and 15 - r, which balances
- * the causal work). Here: the n_q rows of each request are cut into 2 * world
+ * the GPUs divide a prefill's query tokens, not its heads, and pair slices so
+ * that causal work evens out: with 8 GPUs and 16 slices, GPU r has r and 15 - r).
+ * Here: the n_q rows of each request are cut into 2 * world
  * equal slices and the call scores only rank's two slices, r and
  * 2 * world - 1 - r, exactly as dsa_indexer_scores would (scores of the other
  * rows are not written). world = 1 scores every row (= dsa_indexer_scores).
@@ -208,9 +208,10 @@ typedef struct {
   float eps;        /* RMS norm epsilon, >= 0 */
 } dsa_frontend_dims_t;
 
-/* The fused indexer front end ("低延迟解码：融合的 DSA 解码路径": the query norm,
- * the indexer's query projection, its FP8 quantisation folded into the head
- * weights and the new token's index key, in one kernel). For row (b, t):
+/* The fused indexer front end ("低延迟解码：融合的 DSA 解码路径": one kernel for the
+ * work ahead of the scorer -- normalise the query latent, project it onto the
+ * indexer heads, make it FP8 with the scale moved into the head weights, and
+ * produce the new token's index key). For row (b, t):
  *   n  = bf16(c_q / sqrt(mean(c_q^2) + eps) * gamma_q)     (fp32 arithmetic)
  *   q  = bf16(n @ w_q^T), q[h] = q[128 h .. 128 h + 127]   (fp32 accumulation)
  *   q8[h] = E4M3_rne_satfinite(q[h] * (448 / amax_h)), w'[h] = w[h] * (amax_h / 448)

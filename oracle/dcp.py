@@ -3,15 +3,14 @@
 Source: "vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "长上下文：带稀疏 indexer 的
 decode 上下文并行", subsection "流量减少 10× 的精确 top-k 合并".
 
-What the page describes: W GPUs split a request's cache by token, GPU r holding
-every W-th token (tokens s with s mod W == r). Each GPU ranks only its own
-tokens, so the global top-2048 is merged before attention. Instead of sending
-its whole local top-2048 (fp32 score, token id pairs), each GPU picks its best
-1.5 * 2048 / W candidates straight from BF16 scores and packs each candidate
-with its score into 32 bits; every GPU gathers all packs and radix-selects the
-same global top-2048. The merge stays exact: when a GPU holds more of the
-top-2048 than it sent, the selection notices and that GPU re-sends its full
-local top-k for the row.
+The method, restated: a request's cache is divided by token over W GPUs
+(GPU r owns the tokens s with s mod W == r), so each GPU can rank only its own
+tokens and the global top-2048 has to be assembled across them. The exchange
+is kept small: a GPU contributes a fixed number of its best tokens (1.5 * 2048
+/ W), each as one 32-bit word holding its BF16 score, and every GPU runs the
+same radix selection over all contributions. Exactness is restored by a check
+after that selection: a GPU whose every contribution won may own further
+winners, and it then contributes its complete local top-k for that row.
 
 Readings (the page gives the steps, not the bits):
   * BF16 score: round-to-nearest-even of the fp32 score. Its order key is the

@@ -2,9 +2,10 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: "vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "低延迟解码：融合的 DSA
-解码路径" [FUSE]: one kernel takes the query norm, the indexer's query
-projection, its FP8 quantisation folded into the head weights, and the new
-token's index key. The MXFP4 key format is the page's "量化：原生 MXFP4 索引器"
+解码路径" [FUSE], which fuses into a single kernel the work ahead of the scorer:
+normalising the query latent, projecting it onto the indexer heads, turning the
+result into FP8 with its scale moved into the head weights, and producing the
+new token's index key. The MXFP4 key format is the page's "量化：原生 MXFP4 索引器"
 [MX4] in the OCP Microscaling layout (formats.py).
 
 Readings (the page names the steps, not their arithmetic):

@@ -1,9 +1,9 @@
 """Token-sharded prefill of the indexer -- TEST INFRASTRUCTURE ONLY.
 
 Source: "vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "预填充：按 token 而非按头分片注意力":
-for large prefill steps every GPU scores its own query tokens against the whole
-context with every indexer head; to balance causal attention each request is
-cut into 16 slices and GPU r takes slices r and 15 - r (8 GPUs).
+in a large prefill the GPUs divide the query tokens rather than the heads, each
+scoring its tokens against the whole context; the division pairs slices so that
+the causal work evens out (8 GPUs, 16 slices, GPU r with slices r and 15 - r).
 
 Reading: with W ranks, the n_q query rows of a request are cut into 2W equal
 slices of consecutive rows; rank r owns slices r and 2W - 1 - r. The scores of
