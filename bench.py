@@ -180,7 +180,21 @@ def cpu_baseline(inp, budget_s=15.0):
     per_step = dt / done * inp.batch
     return {"value": 1.0 / per_step, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"{done} of {inp.batch} requests of one step (numpy float64; BLAS threads = default)",
-            "seconds": dt}
+            "seconds": dt, "single_thread_b1_ctx4k_s": oracle_single_thread_small()}
+
+
+def oracle_single_thread_small():
+    """Seconds of the oracle's whole step on the small parity workload (b1_ctx4k),
+    in a fresh interpreter limited to one BLAS / OpenMP thread."""
+    code = ("import sys, time; sys.path.insert(0, %r); import gen; from oracle import dsa as O; "
+            "inp = gen.make_workload('b1_ctx4k'); t = time.perf_counter(); O.decode(inp); "
+            "print(time.perf_counter() - t)") % ROOT
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=300)
+        return float(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
 
 
 def run_reference(args, rank):
