@@ -340,20 +340,26 @@ def run_stage(args):
                      "keys_scored": keys, "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9,
                      "tflops": flops / (ms * 1e-3) / 1e12})
     if args.stage == "dcp_merge":
-        from oracle import dcp as D
-
         st = stats.cpu().numpy()
         full = W * inp.topk * 8  # every shard's local top-K as (fp32 score, int32 token) pairs
         line.update({"world": W, "resent_rows": int((st[:, 0] != 0).sum()),
                      "words_per_row": [int(x) for x in st[:, 1]],
                      "traffic_ratio_vs_full_exchange": [full / (4 * int(x)) for x in st[:, 1]]})
-        # the oracle beside it, on the first row of the same scores
-        row = sc[0, :int(inp.ctx[0]) - inp.n_q + 1].cpu().numpy()
-        t0 = time.perf_counter()
-        res = D.merge(row, W, inp.topk)
-        line["oracle_ms_per_row"] = (time.perf_counter() - t0) * 1e3
-        line["row0_equals_oracle"] = bool(np.array_equal(idx[0].cpu().numpy(), res["idx"]))
+        line["cpu_baseline"] = cpu_baseline_dcp(sc[0, :int(inp.ctx[0]) - inp.n_q + 1].cpu().numpy(), W, inp.topk,
+                                                idx[0].cpu().numpy())
     print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_dcp(row, world, topk, gpu_idx):
+    """The oracle's merge of one row of the same scores, timed on the host (the
+    stage's CPU baseline), and whether the GPU's row equals it."""
+    from oracle import dcp as D
+
+    t0 = time.perf_counter()
+    res = D.merge(row, world, topk)
+    dt = time.perf_counter() - t0
+    return {"kind": "oracle", "sample": "row 0 of the call", "ms_per_row": dt * 1e3,
+            "cores": len(os.sched_getaffinity(0)), "row0_equals_gpu": bool(np.array_equal(gpu_idx, res["idx"]))}
 
 
 def _rank_rows(n_q, world, rank):
