@@ -31,3 +31,12 @@ def test_paired_slices_balance_causal_work_and_contiguous_ones_do_not():
     r = 3
     rows = list(range(r * ss, (r + 1) * ss)) + list(range((2 * world - 1 - r) * ss, (2 * world - r) * ss))
     assert work[r] == sum(ctx - n_q + t + 1 for t in rows) == ss * (2 * (ctx - n_q + 1) + n_q - 1)
+
+
+def test_bench_counts_the_same_rows_as_the_split():
+    import bench
+
+    for world in (1, 2, 8):
+        n_q = 64 * world
+        for rank in range(world):
+            assert bench._rank_rows(n_q, world, rank) == P.rank_rows(n_q, world, rank).tolist()
