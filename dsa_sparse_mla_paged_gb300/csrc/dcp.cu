@@ -7,12 +7,12 @@
 //   shard  one CTA per (shard, row): the shard's first min(K, L_r) tokens in
 //          the shard's order (bf16 score key desc, token asc), as the lists a
 //          GPU would keep (key, token) by position
-//   merge  one CTA per row: round 1 packs each shard's first m = ceil(1.5 K / W)
+//   merge  one CTA per row: the first exchange packs each shard's first m = ceil(1.5 K / W)
 //          candidates (at most K) into 32-bit words (key16 << 16 |
 //          (4095 - position) << 4 | (15 - shard)), radix-selects the K largest,
 //          and finds the shards whose m candidates were all selected while they
-//          hold more among their first K; those send their first K and round 2
-//          selects again. The winners are written in ascending token order,
+//          hold more among their first K; those send their first K and a second
+//          exchange selects again. The winners are written in ascending token order,
 //          with the re-sent shard mask and the words exchanged.
 // Then a fourth kernel, the cross-shard LSE combine of the shards' partial
 // attention outputs (same section: each GPU attends over its own winners,
@@ -356,9 +356,9 @@ __global__ void __cluster_dims__(kShardCluster, 1, 1) __launch_bounds__(kDcpThre
 }
 
 // ---------------------------------------------------------------- merge
-// Candidate c of a round (shard lists laid end to end, `cnt` per shard) -> word.
+// Candidate c of an exchange (shard lists laid end to end, `cnt` per shard) -> word.
 template <int PER>
-__device__ __forceinline__ void round_words(const DcpArgs& a, int row, const int* cnt, const int* off, int total,
+__device__ __forceinline__ void exchange_words(const DcpArgs& a, int row, const int* cnt, const int* off, int total,
                                             uint32_t (&words)[PER]) {
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
@@ -374,13 +374,13 @@ __device__ __forceinline__ void round_words(const DcpArgs& a, int row, const int
   }
 }
 
-// One round's selection bookkeeping. The selected words are the ones >= tau.
+// One exchange's selection bookkeeping. The selected words are the ones >= tau.
 // A shard's words fall with its position, so its selected words are a prefix
 // of its candidates; sel[r] is that prefix's length, found by the one selected
 // candidate whose successor (same shard) is not selected. The winners' tokens
 // go to win[] in candidate order (block scan, no contended atomics).
 template <int PER>
-__device__ __forceinline__ void take_round(const DcpArgs& a, int row, const uint32_t (&wd)[PER], uint32_t tau,
+__device__ __forceinline__ void take_exchange(const DcpArgs& a, int row, const uint32_t (&wd)[PER], uint32_t tau,
                                            const int* off, uint32_t* selbits, int* sel, uint32_t* win, int* smw,
                                            bool collect) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -435,27 +435,27 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
   }
   if (threadIdx.x == 0) s_resend = 0;
   __syncthreads();
-  for (int round = 0; round < 2; ++round) {
+  for (int ex = 0; ex < 2; ++ex) {
     if (threadIdx.x == 0) {
-      int o = 0, words = round == 0 ? 0 : s_words;
+      int o = 0, words = ex == 0 ? 0 : s_words;
       for (int r = 0; r < a.W; ++r) {
         const bool full = (s_resend >> r) & 1;
         cnt[r] = min(full ? a.K : a.m, held[r]);
         off[r] = o;
         o += cnt[r];
-        if (round == 0 || full) words += cnt[r];
+        if (ex == 0 || full) words += cnt[r];
       }
       off[a.W] = o;
       s_words = words;
     }
     __syncthreads();
     const int total = off[a.W];
-    // the K largest words (all distinct); round 2 holds at most ~W/1.5 full lists
-    if (round == 0) {
+    // the K largest words (all distinct); the second exchange holds at most ~W/1.5 full lists
+    if (ex == 0) {
       uint32_t wd[4];
-      round_words<4>(a, row, cnt, off, total, wd);
+      exchange_words<4>(a, row, cnt, off, total, wd);
       const uint32_t tau = block_kth_key<kDcpThreads, 4>(wd, a.K, hist, smw);
-      take_round<4>(a, row, wd, tau, off, selbits, sel, win, smw, true);
+      take_exchange<4>(a, row, wd, tau, off, selbits, sel, win, smw, true);
       if (threadIdx.x == 0) {
         int mask = 0;
         for (int r = 0; r < a.W; ++r)
@@ -463,12 +463,12 @@ __global__ void __launch_bounds__(kDcpThreads, 1) dcp_merge_kernel(DcpArgs a) {
         s_resend = mask;
       }
       __syncthreads();
-      if (s_resend == 0) break;  // round 1's winners stand
+      if (s_resend == 0) break;  // the first exchange's winners stand
     } else {
       uint32_t wd[32];
-      round_words<32>(a, row, cnt, off, total, wd);
+      exchange_words<32>(a, row, cnt, off, total, wd);
       const uint32_t tau = block_kth_key<kDcpThreads, 32>(wd, a.K, hist, smw);
-      take_round<32>(a, row, wd, tau, off, selbits, sel, win, smw, true);
+      take_exchange<32>(a, row, wd, tau, off, selbits, sel, win, smw, true);
     }
   }
   // winners in ascending token order (exactly K of them: the words are distinct)

@@ -246,9 +246,9 @@ dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend
  * 32-bit word key16 << 16 | (4095 - j) << 4 | (15 - r), key16 being the
  * order-preserving 16-bit key of the bf16 score, so word order is the global
  * order (key desc, position asc, shard asc).
- *   round 1  every shard sends its first m = ceil(1.5 K / W) candidates (all
+ *   exchange 1  every shard sends its first m = ceil(1.5 K / W) candidates (all
  *            it holds, if fewer); the K largest words are selected.
- *   round 2  only if some shard holds more than m tokens and all m it sent
+ *   exchange 2  only if some shard holds more than m tokens and all m it sent
  *            were selected: each such shard sends its first min(K, L_r) and
  *            the K largest words are selected again.
  * The result is the top min(K, L) of all tokens under the global order, written

@@ -23,11 +23,11 @@ Readings (the page gives the steps, not the bits):
     the sender's list (the sender keeps the position -> token map) instead of a
     token id, which would not fit. W <= 16 and positions < 4096.
   * The global order is the pack order: bf16 key desc, then position asc, then
-    shard asc. The round sends m = ceil(1.5 K / W) candidates per shard (all a
+    shard asc. The first exchange sends m = ceil(1.5 K / W) candidates per shard (all a
     shard holds when it holds fewer), but never more than K: a shard's tokens
     past its first K cannot be in the top K, and m > K only when W = 1.
   * Re-send test: shard r sent m candidates, holds more than m tokens among its
-    first K, and all m are among the round's top K; then it sends its first K
+    first K, and all m are among that exchange's top K; then it sends its first K
     instead (all it holds when fewer) and the selection runs again. (A shard
     that already sent its first K cannot hold more winners, so m >= K never
     re-sends.)
@@ -78,16 +78,16 @@ def _select(words: np.ndarray, k: int) -> np.ndarray:
 
 
 def merge(scores: np.ndarray, W: int, k: int = 2048) -> dict:
-    """The two-round exact merge. Returns
+    """The exact merge in one or two exchanges. Returns
     idx      int32 [k]: the selected tokens, ascending, -1 padded
     resent   shards that re-sent their first k
-    words    32-bit words exchanged in all (each shard's sent words once per round it sends)
+    words    32-bit words exchanged in all (each shard's sent words once per exchange it sends in)
     """
     assert 1 <= W <= 16 and k <= 4096
     m = math.ceil(1.5 * k / W)
     lists = [shard_list(scores, W, r) for r in range(W)]
 
-    def round_(counts):
+    def exchange(counts):
         words, toks, owner = [], [], []
         for r, (tok, key) in enumerate(lists):
             n = min(counts[r], len(tok))
@@ -100,14 +100,14 @@ def merge(scores: np.ndarray, W: int, k: int = 2048) -> dict:
 
     counts = [min(m, k)] * W
     sent = sum(min(m, k, len(t)) for t, _ in lists)
-    tok_sel, own_sel = round_(counts)
+    tok_sel, own_sel = exchange(counts)
     resent = [r for r in range(W)
               if min(k, len(lists[r][0])) > m and int((own_sel == r).sum()) == m]
     if resent:
         for r in resent:
             counts[r] = k
             sent += min(k, len(lists[r][0]))
-        tok_sel, _ = round_(counts)
+        tok_sel, _ = exchange(counts)
     out = np.full(k, -1, dtype=np.int32)
     keep = np.sort(tok_sel)
     out[:len(keep)] = keep

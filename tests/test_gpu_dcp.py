@@ -1,5 +1,5 @@
 """GPU parity of the decode-context-parallel exact top-k merge (W token shards
-emulated on one GPU) against the oracle's two-round merge: selected tokens
+emulated on one GPU) against the oracle's merge (one or two exchanges): selected tokens
 bit-exact, and the re-sent shard mask and the words exchanged equal.
 
 Source: "vLLM 为 Kimi K3.1 Pro 提供 Day-0 支持", section "长上下文：带稀疏 indexer
