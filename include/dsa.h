@@ -246,11 +246,12 @@ dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend
  * 32-bit word key16 << 16 | (4095 - j) << 4 | (15 - r), key16 being the
  * order-preserving 16-bit key of the bf16 score, so word order is the global
  * order (key desc, position asc, shard asc).
- *   exchange 1  every shard sends its first m = ceil(1.5 K / W) candidates (all
- *            it holds, if fewer); the K largest words are selected.
- *   exchange 2  only if some shard holds more than m tokens and all m it sent
- *            were selected: each such shard sends its first min(K, L_r) and
- *            the K largest words are selected again.
+ *   exchange 1  every shard sends its first m = ceil(1.5 K / W) candidates
+ *               (at most K; all it holds, if fewer); the K largest words are
+ *               selected.
+ *   exchange 2  only if some shard holds more than m tokens among its first K
+ *               and all m it sent were selected: each such shard sends its
+ *               first min(K, L_r) and the K largest words are selected again.
  * The result is the top min(K, L) of all tokens under the global order, written
  * like dsa_topk (ascending token order, -1 padded); rows with L <= K keep every
  * token. It equals dsa_topk's except where bf16 rounding ties or reorders
@@ -258,8 +259,8 @@ dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend
  *   world   W, 1 .. 16 (shard and position must fit the word's 16 low bits)
  *   scores, score_stride, ctx_lens, topk_idx  as dsa_topk
  *   stats   int32 [B * n_q, 2] or NULL: per row the bit mask of shards that
- *           re-sent in round 2, and the words all shards sent in both rounds
- *           (a row with L <= K reports 0 and L)
+ *           re-sent in exchange 2, and the words all shards sent in both
+ *           exchanges (a row with L <= K reports 0 and L)
  * Errors as dsa_topk; the workspace holds the shard lists. */
 dsa_status_t dsa_dcp_topk_merge(const dsa_params_t* params, const float* scores, int64_t score_stride,
                                 const int32_t* ctx_lens, int32_t world, int32_t* topk_idx, int32_t* stats,
