@@ -150,11 +150,27 @@ def check_scores(got: np.ndarray, ref: np.ndarray, errscale: np.ndarray | None =
     return float(rel.max())
 
 
+def selection_errscale(inp, es):
+    """The error scale to widen the selection window with, or None.
+
+    With non-negative head weights every term of score(t, s) over the heads is
+    >= 0, so the score near tau carries no cancellation across heads and the
+    strict window TIE_RTOL * |tau| applies unchanged. Only signed head weights
+    (which can cancel a score towards zero while fp32 rounding still scales with
+    the terms) take the wider window."""
+    return es if np.any(np.asarray(inp.w) < 0) else None
+
+
+# differing tokens that needed the wider (signed-weight) window, for reporting
+WIDE_WINDOW_USES = []
+
+
 def check_selection(got_idx: np.ndarray, ref_idx: np.ndarray, ref_scores: np.ndarray, k: int,
                     errscale: np.ndarray | None = None):
-    """Equal sets except tokens whose oracle score is within TIE_RTOL*|tau| of tau (or,
-    given errscale, within the score bar of check_scores for that token and the
-    rank-k token); both ascending, -1 padded."""
+    """Equal sets except tokens whose oracle score is within TIE_RTOL*|tau| of tau;
+    both ascending, -1 padded. Given errscale (signed head weights only, see
+    selection_errscale), the window is widened to the score bar of check_scores
+    for that token and the rank-k token."""
     from oracle import dsa as O
 
     for arr in (got_idx, ref_idx):
@@ -168,11 +184,13 @@ def check_selection(got_idx: np.ndarray, ref_idx: np.ndarray, ref_scores: np.nda
     tau = O.kth_score(ref_scores, k)
     diff = np.array(sorted(g ^ r))
     dev = np.abs(ref_scores[diff].astype(np.float64) - tau)
-    win = np.full(len(diff), TIE_RTOL * abs(tau))
+    strict = np.full(len(diff), TIE_RTOL * abs(tau))
+    win = strict
     if errscale is not None:
         order = np.lexsort((np.arange(len(ref_scores)), -ref_scores.astype(np.float64)))
         e_tau = errscale[order[k - 1]]
-        win = np.maximum(win, SCORE_RTOL * COND_FRAC * (errscale[diff] + e_tau))
+        win = np.maximum(strict, SCORE_RTOL * COND_FRAC * (errscale[diff] + e_tau))
+        WIDE_WINDOW_USES.append(int((dev > strict).sum()))
     assert (dev <= win).all(), f"selection differs beyond near-ties: {diff[dev > win][:10]}"
     return len(diff)
 

@@ -18,7 +18,7 @@ from oracle import dsa as O
 from oracle import frontend as F
 from oracle.formats import e4m3_decode
 
-from dsa_testlib import Dev, bf16_to_np, check_attention, check_selection, score_error_scale
+from dsa_testlib import Dev, bf16_to_np, check_attention, check_selection, score_error_scale, selection_errscale
 
 pytestmark = pytest.mark.gpu
 
@@ -158,7 +158,8 @@ def test_prepared_query_feeds_the_scorer_and_the_decode():
     idx = idx_p.cpu().numpy()
     for (b, t), r in O.decode(upd).items():
         row = b * 2 + t
-        check_selection(idx[row], r["idx"], r["scores"], upd.topk, score_error_scale(upd, b, t))
+        check_selection(idx[row], r["idx"], r["scores"], upd.topk,
+                        selection_errscale(upd, score_error_scale(upd, b, t)))
         ro, rl = O.sparse_mla(upd, b, t, idx[row])
         check_attention(bf16_to_np(out_p[row]), lse_p[row].cpu().numpy(), ro, rl)
 

@@ -14,7 +14,7 @@ import gen
 from oracle import dsa as O
 
 from dsa_testlib import (Dev, bf16_to_np, check_attention, check_scores, check_selection,
-                         rows_error_scale, rows_scores_oracle, score_error_scale)
+                         rows_error_scale, rows_scores_oracle, score_error_scale, selection_errscale)
 
 pytestmark = pytest.mark.gpu
 
@@ -170,7 +170,8 @@ def test_decode_end_to_end_small(case):
     res = O.decode(inp)
     for (b, t), r in res.items():
         row = b * inp.n_q + t
-        check_selection(idx[row], r["idx"], r["scores"], inp.topk, score_error_scale(inp, b, t))
+        check_selection(idx[row], r["idx"], r["scores"], inp.topk,
+                        selection_errscale(inp, score_error_scale(inp, b, t)))
     # attention over the GPU's own (validated) selection
     ro, rl = _oracle_mla_all(inp, idx)
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
@@ -189,7 +190,7 @@ def test_decode_query_rows_and_k(nq, topk, ctx):
     for (b, t), r in O.decode(inp).items():
         row = b * inp.n_q + t
         check_scores(sc[row, :len(r["scores"])], r["scores"], es[row])
-        check_selection(idx[row], r["idx"], r["scores"], inp.topk, es[row])
+        check_selection(idx[row], r["idx"], r["scores"], inp.topk, selection_errscale(inp, es[row]))
     ro, rl = _oracle_mla_all(inp, idx)
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
 
@@ -222,7 +223,8 @@ def test_decode_on_packed_block_rows(kf, lf):
     idx = idx.cpu().numpy()
     for (b, t), r in O.decode(inp).items():
         row_i = b * inp.n_q + t
-        check_selection(idx[row_i], r["idx"], r["scores"], inp.topk, score_error_scale(inp, b, t))
+        check_selection(idx[row_i], r["idx"], r["scores"], inp.topk,
+                        selection_errscale(inp, score_error_scale(inp, b, t)))
     ro, rl = _oracle_mla_all(inp, idx)
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
     assert dsa.get_device_error(d.ws) == 0
@@ -335,7 +337,8 @@ def test_fp4_decode_end_to_end_small(case):
     out, lse, idx = d.decode()
     idx = idx.cpu().numpy()
     for (b, t), r in O.decode(inp).items():
-        check_selection(idx[b * inp.n_q + t], r["idx"], r["scores"], inp.topk, score_error_scale(inp, b, t))
+        check_selection(idx[b * inp.n_q + t], r["idx"], r["scores"], inp.topk,
+                        selection_errscale(inp, score_error_scale(inp, b, t)))
     ro, rl = _oracle_mla_all(inp, idx)
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
 
@@ -373,7 +376,7 @@ def test_workload_fp4_decode():
             row = b * inp.n_q + t
             es = score_error_scale(inp, b, t)
             check_scores(sc[row, :len(r["scores"])], r["scores"], es)
-            check_selection(idx[row], r["idx"], r["scores"], inp.topk, es)
+            check_selection(idx[row], r["idx"], r["scores"], inp.topk, selection_errscale(inp, es))
             o2, l2 = O.sparse_mla(inp, b, t, idx[row])
             check_attention(out[row][None], lse[row][None], o2[None], l2[None])
 
@@ -430,7 +433,7 @@ def test_workload_decode(name):
         r = O.decode(inp, requests=[b])[(b, 0)]
         es = score_error_scale(inp, b, 0)
         check_scores(sc[b, :len(r["scores"])], r["scores"], es)
-        nd = check_selection(idx[b], r["idx"], r["scores"], inp.topk, es)
+        nd = check_selection(idx[b], r["idx"], r["scores"], inp.topk, selection_errscale(inp, es))
         # top-k alone on the oracle's own scores is bit-exact
         ti, _ = d.topk(np.pad(r["scores"], (0, d.cap - len(r["scores"])))[None].repeat(inp.batch, 0))
         assert np.array_equal(ti.cpu().numpy()[b], r["idx"])

@@ -12,6 +12,7 @@ from oracle import dsa as O
 from oracle import prefill as P
 
 from dsa_testlib import (Dev, bf16_to_np, check_attention, check_scores, check_selection, rows_error_scale,
+                         selection_errscale,
                          rows_scores_oracle)
 
 pytestmark = pytest.mark.gpu
@@ -75,7 +76,7 @@ def test_prefill_decode_end_to_end():
     for (b, t), r in res.items():
         row = b * inp.n_q + t
         check_scores(sc[row, :len(r["scores"])], r["scores"], es[row])
-        check_selection(idx[row], r["idx"], r["scores"], inp.topk, es[row])
+        check_selection(idx[row], r["idx"], r["scores"], inp.topk, selection_errscale(inp, es[row]))
     outs, lses = [], []
     for row in range(d.rows):
         o, l = O.sparse_mla(inp, row // inp.n_q, row % inp.n_q, idx[row])
