@@ -22,9 +22,9 @@ DSA_EMIT_PHYS_ROWS = 0x1
 DSA_Q_PREPARED = 0x2
 DSA_DEVERR_BLOCK_TABLE, DSA_DEVERR_CTX, DSA_DEVERR_TOPK_INDEX = 0x1, 0x2, 0x4
 
-# Kernels one dsa_decode launches (q quantisation, indexer, 3 top-k passes:
-# sample / filter / select, sparse MLA, split combine); kept in step with csrc/.
-KERNELS_PER_DECODE = 7
+# Kernels one dsa_decode launches (q quantisation, indexer, top-k, sparse MLA,
+# split combine); kept in step with csrc/.
+KERNELS_PER_DECODE = 5
 
 EXPORTS = (
     "dsa_workspace_size",

@@ -123,7 +123,7 @@ dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t s
   WsLayout L;
   if ((s = check_ws(params, ws, ws_bytes, &L)) != DSA_OK) return s;
   return cuda_status(launch_topk(*params, L, static_cast<char*>(ws), scores, score_stride, ctx_lens,
-                                 block_table, topk_idx, phys_rows, stream));
+                                 block_table, topk_idx, phys_rows, stream, false));
 }
 
 dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend_dims_t* dims, const void* c_q,
@@ -204,7 +204,7 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
                                                    : launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
   if (e == cudaSuccess) e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, L.cap, stream);
   if (e == cudaSuccess)
-    e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream);
+    e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream, true);
   if (e == cudaSuccess)
     e = launch_sparse_mla(*params, L, w8, q, lat_pool, block_table, ctx_lens, topk_idx_out, out, lse,
                           stream);

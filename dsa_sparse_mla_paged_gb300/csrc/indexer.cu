@@ -111,6 +111,8 @@ struct IdxTc {
   const float* wq;
   const uint8_t* key_pool;
   float* scores;
+  uint32_t* gmax;  // [rows][gstride] order key of the largest score of each 32 tokens (for the top-k bound)
+  int gstride;
   int64_t score_stride;
   int64_t key_page_stride;
   int units, n_q, max_pages, num_pages, stages, nacc, group, ncol, tmem_cols;  // n_q: rows per unit
@@ -225,13 +227,16 @@ __device__ __forceinline__ void epi_skip(const IdxTc& a, TileWalk& w, EpiState& 
   }
 }
 
-__device__ __forceinline__ void epi_store(const IdxTc& a, float sum, int rowt, TileWalk& w, EpiState& e,
+__device__ __forceinline__ void epi_store(const IdxTc& a, float sum, int rowt, int lane, TileWalk& w, EpiState& e,
                                           const UnitInfo& ui) {
   const int tok = w.j * kTileTok + rowt;
   const int Lt = ui.ctx - ui.valid + e.t + 1;
   // a short last group computes padding rows past `valid`: never stored
-  if (e.t < ui.valid && tok < Lt && tok < a.score_stride)
-    a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
+  const bool keep = e.t < ui.valid && tok < Lt && tok < a.score_stride;
+  if (keep) a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
+  // the warp's 32 tokens are one group: the key of their largest stored score
+  const uint32_t m = __reduce_max_sync(0xffffffffu, keep ? score_order_key(sum) : 0u);
+  if (lane == 0 && m != 0u) a.gmax[(size_t(ui.row0) + e.t) * a.gstride + (tok >> 5)] = m;
   epi_skip(a, w, e);
 }
 
@@ -292,7 +297,7 @@ __device__ __forceinline__ void epi_block_wide(const IdxTc& a, const float (&v)[
   }
   const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
   const float sum = (a01.x + a01.y) + (a23.x + a23.y);
-  epi_store(a, sum, rowt, w, e, ui);
+  epi_store(a, sum, rowt, lane, w, e, ui);
 }
 
 // Reduce one 32-column accumulator block (tile e.g, query row e.t) of this
@@ -335,7 +340,7 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
       part[h & 3] = fmaf(__shfl_sync(0xffffffffu, wt, h), fmaxf(scale * v[h], 0.f), part[h & 3]);
   }
   const float sum = (part[0] + part[1]) + (part[2] + part[3]);
-  epi_store(a, sum, rowt, w, e, ui);
+  epi_store(a, sum, rowt, lane, w, e, ui);
 }
 
 
@@ -755,6 +760,8 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   a.wq = wq;
   a.key_pool = static_cast<const uint8_t*>(key_pool);
   a.scores = scores;
+  a.gmax = reinterpret_cast<uint32_t*>(ws + L.gmax);
+  a.gstride = L.gstride;
   a.score_stride = score_stride;
   a.key_page_stride = p.key_page_stride;
   a.units = p.batch * map.groups;

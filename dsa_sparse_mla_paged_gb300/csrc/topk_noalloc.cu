@@ -6,8 +6,9 @@
 // into the allocator (cudaMalloc can synchronise the device), or a C caller
 // that is handed only input and output pointers. For them this entry point
 // keeps the top-k scratch (per-row selection state, per-chunk candidate
-// offsets, the candidate buffer) in one file-scope device array that every GPU loading
-// the library holds until the process exits.
+// offsets, the candidate buffer, the rows' 32-token score maxima) in one
+// file-scope device array that every GPU loading the library holds until the
+// process exits.
 #include <mutex>
 
 #include "dsa_internal.cuh"
@@ -22,9 +23,11 @@ constexpr size_t kNoAllocBytes =
     256 +                                                                        // error word
     size_t(kNoAllocMaxRows) * kRowState * 4 +                                    // row state
     size_t(kNoAllocMaxRows) * kNoAllocMaxChunks * 2 * 4 +                        // chunk (offset, count)
-    size_t(kNoAllocMaxRows) * kCandCap * 8;                                      // candidates
+    size_t(kNoAllocMaxRows) * kCandCap * 8 +                                     // candidates
+    size_t(kNoAllocMaxRows) * (kNoAllocMaxCtx / 32) * 4 +                        // 32-token maxima
+    4 * 256;                                                                     // region alignment
 
-// The scratch itself (about 4.3 MB). Only host code below takes its address.
+// The scratch itself (about 13.1 MB). Only host code below takes its address.
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
@@ -49,18 +52,20 @@ cudaError_t scratch_address(void** out) {
 }
 
 // The top-k regions of a workspace, packed into the static array. Every call
-// rewrites the per-row state before anything reads it, so nothing needs clearing.
+// clears the per-row state in its first kernel, so nothing needs clearing here.
 WsLayout noalloc_layout(const dsa_params_t& p) {
   WsLayout L{};
   L.rows = p.batch * p.n_q;
   L.cap = p.max_pages_per_req * p.page_size;
   L.max_chunks = (L.cap + kTopkChunk - 1) / kTopkChunk;
   L.splits = 1;
+  L.gstride = ((L.cap >> 5) + 3) & ~3;
   size_t o = 0;
-  L.err = o; o += 256;
-  L.state = o; o += size_t(L.rows) * kRowState * 4;
-  L.chunkinfo = o; o += size_t(L.rows) * L.max_chunks * 2 * 4;
-  L.cand = o; o += size_t(L.rows) * kCandCap * 8;
+  L.err = o; o = align256(o + 256);
+  L.state = o; o = align256(o + size_t(L.rows) * kRowState * 4);
+  L.chunkinfo = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
+  L.cand = o; o = align256(o + size_t(L.rows) * kCandCap * 8);
+  L.gmax = o; o = align256(o + size_t(L.rows) * L.gstride * 4);
   L.total = o;
   return L;
 }
@@ -89,6 +94,6 @@ extern "C" dsa_status_t dsa_topk_noalloc(const dsa_params_t* params, const float
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return DSA_ERR_CUDA;
   const cudaError_t e = launch_topk(*params, L, static_cast<char*>(base), scores, score_stride, ctx_lens,
-                                    block_table, topk_idx, phys_rows, stream);
+                                    block_table, topk_idx, phys_rows, stream, false);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -90,6 +90,42 @@ def test_topk_bit_exact_on_identical_scores(ctx):
             assert np.array_equal(idx[b], ref), (name, b)
 
 
+def _planted_top_ties(L, seed):
+    """N(0,1) scores with 300 copies of one high value straddling the K-th rank
+    and 40 tokens one fp32 ulp either side of it."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal(L).astype(np.float32)
+    v = np.sort(z)[::-1][2048 - 150]
+    pos = rng.choice(L, 380, replace=False)
+    z[pos[:300]] = v
+    z[pos[300:340]] = np.nextafter(v, np.float32(np.inf))
+    z[pos[340:]] = np.nextafter(v, np.float32(-np.inf))
+    return z
+
+
+@pytest.mark.parametrize("k", [2048, 100])
+def test_topk_bit_exact_long_rows(k):
+    """Rows long enough for the group-maxima bound (and one just below it), on
+    score patterns that keep the candidate set small, straddle tau with ties, or
+    overflow the candidate buffer (few levels: the whole-row select)."""
+    ctx = [1 << 20, 262144 + 17, 100003, 73000]
+    B = len(ctx)
+    inp = gen.make_inputs(B, 1, ctx, seed=17, topk=k)
+    d = Dev(inp)
+    L = max(ctx)
+    for name in ("normal", "top_ties", "few_levels", "extremes", "neg_only"):
+        mat = np.zeros((B, L), np.float32)
+        for b in range(B):
+            if name == "top_ties":
+                mat[b, :ctx[b]] = _planted_top_ties(ctx[b], 50 + b)
+            else:
+                mat[b, :ctx[b]] = dict(_score_patterns(ctx[b], 100 * b + len(name)))[name]
+        idx, _ = d.topk(mat)
+        idx = idx.cpu().numpy()
+        for b in range(B):
+            assert np.array_equal(idx[b], O.topk_select(mat[b, :ctx[b]], k)), (name, b)
+
+
 def test_topk_multi_token_rows_and_phys_rows():
     import dsa_sparse_mla_paged_gb300 as dsa
 
@@ -193,6 +229,26 @@ def test_decode_query_rows_and_k(nq, topk, ctx):
         check_selection(idx[row], r["idx"], r["scores"], inp.topk, selection_errscale(inp, es[row]))
     ro, rl = _oracle_mla_all(inp, idx)
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+
+
+@pytest.mark.parametrize("nq,ctx", [(1, [150000, 90000]), (3, [100000])])
+def test_decode_long_rows(nq, ctx):
+    """Rows long enough that the top-k bound comes from the group maxima the
+    scorer's epilogue writes (one and several query rows per request)."""
+    inp = gen.make_inputs(len(ctx), nq, ctx, seed=330 + nq, bt_mode="permuted")
+    d = Dev(inp)
+    out, lse, idx = d.decode()
+    idx = idx.cpu().numpy()
+    res = O.decode(inp)
+    for (b, t), r in res.items():
+        row = b * inp.n_q + t
+        check_selection(idx[row], r["idx"], r["scores"], inp.topk,
+                        selection_errscale(inp, score_error_scale(inp, b, t)))
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+    import dsa_sparse_mla_paged_gb300 as dsa
+
+    assert dsa.get_device_error(d.ws) == 0
 
 
 @pytest.mark.parametrize("kf,lf", [("fp8", "fp8"), ("mxfp4", "nvfp4")])
