@@ -134,3 +134,170 @@ __device__ uint32_t block_kth_key(const uint32_t (&keys)[PER], int k, int* hist,
 }
 
 }  // namespace dsa
+
+namespace dsa {
+
+// The k-th largest (1-based) of the non-zero keys the CTA holds (PER per
+// thread; 1 <= k <= their number), by histogram rounds over a key range.
+// Round one's range is [lo, hi] of the keys warp 0 holds (lo no lower than
+// `floor`, a key known to be at or below every key, or 0): every key is
+// placed by (key - lo) >> shift into one of 2048 bins (keys outside the range
+// go to the end bins), so keys that crowd into a narrow range still spread
+// over many bins and the shared atomics rarely meet. Each further round
+// spans the chosen bin's range. The bin holding the k-th key is found by all
+// warps (two bins per thread, a warp sum each) and then warp 0 (the warp
+// totals, then that warp's bins). LOWER: stop after one round and return the
+// bin's lowest key (at least k keys reach it). Otherwise: stop when the bin is
+// one key wide, or holds at most 32 keys (one warp ranks them), and return
+// the exact k-th largest key. NT = 1024; `hist` holds 4096 ints (two
+// buffers: a round's bins are cleared while the other round's are read), `smw`
+// 64, `list` 32.
+template <int NT, int PER, bool LOWER>
+__device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t floor, int* hist, int* smw,
+                                    uint32_t* list) {
+  static_assert(NT == 1024, "two bins per thread");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ int s_bin, s_rank, s_cnt, s_n;
+  __shared__ uint32_t s_lo, s_hi, s_key;
+  if (warp == 0) {
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (keys[i]) { mn = min(mn, keys[i]); mx = max(mx, keys[i]); }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+      if (mx == 0u) { mn = floor; mx = 0xFFFFFFFFu; }  // warp 0 holds no key: the widest range
+      s_lo = max(mn, floor);
+      s_hi = max(mx, max(mn, floor));
+      s_n = 0;
+      s_key = 0u;
+    }
+  }
+  hist[threadIdx.x] = 0;
+  hist[threadIdx.x + NT] = 0;
+  __syncthreads();
+  uint32_t lo = s_lo, hi = s_hi;
+  int kk = k, buf = 0;
+  bool first = true;
+  while (true) {
+    int* H = hist + buf * 2048;
+    const uint32_t span = hi - lo;  // keys lo .. hi
+    const int sh = span == 0u ? 0 : max(0, 21 - __clz(span));  // (span >> sh) < 2048
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const uint32_t x = keys[i];
+      if (x == 0u) continue;
+      int b;
+      if (first) {  // keys outside [lo, hi] go to the end bins
+        b = x < lo ? 0 : x > hi ? 2047 : int((x - lo) >> sh);
+      } else {
+        if (x < lo || x > hi) continue;
+        b = int((x - lo) >> sh);
+      }
+      atomicAdd(&H[b], 1);
+    }
+    __syncthreads();
+    // thread t: bins 2047-2t and 2046-2t (from the top); warp w: bins 2047-64w ..
+    const int c0 = H[2047 - 2 * threadIdx.x], c1 = H[2046 - 2 * threadIdx.x];
+    int wsum = c0 + c1;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    if (lane == 0) smw[warp] = wsum;
+    __syncthreads();
+    if (warp == 0) {
+      // defaults for fewer than kk keys (not expected: k <= the key count), so that no index leaves the bins
+      if (lane == 0) {
+        s_bin = 0;
+        s_rank = 1;
+        s_cnt = 0;
+      }
+      __syncwarp();
+      const int wt = smw[lane];
+      int incl = wt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl - wt < kk && kk <= incl);
+      const int W = hit ? __ffs(hit) - 1 : 31;
+      const int kr = kk - __shfl_sync(0xffffffffu, incl - wt, W);
+      const int top = 2047 - 64 * W;  // warp W's bins, two per lane from the top
+      const int a0 = H[top - 2 * lane], a1 = H[top - 2 * lane - 1];
+      const int c2 = a0 + a1;
+      int incl2 = c2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl2, o);
+        if (lane >= o) incl2 += y;
+      }
+      const int before = incl2 - c2;
+      if (before < kr && kr <= incl2) {
+        const int j = kr <= before + a0 ? 0 : 1;
+        s_bin = top - 2 * lane - j;
+        s_rank = kr - before - (j ? a0 : 0);
+        s_cnt = j ? a1 : a0;
+      }
+    }
+    hist[(buf ^ 1) * 2048 + threadIdx.x] = 0;  // the next round's bins (last read a round ago)
+    hist[(buf ^ 1) * 2048 + threadIdx.x + NT] = 0;
+    __syncthreads();
+    buf ^= 1;
+    const int b = s_bin;
+    kk = s_rank;
+    const int n = s_cnt;
+    // bin b's keys: [lo + (b << sh), lo + (b << sh) + 2^sh - 1], widened at the ends in round one
+    const uint32_t blo = lo + (uint32_t(b) << sh);
+    uint32_t nlo = blo, nhi = sh >= 32 ? 0xFFFFFFFFu : blo + ((1u << sh) - 1u);
+    if (nhi < blo || nhi > hi) nhi = hi;
+    const bool below = first && b == 0;  // bin 0 of round one also holds every key below lo
+    if (below) nlo = floor;
+    if (first && b == 2047) {  // the top bin of round one also holds every key above hi
+      if (hi != 0xFFFFFFFFu) nlo = min(nlo, hi + 1u);
+      nhi = 0xFFFFFFFFu;
+    }
+    first = false;
+    if (LOWER) return below ? floor : nlo;
+    lo = nlo;
+    hi = nhi;
+    if (lo == hi) return lo;
+    if (n <= 32) break;
+  }
+  // at most 32 keys lie in [lo, hi]: one warp ranks them
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (keys[i] && keys[i] >= lo && keys[i] <= hi) {
+      const int at = atomicAdd(&s_n, 1);
+      if (at < 32) list[at] = keys[i];
+    }
+  __syncthreads();
+  if (warp == 0) {
+    const int n = min(s_n, 32);
+    const uint32_t mine = lane < n ? list[lane] : 0u;
+    int gt = 0, eq = 0;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t x = list[j];
+      gt += x > mine;
+      eq += x == mine;
+    }
+    if (lane < n && gt < kk && kk <= gt + eq) s_key = mine;
+  }
+  __syncthreads();
+  return s_key;
+}
+
+template <int NT, int PER>
+__device__ __forceinline__ uint32_t block_kth_fast(const uint32_t (&keys)[PER], int k, uint32_t floor, int* hist,
+                                                   int* smw, uint32_t* list) {
+  return block_kth_range<NT, PER, false>(keys, k, floor, hist, smw, list);
+}
+
+// A key at or below the k-th largest such that at least k keys reach it.
+template <int NT, int PER>
+__device__ __forceinline__ uint32_t block_kth_lower(const uint32_t (&keys)[PER], int k, int* hist, int* smw,
+                                                    uint32_t* list) {
+  return block_kth_range<NT, PER, true>(keys, k, 0u, hist, smw, list);
+}
+
+}  // namespace dsa

@@ -202,7 +202,8 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
   float* scores = reinterpret_cast<float*>(w8 + L.scores);
   cudaError_t e = (params->flags & DSA_Q_PREPARED) ? cudaSuccess
                                                    : launch_idx_q_quant(*params, L, w8, q_idx, w, ctx_lens, stream);
-  if (e == cudaSuccess) e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, L.cap, stream);
+  if (e == cudaSuccess)
+    e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, L.cap, stream, 1, 0, true);
   if (e == cudaSuccess)
     e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream, true);
   if (e == cudaSuccess)

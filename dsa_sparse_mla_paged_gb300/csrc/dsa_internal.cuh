@@ -23,11 +23,10 @@ constexpr int kLatRowFp8 = kDQK;                         // 576
 constexpr int kMaxNQ = 8;
 constexpr int kMaxTopK = 2048;
 
-// top-k: a row of scores is filtered in at most cap / kTopkChunk pieces (CTA
-// rounds), each with a record of where its candidates went; each row keeps at
-// most kCandCap candidates for its exact selection.
-constexpr int kTopkChunk = 1024;
+// top-k: each row keeps at most kCandCap candidates for its exact selection,
+// filtered by CTAs of at least kTopkChunk tokens each (one record per CTA).
 constexpr int kCandCap = 8192;
+constexpr int kTopkChunk = 1024;
 constexpr int kRowState = 16;     // int32 words of per-row selection state
 
 // sparse attention: the K selected slots of a row are cut into splits of this
@@ -50,9 +49,10 @@ struct WsLayout {
   size_t wq;        // float [rows][32] folded head weights
   size_t tiles;     // int32 [rows] inclusive prefix of 128-token tiles per scorer unit
   size_t state;     // int32 [rows][kRowState]
-  size_t chunkinfo; // int32 [rows][max_chunks][2] (offset, count) of each chunk's candidates
+  size_t chunkinfo; // int32 [rows][max_chunks][2] (offset, count) of each top-k CTA's candidates
   size_t cand;      // uint64 [rows][kCandCap] top-k candidates (key << 32 | token)
   size_t gmax;      // uint32 [rows][gstride] order key of the largest score of each 32 tokens
+  size_t gmax128;   // uint32 [rows][g128stride] the same per 128 tokens (dsa_decode; zero between calls)
   size_t opart;     // float [rows][splits][96][512]
   size_t lpart;     // float [rows][splits][96]
   size_t topk;      // int32 [rows][topk] (dsa_decode without topk_idx_out)
@@ -65,7 +65,7 @@ struct WsLayout {
   size_t dcp_keys16;  // uint16 [rows][W][S] shard-major score keys, W * S <= cap + 8 * kDcpMaxWorld
   size_t scores;    // float [rows][cap]
   size_t total;
-  int rows, cap, max_chunks, splits, gstride;
+  int rows, cap, max_chunks, splits, gstride, g128stride;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -80,6 +80,7 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.max_chunks = (L.cap + kTopkChunk - 1) / kTopkChunk;
   L.splits = attention_splits(p.topk);
   L.gstride = ((L.cap >> 5) + 3) & ~3;
+  L.g128stride = ((L.cap >> 7) + 3) & ~3;
   size_t o = 0;
   L.err = o; o = align256(o + 256);
   L.q8 = o; o = align256(o + size_t(L.rows) * kIdxHeads * kIdxDim);
@@ -89,6 +90,7 @@ inline WsLayout ws_layout(const dsa_params_t& p) {
   L.chunkinfo = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
   L.cand = o; o = align256(o + size_t(L.rows) * kCandCap * 8);
   L.gmax = o; o = align256(o + size_t(L.rows) * L.gstride * 4);
+  L.gmax128 = o; o = align256(o + size_t(L.rows) * L.g128stride * 4);
   L.opart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * kDNope * 4);
   L.lpart = o; o = align256(o + size_t(L.rows) * L.splits * kHeads * 4);
   L.topk = o; o = align256(o + size_t(L.rows) * p.topk * 4);
@@ -239,9 +241,12 @@ __device__ __forceinline__ void build_tile_plan(const int32_t* __restrict__ ctx_
 cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
                                const float* w, const int32_t* ctx_lens, cudaStream_t st, int world = 1,
                                int rank = 0);
+// keep128: also fold each 128 tokens' largest score key into the workspace's
+// 128-token maxima (dsa_decode, whose top-k clears them after use).
 cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
                            const int32_t* block_table, const int32_t* ctx_lens, float* scores,
-                           int64_t score_stride, cudaStream_t st, int world = 1, int rank = 0);
+                           int64_t score_stride, cudaStream_t st, int world = 1, int rank = 0,
+                           bool keep128 = false);
 // have_gmax: the scorer of the same call has just written the group maxima of
 // these scores into the workspace (dsa_decode); otherwise a first kernel
 // computes them from the scores.

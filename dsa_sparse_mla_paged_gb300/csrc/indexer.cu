@@ -111,8 +111,9 @@ struct IdxTc {
   const float* wq;
   const uint8_t* key_pool;
   float* scores;
-  uint32_t* gmax;  // [rows][gstride] order key of the largest score of each 32 tokens (for the top-k bound)
-  int gstride;
+  uint32_t* gmax;     // [rows][gstride] order key of the largest score of each 32 tokens (for the top-k bound)
+  uint32_t* gmax128;  // [rows][g128stride] the same per 128 tokens, by atomic max; null: not kept
+  int gstride, g128stride;
   int64_t score_stride;
   int64_t key_page_stride;
   int units, n_q, max_pages, num_pages, stages, nacc, group, ncol, tmem_cols;  // n_q: rows per unit
@@ -236,7 +237,10 @@ __device__ __forceinline__ void epi_store(const IdxTc& a, float sum, int rowt, i
   if (keep) a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
   // the warp's 32 tokens are one group: the key of their largest stored score
   const uint32_t m = __reduce_max_sync(0xffffffffu, keep ? score_order_key(sum) : 0u);
-  if (lane == 0 && m != 0u) a.gmax[(size_t(ui.row0) + e.t) * a.gstride + (tok >> 5)] = m;
+  if (lane == 0 && m != 0u) {
+    a.gmax[(size_t(ui.row0) + e.t) * a.gstride + (tok >> 5)] = m;
+    if (a.gmax128) atomicMax(a.gmax128 + (size_t(ui.row0) + e.t) * a.g128stride + (tok >> 7), m);
+  }
   epi_skip(a, w, e);
 }
 
@@ -732,7 +736,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int
 
 cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
                            const int32_t* block_table, const int32_t* ctx_lens, float* scores,
-                           int64_t score_stride, cudaStream_t st, int world, int rank) {
+                           int64_t score_stride, cudaStream_t st, int world, int rank, bool keep128) {
   const UnitMap map = unit_map(p.n_q, world, rank);
   const int gsz = map.gsz;
   const uint8_t* q8 = reinterpret_cast<const uint8_t*>(ws + L.q8);
@@ -761,7 +765,9 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   a.key_pool = static_cast<const uint8_t*>(key_pool);
   a.scores = scores;
   a.gmax = reinterpret_cast<uint32_t*>(ws + L.gmax);
+  a.gmax128 = keep128 ? reinterpret_cast<uint32_t*>(ws + L.gmax128) : nullptr;
   a.gstride = L.gstride;
+  a.g128stride = L.g128stride;
   a.score_stride = score_stride;
   a.key_page_stride = p.key_page_stride;
   a.units = p.batch * map.groups;

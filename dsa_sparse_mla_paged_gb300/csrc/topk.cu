@@ -7,29 +7,33 @@
 //
 // Scores are compared through an order-preserving 32-bit key (larger score ->
 // larger key; -0 and +0 share one key). One kernel, C CTAs per row:
-//   bound   every CTA of a row finds the same threshold key g:
-//           - from the group maxima (the largest key of each 32 consecutive
-//             tokens, written by the scorer's epilogue as it stores the scores,
-//             or by topk_gmax_kernel for scores handed in by the caller): with
-//             groups merged to at most 8,192, g = the K-th largest group
-//             maximum. K groups each hold a token at or above g, so at least K
-//             tokens reach g and the K-th largest score tau is >= g: a bound,
-//             not a guess;
-//           - for rows too short for that bound to be tight, g is a guess (the
-//             r-th largest of an evenly spaced sample, r set for ~2K tokens);
-//   filter  each CTA compacts the tokens of its chunk with key >= g, in index
-//           order, into the row's candidate buffer (one atomic reservation per
-//           CTA, its place recorded per chunk);
-//   select  the CTA that arrives last at the row's counter gathers the
-//           candidates chunk by chunk (in index order again), radix-selects the
-//           exact K-th largest key tau among them and writes the winners in
-//           order, ties at tau lowest index first.
+//   bound   every CTA of a row finds the same threshold key g from the group
+//           maxima (the key of the largest score of each 128 and each 32
+//           consecutive tokens, kept by the scorer's epilogue as it stores
+//           the scores, or by topk_gmax_kernel for scores handed in by the
+//           caller): with groups merged to at most 8,192, g = the lowest key of
+//           the histogram bin that holds the K-th largest group maximum. K
+//           groups each hold a token at or above g, so at least K tokens reach
+//           g and the K-th largest score tau is >= g. Rows too short for that
+//           bound to be tight take a guess instead (from an evenly spaced
+//           sample, aimed at ~2K tokens);
+//   filter  each CTA stages its chunk of scores in shared memory (one bulk
+//           copy, in flight while the bound is found) and compacts the tokens
+//           with key >= g, in index order, into the row's candidate buffer
+//           (one atomic reservation per CTA, recorded per chunk);
+//   select  the CTA that arrives last at the row's counter reads the
+//           candidates, finds the exact K-th largest key tau among them
+//           (histogram rounds, then the few keys of tau's bin ranked by a
+//           warp) and writes the winners in index order, ties at tau lowest
+//           index first: a winner's place is the winners of the chunks before
+//           its own plus those before it in its own chunk (whose candidates are
+//           contiguous and ordered), so the CTAs' arrival order never matters.
 // Whenever at least K tokens reach g and the buffer holds them all, the
 // candidates contain every token with key >= tau, so the selection is exact.
-// Otherwise (a guess that was too high, or more candidates than the buffer
-// holds, e.g. a row of equal scores) the last CTA runs an exact radix select
-// over the whole row by itself. No CTA waits on another: the last one to
-// arrive continues, and the result does not depend on the order of arrival.
+// Otherwise (a bound or guess that was too high, or more candidates than the
+// buffer holds, e.g. a row of equal scores) the last CTA runs an exact radix
+// select over the whole row by itself. So the maxima steer only the speed,
+// never the result. No CTA waits on another: the last one to arrive continues.
 #include <algorithm>
 
 #include "block_select.cuh"
@@ -41,10 +45,11 @@ namespace dsa {
 namespace {
 
 constexpr int kTkThreads = 1024;
+constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kBoundPer = 8;                        // bound keys per thread
 constexpr int kBoundKeys = kTkThreads * kBoundPer;  // 8,192 group maxima or samples at most
 constexpr int kCandPer = kCandCap / kTkThreads;     // candidates per thread in the select
-constexpr int kRoundTok = 32 * 1024;                // tokens a CTA filters at most (1,024 per warp)
+constexpr int kRoundTok = kTkWarps * 1024;          // tokens a CTA filters at most (1,024 per warp)
 constexpr int kGmaxThreads = 256;
 
 // row state words
@@ -57,12 +62,13 @@ struct TopkArgs {
   int64_t stride;
   const int32_t* ctx_lens;
   const int32_t* block_table;
-  const uint32_t* gmax;  // [rows][gstride] key of the largest score of each 32 tokens
-  int gstride;
+  uint32_t* gmax;     // [rows][gstride] key of the largest score of each 32 tokens
+  uint32_t* gmax128;  // [rows][g128stride] the same per 128 tokens (cleared after use)
+  int gstride, g128stride;
   int n_q, cap, K, max_pages, num_pages, max_chunks;
   int chunk;       // tokens per CTA: a multiple of 1,024, at most kRoundTok
   int* state;      // [rows][kRowState]
-  int* chunkinfo;  // [rows][max_chunks][2]: (offset, count) in the candidate buffer, per CTA
+  int* chunkinfo;  // [rows][max_chunks][2]: (offset, count) of each CTA's candidates
   uint64_t* cand;  // [rows][kCandCap]: key << 32 | token
   int* err;
   int32_t* topk_idx;
@@ -98,17 +104,33 @@ __device__ __forceinline__ int phys_row(const TopkArgs& a, int b, int s) {
 // How a row's threshold is found (the same answer in every CTA of the row).
 enum BoundKind { kAll = 0, kMaxima = 1, kSample = 2 };
 
-// Group maxima are merged 2^sh at a time so that at most kBoundKeys remain.
-// The bound is tight once there are several times K groups; below ~1.1 K it
-// would let most of the row through, and a sample serves better.
-__device__ __forceinline__ BoundKind bound_kind(int L, int K, int* sh) {
-  if (L <= kCandCap) return kAll;
-  const int n32 = (L + 31) >> 5;
-  if (int64_t(n32) * 8 < int64_t(K) * 9) return kSample;
-  int s = 0;
-  while (((n32 + (1 << s) - 1) >> s) > kBoundKeys) ++s;
-  *sh = s;
-  return kMaxima;
+struct Bound {
+  BoundKind kind;
+  int gshift;  // 7: the 128-token maxima, 5: the 32-token ones
+  int sh;      // 2^sh of them merged per group
+};
+
+// The coarser maxima when there are enough of them for a tight bound (several
+// times K groups; below ~1.1 K most of the row would pass), else the finer;
+// rows too short for either take a sample.
+__device__ __forceinline__ Bound bound_of(int L, int K) {
+  Bound bd{kAll, 0, 0};
+  if (L <= kCandCap) return bd;
+  const int n128 = (L + 127) >> 7, n32 = (L + 31) >> 5;
+  int n;
+  if (int64_t(n128) * 8 >= int64_t(K) * 9) {
+    bd.gshift = 7;
+    n = n128;
+  } else if (int64_t(n32) * 8 >= int64_t(K) * 9) {
+    bd.gshift = 5;
+    n = n32;
+  } else {
+    bd.kind = kSample;
+    return bd;
+  }
+  while (((n + (1 << bd.sh) - 1) >> bd.sh) > kBoundKeys) ++bd.sh;
+  bd.kind = kMaxima;
+  return bd;
 }
 
 // Visit every token s < L of `row` with its key, f(s, key): thread t takes
@@ -243,21 +265,22 @@ __device__ void select_whole_row(const TopkArgs& a, const Row& w, int* hist, int
 }
 
 // ---------------------------------------------------------------- group maxima
-// For scores handed in by the caller: the key of the largest score of each 32
-// consecutive tokens of every row that the bound will use, and the row's
-// selection state cleared. A warp reads 1,024-token blocks (lane l: float4s
-// 4 l + 128 i, eight in flight); each group of 32 is eight lanes' float4s.
-__global__ void __launch_bounds__(kGmaxThreads) topk_gmax_kernel(TopkArgs a, uint32_t* gmax) {
+// For scores handed in by the caller: the keys of the largest score of each
+// 32 and each 128 consecutive tokens of every row that the bound will use, and
+// the row's selection state cleared. A warp reads 1,024-token blocks (lane l:
+// float4s 4 l + 128 i, eight in flight); a group of 32 is eight lanes'
+// float4s, a group of 128 the warp's i-th load.
+__global__ void __launch_bounds__(kGmaxThreads) topk_gmax_kernel(TopkArgs a) {
   pdl_wait();
   const Row w = row_of(a, blockIdx.y);
   int* st = a.state + size_t(w.r) * kRowState;
   if (blockIdx.x == 0 && threadIdx.x < 3) st[kStCursor + threadIdx.x] = 0;
-  int sh = 0;
-  if (w.L <= a.K || bound_kind(w.L, a.K, &sh) != kMaxima) return;
+  if (w.L <= a.K || bound_of(w.L, a.K).kind != kMaxima) return;
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * (kGmaxThreads / 32);
   const float* row = a.scores + size_t(w.r) * a.stride;
-  uint32_t* gm = gmax + size_t(w.r) * a.gstride;
+  uint32_t* gm = a.gmax + size_t(w.r) * a.gstride;
+  uint32_t* gm128 = a.gmax128 + size_t(w.r) * a.g128stride;
   for (int blk = blockIdx.x * (kGmaxThreads / 32) + (threadIdx.x >> 5); blk * 1024 < w.L; blk += nw) {
     float4 v[8];
 #pragma unroll
@@ -278,23 +301,39 @@ __global__ void __launch_bounds__(kGmaxThreads) topk_gmax_kernel(TopkArgs a, uin
       m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
       m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
       if ((lane & 7) == 0 && s < w.L) gm[s >> 5] = m;
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      if (lane == 0 && s < w.L) gm128[s >> 7] = m;
     }
   }
 }
 
 // ---------------------------------------------------------------- the selection
+// Dynamic shared memory: the CTA's chunk of scores (staged by one bulk copy
+// while the bound is computed), later reused by the last CTA for the winner
+// counts of the ordered write.
 __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
-  __shared__ int hist[4096];
+  __shared__ int hw[4096];  // histograms of the selections
   __shared__ int smw[64];
+  __shared__ uint32_t s_list[32];
   __shared__ int s_base, s_last, s_run;
-  __shared__ int s_wt[32];
-  extern __shared__ int rec_smem[];  // the last CTA: [nrec + 1] prefix of counts, [nrec] offsets
-  pdl_wait();
+  __shared__ int s_wt[kTkWarps];  // per warp: candidates, then their offset
+  __shared__ __align__(8) uint64_t s_bar;
+  extern __shared__ __align__(16) float stage[];
   const int tid = threadIdx.x;
+  if (tid == 0) {
+    ptx::mbar_init(&s_bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  // the attention's CTAs may take the SMs this grid leaves (they wait for its completion)
+  pdl_trigger();
   const Row w = row_of(a, blockIdx.y);
   const int c = blockIdx.x, C = gridDim.x;
   int32_t* out = a.topk_idx + size_t(w.r) * a.K;
   int32_t* phys = a.phys_rows ? a.phys_rows + size_t(w.r) * a.K : nullptr;
+  uint32_t* gm128 = a.gmax128 + size_t(w.r) * a.g128stride;
   if (w.L <= a.K) {
     // every visible token is kept (an invalid row keeps none)
     if (c != 0) return;
@@ -304,56 +343,49 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
       out[i] = keep ? i : -1;
       if (phys) phys[i] = keep ? phys_row(a, w.b, i) : -1;
     }
+    for (int i = tid; i < (w.L + 127) >> 7; i += kTkThreads) gm128[i] = 0u;  // for the scorer's next maxima
     return;
   }
   const float* row = a.scores + size_t(w.r) * a.stride;
   int* st = a.state + size_t(w.r) * kRowState;
+  // CTA c filters tokens [rb, re); its scores go to shared memory by one bulk
+  // copy (rounded up to 16 B: still inside the row, whose stride is a multiple of 4)
+  const int rb = c * a.chunk;
+  const int re = min(w.L, rb + a.chunk);
+  const uint32_t nbytes = re > rb ? uint32_t((re - rb) * 4 + 15) & ~15u : 0u;
+  if (tid == 0 && nbytes) {
+    ptx::mbar_arrive_expect_tx(&s_bar, nbytes);
+    for (uint32_t o = 0; o < nbytes; o += 32768)
+      ptx::bulk_load(reinterpret_cast<uint8_t*>(stage) + o, reinterpret_cast<const uint8_t*>(row + rb) + o,
+                     min(32768u, nbytes - o), &s_bar);
+  }
 
   // ---------------------------------------------------------------- bound
-  int sh = 0;
-  const BoundKind kind = bound_kind(w.L, a.K, &sh);
+  const Bound bd = bound_of(w.L, a.K);
   uint32_t g = 0u;
-  if (kind == kMaxima) {
-    // group i: 32-token maxima [i << sh, (i + 1) << sh) merged
-    const int n32 = (w.L + 31) >> 5;
-    const int ng = (n32 + (1 << sh) - 1) >> sh;
-    const uint32_t* gm = a.gmax + size_t(w.r) * a.gstride;
+  if (bd.kind == kMaxima) {
+    // group i: maxima [i << sh, (i + 1) << sh) of the chosen size, merged
+    const int n = (w.L + (1 << bd.gshift) - 1) >> bd.gshift;
+    const int ng = (n + (1 << bd.sh) - 1) >> bd.sh;
+    const uint32_t* gm = bd.gshift == 7 ? gm128 : a.gmax + size_t(w.r) * a.gstride;
     uint32_t mk[kBoundPer];
-    if (sh >= 2) {
 #pragma unroll
-      for (int u = 0; u < kBoundPer; ++u) mk[u] = 0u;
-      // uint4 words; a group's words are [i << sh, min(n32, (i + 1) << sh))
-      const int nq = 1 << (sh - 2);
-      for (int q = 0; q < nq; ++q) {
-        uint4 v[kBoundPer];
-#pragma unroll
-        for (int u = 0; u < kBoundPer; ++u) {
-          const int gi = u * kTkThreads + tid;
-          const int j = (gi << sh) + 4 * q;
-          v[u] = (gi < ng && j < n32) ? __ldcg(reinterpret_cast<const uint4*>(gm + j)) : make_uint4(0, 0, 0, 0);
-          if (gi < ng && j < n32 && j + 4 > n32) {  // the row's last words: only those below n32
-            if (j + 1 >= n32) v[u].y = 0u;
-            if (j + 2 >= n32) v[u].z = 0u;
-            v[u].w = 0u;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kBoundPer; ++u) mk[u] = max(mk[u], max(max(v[u].x, v[u].y), max(v[u].z, v[u].w)));
-      }
-    } else {
+    for (int u = 0; u < kBoundPer; ++u) {
+      const int gi = u * kTkThreads + tid;
+      mk[u] = (bd.sh == 0 && gi < ng) ? __ldcg(gm + gi) : 0u;
+    }
+    if (bd.sh > 0) {
 #pragma unroll
       for (int u = 0; u < kBoundPer; ++u) {
         const int gi = u * kTkThreads + tid;
-        uint32_t m = 0u;
         if (gi < ng) {
-          const int j0 = gi << sh, j1 = min(n32, j0 + (1 << sh));
-          for (int j = j0; j < j1; ++j) m = max(m, __ldcg(gm + j));
+          const int j0 = gi << bd.sh, j1 = min(n, j0 + (1 << bd.sh));
+          for (int j = j0; j < j1; ++j) mk[u] = max(mk[u], __ldcg(gm + j));
         }
-        mk[u] = m;
       }
     }
-    g = block_kth_key<kTkThreads, kBoundPer>(mk, a.K, hist, smw);
-  } else if (kind == kSample) {
+    g = block_kth_lower<kTkThreads, kBoundPer>(mk, a.K, hw, smw, s_list);
+  } else if (bd.kind == kSample) {
     // sample i at position floor(i * L / ns); the r-th largest, r for ~2K tokens
     const int ns = min(w.L, kBoundKeys);
     uint32_t sk[kBoundPer];
@@ -363,46 +395,46 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
       sk[u] = i < ns ? order_key(__ldcg(row + int(int64_t(i) * w.L / ns))) : 0u;
     }
     const int r = int(min(int64_t(ns), (int64_t(2) * a.K * ns + w.L - 1) / w.L));
-    g = block_kth_key<kTkThreads, kBoundPer>(sk, r, hist, smw);
+    g = block_kth_lower<kTkThreads, kBoundPer>(sk, r, hw, smw, s_list);
+  }
+  if (nbytes && !ptx::mbar_wait(&s_bar, 0)) {
+    if (tid == 0) atomicOr(a.err, DSA_DEVERR_TIMEOUT);
+    ptx::mbar_wait(&s_bar, 0);  // the copy still owns the buffer: one more bounded wait
   }
 
   // ---------------------------------------------------------------- filter
-  // CTA c: tokens [c * chunk, (c + 1) * chunk); warp w reads [base + 1024 w,
-  // + 1024), lane l the float4s l + 32 i (i < 8): coalesced, and (warp, i, lane,
-  // element) is index order. The CTA reserves its place with one atomic and
-  // records it at index c.
+  // Warp w reads the block [rb + 1024 w, + 1024) from shared memory, lane l
+  // its float4s l + 32 j (j < 8): (warp, j, lane, element) is index order.
+  // One atomic reserves the CTA's place in the row's candidate buffer.
   const int lane = tid & 31, warp = tid >> 5;
   const unsigned lt = (1u << lane) - 1u;
-  {
-    const int rb = c * a.chunk;
-    const int re = min(w.L, rb + a.chunk);
-    const int wb = rb + warp * 1024;
-    float4 v[8];
+  const int wb = rb + warp * 1024;
+  uint32_t pass = 0u;  // bit 4 j + e: token wb + 4 (lane + 32 j) + e is a candidate
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int s = wb + 4 * (lane + 32 * i);
-      // a float4 that starts below re lies inside the row's stride (a multiple of 4)
-      v[i] = s < re ? __ldcg(reinterpret_cast<const float4*>(row + s)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < 8; ++j) {
+    const int s = wb + 4 * (lane + 32 * j);
+    if (s < re) {
+      const float4 v = *reinterpret_cast<const float4*>(stage + (s - rb));
+      pass |= uint32_t(order_key(v.x) >= g) << (4 * j);
+      pass |= uint32_t(s + 1 < re && order_key(v.y) >= g) << (4 * j + 1);
+      pass |= uint32_t(s + 2 < re && order_key(v.z) >= g) << (4 * j + 2);
+      pass |= uint32_t(s + 3 < re && order_key(v.w) >= g) << (4 * j + 3);
     }
-    uint32_t pass = 0;  // bit 4i + j: token wb + 4 (lane + 32 i) + j is a candidate
+  }
+  const int wcnt = __reduce_add_sync(0xffffffffu, __popc(pass));
+  if (lane == 0) s_wt[warp] = wcnt;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = s_wt[lane];
+    int incl = x;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int s = wb + 4 * (lane + 32 * i);
-      pass |= uint32_t(s < re && order_key(v[i].x) >= g) << (4 * i);
-      pass |= uint32_t(s + 1 < re && order_key(v[i].y) >= g) << (4 * i + 1);
-      pass |= uint32_t(s + 2 < re && order_key(v[i].z) >= g) << (4 * i + 2);
-      pass |= uint32_t(s + 3 < re && order_key(v[i].w) >= g) << (4 * i + 3);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
-    const int wtot = __reduce_add_sync(0xffffffffu, __popc(pass));
-    if (lane == 0) s_wt[warp] = wtot;
-    __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int i = 0; i < 32; ++i) {
-        const int x = s_wt[i];
-        s_wt[i] = run;
-        run += x;
-      }
+    s_wt[lane] = incl - x;
+    const int run = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
       int base = 0;
       if (run > 0) {
         base = atomicAdd(st + kStCursor, run);
@@ -412,28 +444,32 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
       s_run = run;
       *reinterpret_cast<int2*>(a.chunkinfo + (size_t(w.r) * a.max_chunks + c) * 2) = make_int2(base, run);
     }
-    __syncthreads();
-    if (wtot > 0 && s_base + s_run <= kCandCap) {
-      uint64_t* o = a.cand + size_t(w.r) * kCandCap + s_base + s_wt[warp];
+  }
+  __syncthreads();
+  if (wcnt > 0 && s_base + s_run <= kCandCap) {
+    uint64_t* o = a.cand + size_t(w.r) * kCandCap + s_base + s_wt[warp];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        // this float4's candidates (0..4 per lane) placed by three bit-plane ballots
-        const uint32_t ci = (pass >> (4 * i)) & 15u;
-        const int n = __popc(ci);
-        const unsigned b0 = __ballot_sync(0xffffffffu, n & 1), b1 = __ballot_sync(0xffffffffu, n & 2),
-                       b2 = __ballot_sync(0xffffffffu, n & 4);
-        const int ti = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
-        if (ti == 0) continue;
-        int p = __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
-        const int s = wb + 4 * (lane + 32 * i);
-        const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    for (int j = 0; j < 8; ++j) {
+      // this float4's candidates (0..4 per lane) placed by three bit-plane ballots
+      const uint32_t ci = (pass >> (4 * j)) & 15u;
+      const int nn = __popc(ci);
+      const unsigned b0 = __ballot_sync(0xffffffffu, nn & 1), b1 = __ballot_sync(0xffffffffu, nn & 2),
+                     b2 = __ballot_sync(0xffffffffu, nn & 4);
+      const int ti = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+      if (ti == 0) continue;
+      int p = __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+      const int s = wb + 4 * (lane + 32 * j);
+      if (ci) {
+        const float4 v = *reinterpret_cast<const float4*>(stage + (s - rb));
+        const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if ((ci >> j) & 1u) o[p++] = (uint64_t(order_key(vv[j])) << 32) | uint32_t(s + j);
-        o += ti;
+        for (int e = 0; e < 4; ++e)
+          if ((ci >> e) & 1u) o[p++] = (uint64_t(order_key(vv[e])) << 32) | uint32_t(s + e);
       }
+      o += ti;
     }
   }
+
   // the last CTA of the row to get here selects
   __syncthreads();
   if (tid == 0) {
@@ -446,86 +482,98 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
   const int total = __ldcg(st + kStCursor);
   const int ovf = __ldcg(st + kStOverflow);
   if (ovf != 0 || total < a.K) {
-    select_whole_row(a, w, hist, smw, out, phys);
+    select_whole_row(a, w, hw, smw, out, phys);
   } else {
-    // chunk records -> exclusive prefix of counts (record order = index order)
-    const int nrec = C;
-    int* s_pre = rec_smem;
-    int* s_off = rec_smem + nrec + 1;
-    int carry = 0;
-    for (int r0 = 0; r0 < nrec; r0 += kTkThreads) {
-      const int ri = r0 + tid;
-      const int2 rec = ri < nrec
-                           ? __ldcg(reinterpret_cast<const int2*>(a.chunkinfo + (size_t(w.r) * a.max_chunks + ri) * 2))
-                           : make_int2(0, 0);
-      int tot;
-      const int cp = block_excl_scan<kTkThreads>(rec.y, &tot, smw) + carry;
-      if (ri < nrec) {
-        s_pre[ri] = cp;
-        s_off[ri] = rec.x;
-      }
-      carry += tot;
-    }
-    if (tid == 0) s_pre[nrec] = carry;
-    __syncthreads();
-    // thread t: candidates t * 8 .. t * 8 + 7 of the ordered list
+    // candidates in reservation order: each CTA's are contiguous and in index
+    // order, the CTAs in any order. tau and the winners need no order; a
+    // winner's output place is (winners of the chunks before its own) +
+    // (winners of its chunk before it), its chunk being token / chunk. The
+    // chunk records load with the candidates.
     const uint64_t* cand = a.cand + size_t(w.r) * kCandCap;
-    const int p0 = tid * kCandPer;
-    int ch = 0;
-    if (p0 < total) {
-      int lo = 0, hi = nrec - 1;  // last record with s_pre <= p0
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_pre[mid] <= p0) lo = mid; else hi = mid - 1;
-      }
-      ch = lo;
-    }
-    int src[kCandPer];
-#pragma unroll
-    for (int u = 0; u < kCandPer; ++u) {
-      const int p = p0 + u;
-      src[u] = -1;
-      if (p < total) {
-        while (s_pre[ch + 1] <= p) ++ch;
-        src[u] = s_off[ch] + (p - s_pre[ch]);
-      }
-    }
     uint64_t cv[kCandPer];
 #pragma unroll
-    for (int u = 0; u < kCandPer; ++u) cv[u] = src[u] >= 0 ? __ldcg(cand + src[u]) : 0ull;
+    for (int u = 0; u < kCandPer; ++u) {
+      const int p = tid * kCandPer + u;
+      cv[u] = p < total ? __ldcg(cand + p) : 0ull;
+    }
+    const int* recs = a.chunkinfo + size_t(w.r) * a.max_chunks * 2;
+    int2 rec = tid < C ? __ldcg(reinterpret_cast<const int2*>(recs) + tid) : make_int2(0, 0);
     uint32_t mk[kCandPer];
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) mk[u] = uint32_t(cv[u] >> 32);
-    const uint32_t tau = block_kth_key<kTkThreads, kCandPer>(mk, a.K, hist, smw);
-    // one scan of (keys > tau, keys == tau) packed 16 | 16 bits: the tokens
-    // selected before this thread are those above tau plus the first `need`
-    // ties in index order
-    int gt = 0, ne = 0;
+    const uint32_t tau = block_kth_fast<kTkThreads, kCandPer>(mk, a.K, g, hw, smw, s_list);
+    int gt = 0, eq = 0;
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) {
-      gt += src[u] >= 0 && mk[u] > tau;
-      ne += src[u] >= 0 && mk[u] == tau;
+      gt += mk[u] > tau;
+      eq += mk[u] == tau;  // an empty slot has key 0 < tau
     }
     int t2;
-    const int pk = block_excl_scan<kTkThreads>((gt << 16) | ne, &t2, smw);
+    block_excl_scan<kTkThreads>((gt << 16) | eq, &t2, smw);
     const int need = a.K - (t2 >> 16);
-    int e = pk & 0xFFFF;
-    int p = (pk >> 16) + min(e, need);
+    // ties at tau: the `need` lowest tokens (the need-th largest of ~token)
+    uint32_t tie_max = 0xFFFFFFFFu;
+    if ((t2 & 0xFFFF) > need) {
+      uint32_t tk[kCandPer];
+#pragma unroll
+      for (int u = 0; u < kCandPer; ++u) tk[u] = mk[u] == tau ? 0xFFFFFFFFu - uint32_t(cv[u]) : 0u;
+      tie_max = 0xFFFFFFFFu - block_kth_fast<kTkThreads, kCandPer>(tk, need, 0u, hw, smw, s_list);
+    }
+    unsigned win = 0;
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u)
+      if (mk[u] > tau || (mk[u] == tau && uint32_t(cv[u]) <= tie_max)) win |= 1u << u;
+    int tw;
+    const int wbase = block_excl_scan<kTkThreads>(__popc(win), &tw, smw);  // winners before mine
+    // winners before reservation position p: s_wb[p / 32] + those of its thread below p % 32
+    int* s_wb = reinterpret_cast<int*>(stage);    // [kTkThreads + 1]
+    int* s_wm = s_wb + kTkThreads + 1;            // [kTkThreads] winner bits per thread
+    int* s_first = s_wm + kTkThreads;             // [C] winners before the chunk's first candidate
+    int* s_pre = s_first + C;                     // [C] winners of the chunks before
+    s_wb[tid] = wbase;
+    s_wm[tid] = int(win);
+    if (tid == 0) s_wb[kTkThreads] = tw;
+    __syncthreads();
+    auto wbefore = [&](int p) {
+      const int t = p / kCandPer;
+      return t >= kTkThreads ? s_wb[kTkThreads]
+                             : s_wb[t] + __popc(unsigned(s_wm[t]) & ((1u << (p % kCandPer)) - 1u));
+    };
+    int carry = 0;
+    for (int c0 = 0; c0 < C; c0 += kTkThreads) {
+      const int ch = c0 + tid;
+      if (c0 > 0) rec = ch < C ? __ldcg(reinterpret_cast<const int2*>(recs) + ch) : make_int2(0, 0);
+      int wch = 0, first = 0;
+      if (ch < C && rec.y > 0) {
+        first = wbefore(rec.x);
+        wch = wbefore(rec.x + rec.y) - first;
+      }
+      int t;
+      const int pre = block_excl_scan<kTkThreads>(wch, &t, smw) + carry;
+      if (ch < C) {
+        s_first[ch] = first;
+        s_pre[ch] = pre;
+      }
+      carry += t;
+    }
+    __syncthreads();
+    int wb = wbase;
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) {
-      if (src[u] < 0) break;
-      const bool sel = mk[u] > tau || (mk[u] == tau && e++ < need);
-      if (sel) {
+      if ((win >> u) & 1u) {
         const int s = int(uint32_t(cv[u]));
-        if (p < a.K) {
-          out[p] = s;
-          if (phys) phys[p] = phys_row(a, w.b, s);
+        const int ch = s / a.chunk;
+        const int pos = s_pre[ch] + (wb - s_first[ch]);
+        if (pos < a.K) {
+          out[pos] = s;
+          if (phys) phys[pos] = phys_row(a, w.b, s);
         }
-        ++p;
+        ++wb;
       }
     }
   }
-  // the row's state starts from zero at the next call
+  // the row's 128-token maxima and state start from zero at the next call
+  for (int i = tid; i < (w.L + 127) >> 7; i += kTkThreads) gm128[i] = 0u;
   __syncthreads();
   if (tid == 0) {
     st[kStCursor] = 0;
@@ -537,8 +585,8 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
 }  // namespace
 
 // CTAs per row: about one wave over all rows, each filtering a chunk of a
-// multiple of 1,024 tokens, at most kRoundTok (so at most cap / 1,024 = the
-// row's max_chunks records, and at most 8,192 CTAs per row at the largest cap).
+// multiple of 1,024 tokens, at most kRoundTok (so at most 8,192 CTAs per row
+// at the largest cap).
 struct TopkGrid {
   int ctas, chunk;
 };
@@ -560,8 +608,10 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   a.stride = score_stride;
   a.ctx_lens = ctx_lens;
   a.block_table = block_table;
-  a.gmax = reinterpret_cast<const uint32_t*>(ws + L.gmax);
+  a.gmax = reinterpret_cast<uint32_t*>(ws + L.gmax);
+  a.gmax128 = reinterpret_cast<uint32_t*>(ws + L.gmax128);
   a.gstride = L.gstride;
+  a.g128stride = L.g128stride;
   a.n_q = p.n_q;
   a.cap = L.cap;
   a.K = p.topk;
@@ -577,12 +627,11 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   cudaError_t e = cudaSuccess;
   if (!have_gmax) {
     const int gx = std::max(1, (L.cap + 16383) / 16384);  // two 1,024-token blocks per warp
-    e = launch_pdl(topk_gmax_kernel, dim3(gx, L.rows), dim3(kGmaxThreads), 0, st, a,
-                   reinterpret_cast<uint32_t*>(ws + L.gmax));
+    e = launch_pdl(topk_gmax_kernel, dim3(gx, L.rows), dim3(kGmaxThreads), 0, st, a);
   }
   const TopkGrid tg = topk_grid(L);
   a.chunk = tg.chunk;
-  const size_t smem = size_t(2 * tg.ctas + 1) * 4;
+  const size_t smem = std::max(size_t(tg.chunk) * 4, size_t(2 * kTkThreads + 1 + 2 * tg.ctas) * 4);
   if (e == cudaSuccess && smem > 48 * 1024)
     e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e == cudaSuccess)

@@ -6,7 +6,7 @@
 // into the allocator (cudaMalloc can synchronise the device), or a C caller
 // that is handed only input and output pointers. For them this entry point
 // keeps the top-k scratch (per-row selection state, per-chunk candidate
-// offsets, the candidate buffer, the rows' 32-token score maxima) in one
+// offsets, the candidate buffer, the rows' 32- and 128-token score maxima) in one
 // file-scope device array that every GPU loading the library holds until the
 // process exits.
 #include <mutex>
@@ -18,16 +18,16 @@ namespace {
 
 constexpr int kNoAllocMaxRows = 64;                 // batch * n_q
 constexpr int kNoAllocMaxCtx = 1 << 20;             // max_pages_per_req * page_size
-constexpr int kNoAllocMaxChunks = kNoAllocMaxCtx / kTopkChunk;
 constexpr size_t kNoAllocBytes =
     256 +                                                                        // error word
     size_t(kNoAllocMaxRows) * kRowState * 4 +                                    // row state
-    size_t(kNoAllocMaxRows) * kNoAllocMaxChunks * 2 * 4 +                        // chunk (offset, count)
+    size_t(kNoAllocMaxRows) * (kNoAllocMaxCtx / kTopkChunk) * 2 * 4 +            // chunk (offset, count)
     size_t(kNoAllocMaxRows) * kCandCap * 8 +                                     // candidates
     size_t(kNoAllocMaxRows) * (kNoAllocMaxCtx / 32) * 4 +                        // 32-token maxima
-    4 * 256;                                                                     // region alignment
+    size_t(kNoAllocMaxRows) * (kNoAllocMaxCtx / 128) * 4 +                       // 128-token maxima
+    6 * 256;                                                                     // region alignment
 
-// The scratch itself (about 13.1 MB). Only host code below takes its address.
+// The scratch itself (about 15.2 MB). Only host code below takes its address.
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
@@ -60,12 +60,14 @@ WsLayout noalloc_layout(const dsa_params_t& p) {
   L.max_chunks = (L.cap + kTopkChunk - 1) / kTopkChunk;
   L.splits = 1;
   L.gstride = ((L.cap >> 5) + 3) & ~3;
+  L.g128stride = ((L.cap >> 7) + 3) & ~3;
   size_t o = 0;
   L.err = o; o = align256(o + 256);
   L.state = o; o = align256(o + size_t(L.rows) * kRowState * 4);
   L.chunkinfo = o; o = align256(o + size_t(L.rows) * L.max_chunks * 2 * 4);
   L.cand = o; o = align256(o + size_t(L.rows) * kCandCap * 8);
   L.gmax = o; o = align256(o + size_t(L.rows) * L.gstride * 4);
+  L.gmax128 = o; o = align256(o + size_t(L.rows) * L.g128stride * 4);
   L.total = o;
   return L;
 }

@@ -287,7 +287,7 @@ dsa_status_t dsa_lse_combine(const dsa_params_t* params, int32_t parts, const vo
  * and output pointers). The article has no counterpart: this is a deployment
  * variant of dsa_topk, with the same arguments minus the workspace and the same
  * results bit for bit.
- * - Scratch: one static device array of about 4.3 MB inside libdsa, held by
+ * - Scratch: one static device array of about 15.2 MB inside libdsa, held by
  *   every GPU that loads the library until the process exits. The call
  *   allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  * - Limits: batch * n_q <= 64 and max_pages_per_req * page_size <= 1,048,576;
