@@ -247,14 +247,17 @@ __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t
     const int b = s_bin;
     kk = s_rank;
     const int n = s_cnt;
-    // bin b's keys: [lo + (b << sh), lo + (b << sh) + 2^sh - 1], widened at the ends in round one
-    const uint32_t blo = lo + (uint32_t(b) << sh);
-    uint32_t nlo = blo, nhi = sh >= 32 ? 0xFFFFFFFFu : blo + ((1u << sh) - 1u);
-    if (nhi < blo || nhi > hi) nhi = hi;
+    // bin b's keys: [lo + (b << sh), lo + (b << sh) + 2^sh - 1] (in 64 bits: the
+    // top bin of round one may start past 2^32), widened at the ends in round one
+    const uint64_t blo = uint64_t(lo) + (uint64_t(b) << sh);
+    const uint64_t bhi = blo + ((uint64_t(1) << sh) - 1u);
+    uint32_t nlo = uint32_t(min(blo, uint64_t(hi)));
+    uint32_t nhi = uint32_t(min(bhi, uint64_t(hi)));
     const bool below = first && b == 0;  // bin 0 of round one also holds every key below lo
     if (below) nlo = floor;
     if (first && b == 2047) {  // the top bin of round one also holds every key above hi
-      if (hi != 0xFFFFFFFFu) nlo = min(nlo, hi + 1u);
+      // (when its own range starts above hi, it holds only those: then hi < 2^32 - 1)
+      nlo = blo <= uint64_t(hi) ? uint32_t(blo) : hi + 1u;
       nhi = 0xFFFFFFFFu;
     }
     first = false;

@@ -205,10 +205,11 @@ dsa_status_t dsa_decode(const dsa_params_t* params, const void* q_idx, const flo
   if (e == cudaSuccess)
     e = launch_indexer(*params, L, w8, key_pool, block_table, ctx_lens, scores, L.cap, stream, 1, 0, true);
   if (e == cudaSuccess)
-    e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream, true);
+    e = launch_topk(*params, L, w8, scores, L.cap, ctx_lens, block_table, topk_idx_out, nullptr, stream, true,
+                    lat_pool);
   if (e == cudaSuccess)
     e = launch_sparse_mla(*params, L, w8, q, lat_pool, block_table, ctx_lens, topk_idx_out, out, lse,
-                          stream);
+                          stream, true);
   return cuda_status(e);
 }
 

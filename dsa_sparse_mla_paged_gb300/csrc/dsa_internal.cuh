@@ -249,10 +249,12 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
                            bool keep128 = false);
 // have_gmax: the scorer of the same call has just written the group maxima of
 // these scores into the workspace (dsa_decode); otherwise a first kernel
-// computes them from the scores.
+// computes them from the scores. lat_pool (dsa_decode, else null): the
+// candidates' latent rows are prefetched into L2 for the attention.
 cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                         int64_t score_stride, const int32_t* ctx_lens, const int32_t* block_table,
-                        int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st, bool have_gmax);
+                        int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st, bool have_gmax,
+                        const void* lat_pool = nullptr);
 cudaError_t launch_dcp_merge(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                              int64_t score_stride, const int32_t* ctx_lens, int world, int32_t* topk_idx,
                              int32_t* stats, cudaStream_t st);
@@ -275,9 +277,11 @@ struct FrontendIn {
 };
 cudaError_t launch_idx_frontend(const dsa_params_t& p, const WsLayout& L, char* ws, const FrontendIn& in,
                                 cudaStream_t st);
+// early: the call follows this library's own kernels in one chain (dsa_decode),
+// so the query and the set-up may be fetched before the wait on the top-k.
 cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q,
                               const void* lat_pool, const int32_t* block_table,
                               const int32_t* ctx_lens, const int32_t* topk_idx, void* out,
-                              float* lse, cudaStream_t st);
+                              float* lse, cudaStream_t st, bool early = false);
 
 }  // namespace dsa

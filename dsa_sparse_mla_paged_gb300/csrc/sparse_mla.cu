@@ -66,6 +66,7 @@ struct MlaTc {
   float* opart;
   float* lpart;
   int* err;
+  int early;  // set up and fetch Q before the wait on the previous kernel (dsa_decode: q is a caller input)
 };
 
 __device__ __forceinline__ uint32_t bf16x2_from_e4m3x2(uint16_t two) {
@@ -276,7 +277,6 @@ __device__ void converter_role_nv(const MlaTc& a, int ct, int lane, int nt, cons
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
     sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, MlaTc a) {
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = sm;
@@ -300,8 +300,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
   const int peer = half ^ 1;
   const int split = blockIdx.x >> 1, r = blockIdx.y;
   const int b = r / a.n_q, t = r - b * a.n_q;
-  const int ctx = a.ctx_lens[b];
-  const int L = (ctx < a.n_q || ctx > a.cap) ? 0 : ctx - a.n_q + t + 1;
   const int j0 = split * a.per_split;
   const int j1 = min(a.K, j0 + a.per_split);
   const int nt = j1 > j0 ? (j1 - j0 + kNT - 1) / kNT : 0;
@@ -311,6 +309,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
   float* lp = a.lpart + (size_t(r) * a.splits + split) * kHeads;
 
   if (nt == 0) {  // a split past the top-k list (both CTAs of the pair return here)
+    pdl_wait();
+    pdl_trigger();
     for (int i = threadIdx.x; i < kHeads * 256; i += blockDim.x) op[(i >> 8) * kDNope + (i & 255)] = 0.f;
     if (half == 0)
       for (int i = threadIdx.x; i < kHeads; i += blockDim.x) lp[i] = -INFINITY;
@@ -343,15 +343,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
+  // this CTA's K-blocks of the query (rows r * 96 ..): CTA 0 nope 0..3 and the rope, CTA 1 nope 4..7
+  auto issue_q = [&]() {
+    ptx::mbar_arrive_expect_tx(q_full, nkb * kQBlk);
+    for (int kl = 0; kl < nkb; ++kl) {
+      const int kbg = half == 0 ? (kl < 4 ? kl : 8) : 4 + kl;
+      ptx::tma_load_2d(Qs + kl * kQBlk, &qmap, q_full, kbg * 64, r * kHeads);
+    }
+  };
+  if (a.early && warp == 3 && lane == 0) issue_q();
+  // everything above is on-chip set-up or a read of the caller's query; what
+  // comes next reads the top-k list of the previous kernel
+  pdl_wait();
+  pdl_trigger();  // the split combine may take free SMs now (it waits for this grid)
+  const int ctx = a.ctx_lens[b];
+  const int L = (ctx < a.n_q || ctx > a.cap) ? 0 : ctx - a.n_q + t + 1;
 
   if (warp == 3) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(q_full, nkb * kQBlk);
-      for (int kl = 0; kl < nkb; ++kl) {
-        const int kbg = half == 0 ? (kl < 4 ? kl : 8) : 4 + kl;
-        ptx::tma_load_2d(Qs + kl * kQBlk, &qmap, q_full, kbg * 64, r * kHeads);
-      }
+      if (!a.early) issue_q();
       if (!ptx::mbar_wait(q_full, 0)) ok = false;
       const uint32_t id_qk = ptx::idesc(1, 1, 128, kNT);
       const uint32_t id_pv = ptx::idesc(1, 1, 128, 256, 0, 1);
@@ -456,9 +467,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
       }
       // each warp tells the peer it has read its rows; warp 0 first re-arms
       // x_full[bk] for tile k+2 (the peer sends only after all three arrivals)
+      // (only when the peer has a tile k + 2 to send into this buffer)
       __syncwarp();
-      if (lane == 0) {
-        if (warp == 0 && k + 2 < nt) ptx::mbar_arrive_expect_tx(x_full + bk, kXBytes);
+      if (lane == 0 && k + 2 < nt) {
+        if (warp == 0) ptx::mbar_arrive_expect_tx(x_full + bk, kXBytes);
         ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(x_free + bk), peer));
       }
       const unsigned long long vm = vmask[k];
@@ -548,7 +560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
 // LSE merge of the splits of one row: out = sum_i e^{lse_i - lse} O_i, lse = ln sum_i e^{lse_i}.
 // One CTA per (row, 2 heads): 128 threads per head, 4 dims each. In every warp
 // lane i < splits holds split i's lse, so the weights come from two shuffle
-// reductions; the partial rows are read 8 splits at a time.
+// reductions; every split's partial row is read at once.
 constexpr int kCombThreads = 256;
 constexpr int kCombHeads = kCombThreads / 128;
 
@@ -573,19 +585,22 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* 
   const float wgt = m == -INFINITY ? 0.f : expf(li - L);
   const float4* src = reinterpret_cast<const float4*>(opart + (size_t(r) * splits * kHeads + h) * kDNope) + d4;
   const size_t split_stride = size_t(kHeads) * kDNope / 4;  // float4 per split
+  // every split's partial in flight at once (splits <= kMaxSplits; a slot past
+  // the last split reads split 0 again with weight 0), then added in split order
+  float wv[kMaxSplits];
+#pragma unroll
+  for (int u = 0; u < kMaxSplits; ++u) {
+    const float wi = __shfl_sync(0xffffffffu, wgt, u & 31);
+    wv[u] = u < splits ? wi : 0.f;
+  }
+  float4 v[kMaxSplits];
+#pragma unroll
+  for (int u = 0; u < kMaxSplits; ++u) v[u] = __ldg(src + (u < splits ? u : 0) * split_stride);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = 0; i0 < splits; i0 += 8) {
-    float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = i0 + u < splits ? __ldg(src + (i0 + u) * split_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float wi = __shfl_sync(0xffffffffu, wgt, (i0 + u) & 31);
-      if (i0 + u < splits) {
-        acc.x = fmaf(wi, v[u].x, acc.x); acc.y = fmaf(wi, v[u].y, acc.y);
-        acc.z = fmaf(wi, v[u].z, acc.z); acc.w = fmaf(wi, v[u].w, acc.w);
-      }
-    }
+  for (int u = 0; u < kMaxSplits; ++u) {
+    acc.x = fmaf(wv[u], v[u].x, acc.x); acc.y = fmaf(wv[u], v[u].y, acc.y);
+    acc.z = fmaf(wv[u], v[u].z, acc.z); acc.w = fmaf(wv[u], v[u].w, acc.w);
   }
   const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
   const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
@@ -600,7 +615,7 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* 
 
 cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q,
                               const void* lat_pool, const int32_t* block_table, const int32_t* ctx_lens,
-                              const int32_t* topk_idx, void* out, float* lse, cudaStream_t st) {
+                              const int32_t* topk_idx, void* out, float* lse, cudaStream_t st, bool early) {
   CUtensorMap qmap;
   {
     const uint64_t dims[2] = {uint64_t(kDQK), uint64_t(L.rows) * kHeads};
@@ -629,6 +644,7 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   t.opart = reinterpret_cast<float*>(ws + L.opart);
   t.lpart = reinterpret_cast<float*>(ws + L.lpart);
   t.err = reinterpret_cast<int*>(ws + L.err);
+  t.early = early ? 1 : 0;
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kTcMlaSmem));
   if (e != cudaSuccess) return e;

@@ -73,6 +73,11 @@ struct TopkArgs {
   int* err;
   int32_t* topk_idx;
   int32_t* phys_rows;
+  // dsa_decode: the latent pool whose rows the attention reads next; each CTA
+  // prefetches its candidates' rows into L2 once its part is done (or null)
+  const uint8_t* lat_pool;
+  int64_t lat_stride;
+  int lat_row;
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) { return score_order_key(f); }
@@ -470,14 +475,29 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     }
   }
 
-  // the last CTA of the row to get here selects
+  // the last CTA of the row to get here selects; every thread's candidate
+  // writes are made visible device-wide before the CTA's arrival
+  __threadfence();
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     s_last = atomicAdd(st + kStArrived, 1) == C - 1;
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last) {
+    // the attention gathers the winners' latent rows next: start pulling this
+    // chunk's candidates (a superset of its winners) into L2
+    if (a.lat_pool) {
+      for (uint32_t m = pass; m; m &= m - 1u) {
+        const int j = __ffs(m) - 1;
+        const int s = wb + 4 * (lane + 32 * (j >> 2)) + (j & 3);
+        const int pg = a.block_table[size_t(w.b) * a.max_pages + s / kPage];
+        if (pg >= 0 && pg < a.num_pages)
+          ptx::prefetch_l2_bulk(a.lat_pool + size_t(pg) * a.lat_stride + size_t(s % kPage) * a.lat_row, a.lat_row);
+      }
+    }
+    return;
+  }
   __threadfence();
   const int total = __ldcg(st + kStCursor);
   const int ovf = __ldcg(st + kStOverflow);
@@ -602,7 +622,8 @@ TopkGrid topk_grid(const WsLayout& L) {
 
 cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, const float* scores,
                         int64_t score_stride, const int32_t* ctx_lens, const int32_t* block_table,
-                        int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st, bool have_gmax) {
+                        int32_t* topk_idx, int32_t* phys_rows, cudaStream_t st, bool have_gmax,
+                        const void* lat_pool) {
   TopkArgs a;
   a.scores = scores;
   a.stride = score_stride;
@@ -624,6 +645,9 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   a.err = reinterpret_cast<int*>(ws + L.err);
   a.topk_idx = topk_idx;
   a.phys_rows = phys_rows;
+  a.lat_pool = static_cast<const uint8_t*>(lat_pool);
+  a.lat_stride = p.lat_page_stride;
+  a.lat_row = p.lat_fmt == DSA_LAT_NVFP4_352 ? kDNope / 2 + kDNope / 16 + kDRope : kLatRowFp8;
   cudaError_t e = cudaSuccess;
   if (!have_gmax) {
     const int gx = std::max(1, (L.cap + 16383) / 16384);  // two 1,024-token blocks per warp

@@ -126,6 +126,23 @@ def test_topk_bit_exact_long_rows(k):
             assert np.array_equal(idx[b], O.topk_select(mat[b, :ctx[b]], k)), (name, b)
 
 
+@pytest.mark.parametrize("k", [1, 2, 16, 33])
+def test_topk_small_k_many_rows(k):
+    """Small K over rows of several chunks: the K-th key usually lies above
+    the keys the first warp samples, in the top bin of the first histogram
+    round (whose range can start past 2^32 in 32-bit arithmetic)."""
+    rng = np.random.default_rng(40 + k)
+    ctx = [int(x) for x in rng.integers(3000, 9000, 12)]
+    inp = gen.make_inputs(len(ctx), 1, ctx, seed=41, topk=k)
+    d = Dev(inp)
+    mat = rng.standard_normal((len(ctx), max(ctx))).astype(np.float32)
+    for rep in range(3):
+        idx, _ = d.topk(mat)
+        idx = idx.cpu().numpy()
+        for b in range(len(ctx)):
+            assert np.array_equal(idx[b], O.topk_select(mat[b, :ctx[b]], k)), (rep, b)
+
+
 def test_topk_multi_token_rows_and_phys_rows():
     import dsa_sparse_mla_paged_gb300 as dsa
 
