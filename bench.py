@@ -31,22 +31,41 @@ sys.path.insert(0, ROOT)
 
 METRIC = "DSA decode layer-steps/sec and achieved HBM GB/s (% of GB300 roofline)"
 UNIT = "layer-steps/s"
-KEY_B, LAT_B = 132, 576
+# q_idx bf16 [32][128] + w fp32 [32] + q bf16 [96][576] + out bf16 [96][512] per query row
 Q_OUT_B = 32 * 128 * 2 + 32 * 4 + 96 * 576 * 2 + 96 * 512 * 2
 
 
-def step_bytes(ctx, n_q, topk):
-    """Algorithmic bytes of one step: every index key, each selected latent, q/w/out."""
-    tot = 0
-    for c in ctx:
-        union = min(int(c), topk + n_q - 1) if n_q > 1 else min(int(c), topk)
-        tot += KEY_B * int(c) + LAT_B * union + n_q * Q_OUT_B
-    return tot
+def fmt_bytes(inp):
+    """Bytes per token of the workload's index key and latent formats."""
+    import gen
+
+    return gen.KEY_BYTES[inp.key_fmt], gen.LAT_BYTES[inp.lat_fmt]
 
 
-def indexer_bytes(ctx, n_q):
+def latent_union(idx, batch, n_q):
+    """|union over t of S_{b,t}| per request, from the top-k indices a step produced
+    (int32 [batch * n_q, K], -1 padded)."""
+    idx = np.asarray(idx).reshape(batch, n_q, -1)
+    return [int(np.unique(r[r >= 0]).size) for r in idx.reshape(batch, -1)]
+
+
+def step_bytes(inp, union):
+    """Algorithmic bytes of one step: every visible index key once per request, each
+    latent of the union of the request's selected sets once, q/w/out per row."""
+    kb, lb = fmt_bytes(inp)
+    return sum(kb * int(c) + lb * int(u) + inp.n_q * Q_OUT_B for c, u in zip(inp.ctx, union))
+
+
+def indexer_bytes(inp):
     """Algorithmic bytes of the indexer stage: keys + scales once, the query and weights."""
-    return sum(KEY_B * int(c) for c in ctx) + len(ctx) * n_q * (32 * 128 * 2 + 32 * 4)
+    kb, _ = fmt_bytes(inp)
+    return sum(kb * int(c) for c in inp.ctx) + inp.batch * inp.n_q * (32 * 128 * 2 + 32 * 4)
+
+
+def step_dtype(inp):
+    """The arithmetic of the step: the scorer's MMA operands and the attention MMA's."""
+    storage = {"fp8": "fp8", "mxfp4": "mxfp4"}[inp.key_fmt] + "/" + {"fp8": "fp8", "nvfp4": "nvfp4"}[inp.lat_fmt]
+    return "fp8+bf16" if storage == "fp8/fp8" else f"fp8+bf16 ({storage} storage)"
 
 
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -197,34 +216,46 @@ def oracle_single_thread_small():
         return None
 
 
+def reference_plan(t_step, steps, warmup, budget_s):
+    """Whole oracle steps to run: (warm-up steps, timed steps) within budget_s seconds,
+    given the seconds of one step. The requested counts are kept when they fit; at
+    least one of each is run."""
+    w = max(1, min(warmup, int(0.2 * budget_s / t_step)))
+    k = max(1, min(steps, int(0.8 * budget_s / t_step)))
+    return w, k
+
+
 def run_reference(args, rank):
+    """The reference arm: the oracle (float64 NumPy on the host cores) running whole
+    steps of the workload -- every request of the batch per step."""
     import gen
 
     line = {"impl": "reference", "metric": METRIC, "unit": UNIT, "higher_is_better": True, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "data": "synthetic", "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64"}
+            "data": "synthetic", "scaling": "weak", "vs_baseline": None, "dtype": "f64"}
     if rank != 0:
         return
     from oracle import dsa as O
 
     inp = gen.make_workload(args.workload)
-    # one step of the reference arm = the oracle on one request (a bounded sample
-    # of the workload's step); throughput is scaled to whole steps
-    def one(i):
-        O.decode(inp, requests=[i % inp.batch])
-    for i in range(args.warmup):
-        one(i)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        one(i)
+    O.decode(inp)  # the first warm-up step, which also sizes the run
+    t_first = time.perf_counter() - t0
+    warm, steps = reference_plan(t_first, args.steps, args.warmup, getattr(args, "ref_budget", 150.0))
+    for _ in range(warm - 1):
+        O.decode(inp)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        O.decode(inp)
     dt = time.perf_counter() - t0
-    per_step = dt / args.steps * inp.batch
+    per_step = dt / steps
     v = 1.0 / per_step
-    line.update({"value": v, "ms_per_step": per_step * 1e3,
+    cores = len(os.sched_getaffinity(0))
+    line.update({"steps": steps, "warmup": warm, "steps_requested": args.steps, "warmup_requested": args.warmup,
+                 "value": v, "ms_per_step": per_step * 1e3, "timed_seconds": dt,
                  "config": {"workload": args.workload, "batch": inp.batch, "n_q": inp.n_q,
                             "ctx": int(inp.ctx.max()), "topk": inp.topk},
-                 "cpu_baseline": {"value": v, "unit": UNIT, "kind": "oracle", "cores": len(os.sched_getaffinity(0)),
-                                  "sample": "one request per step (1/batch of a layer-step)"},
+                 "cpu_baseline": {"value": v, "unit": UNIT, "kind": "oracle", "cores": cores,
+                                  "sample": f"{steps} whole steps ({inp.batch} requests each), timed back to back"},
                  "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
     print(json.dumps(line), flush=True)
 
@@ -239,8 +270,7 @@ def run_stage(args):
     import dsa_sparse_mla_paged_gb300 as dsa
     import gen
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from dsa_testlib import Dev
+    from gen.device import Dev
 
     torch.cuda.set_device(0)
     dsa.load()
@@ -318,8 +348,8 @@ def run_stage(args):
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1) / args.steps
     score_bytes = 4 * sum(int(c) for c in inp.ctx) * inp.n_q
-    nbytes = {"indexer": indexer_bytes(inp.ctx, inp.n_q), "topk": score_bytes,
-              "mla": step_bytes(inp.ctx, inp.n_q, inp.topk) - indexer_bytes(inp.ctx, inp.n_q),
+    nbytes = {"indexer": indexer_bytes(inp), "topk": score_bytes,
+              "mla": step_bytes(inp, latent_union(idx.cpu().numpy(), inp.batch, inp.n_q)) - indexer_bytes(inp),
               # every score read once; the partials read once and the result written
               "dcp_merge": score_bytes, "dcp_combine": (W + 1) * d.rows * 96 * 512 * 2 + (W + 1) * d.rows * 96 * 4,
               # weights once, the rows' inputs, q8 + w' out, one key per row
@@ -335,7 +365,7 @@ def run_stage(args):
         rows = list(range(inp.n_q)) if W == 1 else [int(t) for t in _rank_rows(inp.n_q, W, max(args.rank, 0))]
         keys = sum(max(0, int(c) - inp.n_q + t + 1) for c in inp.ctx for t in rows)
         flops = 2.0 * 32 * 128 * keys
-        byts = 132 * sum(int(c) for c in inp.ctx) + 4 * keys + len(rows) * inp.batch * (32 * 128 * 2 + 32 * 4)
+        byts = fmt_bytes(inp)[0] * sum(int(c) for c in inp.ctx) + 4 * keys + len(rows) * inp.batch * (32 * 128 * 2 + 32 * 4)
         line.update({"world": W, "rank": max(args.rank, 0), "rows_scored": len(rows) * inp.batch,
                      "keys_scored": keys, "bytes": byts, "gbs": byts / (ms * 1e-3) / 1e9,
                      "tflops": flops / (ms * 1e-3) / 1e12})
@@ -374,8 +404,7 @@ def run_ours(args, rank, world):
     import dsa_sparse_mla_paged_gb300 as dsa
     import gen
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from dsa_testlib import Dev
+    from gen.device import Dev
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -577,20 +606,22 @@ def run_ours(args, rank, world):
 
     if rank == 0:
         peak, peak_kind = peaks()
-        sbytes = step_bytes(inp.ctx, inp.n_q, inp.topk)
-        ibytes = indexer_bytes(inp.ctx, inp.n_q)
+        union = latent_union(idx.cpu().numpy(), inp.batch, inp.n_q)
+        sbytes = step_bytes(inp, union)
+        ibytes = indexer_bytes(inp)
         gbs = sbytes / (ms * 1e-3) / 1e9
         idx_gbs = ibytes / (idx_ms_live * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": replica_throughput(ms, world), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8+bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": step_dtype(inp), "data": "synthetic",
             "config": {"workload": args.workload, "batch": inp.batch, "n_q": inp.n_q,
                        "ctx": int(inp.ctx.max()), "topk": inp.topk, "page_size": inp.page_size,
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (%.2f GB per step), no flush" % (
                            (inp.key_pool.nbytes + inp.lat_pool.nbytes) / 1e9)},
             "achieved_gbs": gbs, "hbm_frac": gbs / peak, "step_bytes": sbytes,
+            "latent_union_per_request": {"min": min(union), "max": max(union), "sum": sum(union)},
             "stage_ms": stage_ms, "ms_per_step_as_parts": ms_parts,
             "roofline": {"bound": "hbm", "kernel": "indexer stage (dsa_indexer_scores: q quantisation + scorer)",
                          "achieved": idx_gbs,
@@ -618,6 +649,8 @@ def main():
     ap.add_argument("--workload", default="b4_ctx1m")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=150.0,
+                    help="reference arm: seconds of oracle steps to run at most (warm-up + timed)")
     ap.add_argument("--stage", default="all",
                     choices=["all", "indexer", "topk", "mla", "dcp_merge", "dcp_combine", "frontend", "prefill"],
                     help="time one entry point alone (kernel profiling; the dcp_* stages emulate --world shards)")

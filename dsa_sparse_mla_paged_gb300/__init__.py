@@ -6,7 +6,7 @@ exceptions. There is no fallback: if libdsa.so is missing, ``load()`` raises.
 
 Entry points mirror include/dsa.h: ``workspace_size``, ``indexer_scores``,
 ``indexer_frontend``, ``indexer_prefill_scores``, ``topk``, ``topk_noalloc``, ``dcp_topk_merge``, ``lse_combine``, ``sparse_mla_decode``,
-``decode``, ``get_device_error``, ``status_string``.
+``decode``, ``get_device_error``, ``selftest_wait_timeout``, ``status_string``.
 """
 from __future__ import annotations
 
@@ -20,7 +20,7 @@ DSA_KEY_FP8_132, DSA_KEY_MXFP4_68 = 0, 1
 DSA_LAT_FP8_576, DSA_LAT_NVFP4_352 = 0, 1
 DSA_EMIT_PHYS_ROWS = 0x1
 DSA_Q_PREPARED = 0x2
-DSA_DEVERR_BLOCK_TABLE, DSA_DEVERR_CTX, DSA_DEVERR_TOPK_INDEX = 0x1, 0x2, 0x4
+DSA_DEVERR_BLOCK_TABLE, DSA_DEVERR_CTX, DSA_DEVERR_TOPK_INDEX, DSA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 # Kernels one dsa_decode launches (q quantisation, indexer, top-k, sparse MLA,
 # split combine); kept in step with csrc/.
@@ -38,6 +38,7 @@ EXPORTS = (
     "dsa_sparse_mla_decode",
     "dsa_decode",
     "dsa_get_device_error",
+    "dsa_selftest_wait_timeout",
     "dsa_status_string",
 )
 
@@ -117,6 +118,7 @@ def load() -> ctypes.CDLL:
         "dsa_sparse_mla_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_decode": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_get_device_error": [vp, vp, ctypes.POINTER(ctypes.c_int32)],
+        "dsa_selftest_wait_timeout": [vp, sz, ctypes.c_uint32, vp],
         "dsa_status_string": [ctypes.c_int],
     }
     for name, args in sig.items():
@@ -232,6 +234,16 @@ def decode(params, q_idx, w, key_pool, q, lat_pool, block_table, ctx_lens, out, 
 
 
 def get_device_error(ws, stream=None) -> int:
+    """The workspace's DSA_DEVERR_* bits since the last read (then cleared). A
+    timed-out wait (status DSA_ERR_TIMEOUT) is reported through the bits too."""
     code = ctypes.c_int32(0)
-    _check("dsa_get_device_error", load().dsa_get_device_error(_ptr(ws), _stream(stream), ctypes.byref(code)))
+    st = load().dsa_get_device_error(_ptr(ws), _stream(stream), ctypes.byref(code))
+    if st != DSA_ERR_TIMEOUT:
+        _check("dsa_get_device_error", st)
     return int(code.value)
+
+
+def selftest_wait_timeout(ws, poll_limit=10000, stream=None):
+    """Run the bounded-wait abort path on purpose (sets DSA_DEVERR_TIMEOUT in ws)."""
+    _check("dsa_selftest_wait_timeout", load().dsa_selftest_wait_timeout(
+        _ptr(ws), _nbytes(ws), int(poll_limit), _stream(stream)))

@@ -222,7 +222,7 @@ dsa_status_t dsa_get_device_error(void* ws, cudaStream_t stream, int32_t* code) 
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   *code = v;
-  return DSA_OK;
+  return (v & DSA_DEVERR_TIMEOUT) ? DSA_ERR_TIMEOUT : DSA_OK;
 }
 
 const char* dsa_status_string(dsa_status_t status) {

@@ -64,7 +64,7 @@ typedef enum {
   DSA_ERR_UNSUPPORTED = 2,  /* a size or format this build does not implement */
   DSA_ERR_WORKSPACE = 3,    /* ws_bytes below dsa_workspace_size() */
   DSA_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
-  DSA_ERR_TIMEOUT = 5       /* reserved: a bounded device wait gave up */
+  DSA_ERR_TIMEOUT = 5       /* a bounded device wait gave up (dsa_get_device_error) */
 } dsa_status_t;
 
 /* Index-key formats (section "面向三种状态的 KV 缓存": index key 132 B in FP8,
@@ -144,15 +144,6 @@ dsa_status_t dsa_indexer_scores(const dsa_params_t* params, const void* q_idx, c
                                 const int32_t* ctx_lens, float* scores, int64_t score_stride,
                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Stage 2, exact top-k ("K3.1 Pro 中的稀疏注意力": keep the top 2,048 tokens).
- * For each row: the min(K, L) tokens with the highest fp32 score, ties going to
- * the lower token index (-0 == +0), written in ascending token order to
- * topk_idx[row][0 .. min(K, L)), the rest of the row set to -1.
- *   scores   fp32 [B * n_q, score_stride] (only s < L_{b,t} is read)
- *   topk_idx int32 [B * n_q, K]
- *   phys_rows int32 [B * n_q, K] or NULL: page * page_size + slot of each
- *            selected token ("融合的 indexer ... 输出注意力读取的物理 KV 行"),
- *            -1 padded; needs DSA_EMIT_PHYS_ROWS and block_table. */
 /* Stage 1 for a prefill chunk with token sharding ("预填充：按 token 而非按头分片注意力":
  * the GPUs divide a prefill's query tokens, not its heads, and pair slices so
  * that causal work evens out: with 8 GPUs and 16 slices, GPU r has r and 15 - r).
@@ -168,6 +159,15 @@ dsa_status_t dsa_indexer_prefill_scores(const dsa_params_t* params, int32_t worl
                                         const int32_t* ctx_lens, float* scores, int64_t score_stride, void* ws,
                                         size_t ws_bytes, cudaStream_t stream);
 
+/* Stage 2, exact top-k ("K3.1 Pro 中的稀疏注意力": keep the top 2,048 tokens).
+ * For each row: the min(K, L) tokens with the highest fp32 score, ties going to
+ * the lower token index (-0 == +0), written in ascending token order to
+ * topk_idx[row][0 .. min(K, L)), the rest of the row set to -1.
+ *   scores   fp32 [B * n_q, score_stride] (only s < L_{b,t} is read)
+ *   topk_idx int32 [B * n_q, K]
+ *   phys_rows int32 [B * n_q, K] or NULL: page * page_size + slot of each
+ *            selected token ("融合的 indexer ... 输出注意力读取的物理 KV 行"),
+ *            -1 padded; needs DSA_EMIT_PHYS_ROWS and block_table. */
 dsa_status_t dsa_topk(const dsa_params_t* params, const float* scores, int64_t score_stride,
                       const int32_t* ctx_lens, const int32_t* block_table, int32_t* topk_idx,
                       int32_t* phys_rows, void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -254,8 +254,11 @@ dsa_status_t dsa_indexer_frontend(const dsa_params_t* params, const dsa_frontend
  *               first min(K, L_r) and the K largest words are selected again.
  * The result is the top min(K, L) of all tokens under the global order, written
  * like dsa_topk (ascending token order, -1 padded); rows with L <= K keep every
- * token. It equals dsa_topk's except where bf16 rounding ties or reorders
- * scores.
+ * token. Against dsa_topk run on the bf16-rounded scores it is identical for
+ * W = 1; for W > 1 it keeps the same tokens above the K-th bf16 value and as
+ * many at that value, but picks among the tokens tied at it by (position in
+ * shard, shard) rather than by token index, so that pick depends on W. Against
+ * dsa_topk on the fp32 scores it also differs where bf16 rounding reorders.
  *   world   W, 1 .. 16 (shard and position must fit the word's 16 low bits)
  *   scores, score_stride, ctx_lens, topk_idx  as dsa_topk
  *   stats   int32 [B * n_q, 2] or NULL: per row the bit mask of shards that
@@ -292,9 +295,14 @@ dsa_status_t dsa_lse_combine(const dsa_params_t* params, int32_t parts, const vo
  *   allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  * - Limits: batch * n_q <= 64 and max_pages_per_req * page_size <= 1,048,576;
  *   larger problems return DSA_ERR_UNSUPPORTED and launch nothing.
- * - The first call on a device looks up the array's device address (once per
- *   device, on the current device); make that first call before any stream
- *   capture.
+ * - The first call on a device loads libdsa's device code on it (with CUDA's
+ *   default lazy module loading, this is when the array is reserved) and looks
+ *   up the array's address; that first call may allocate and synchronise.
+ *   Make it outside any real-time loop and before any stream capture: later
+ *   calls on that device allocate nothing.
+ * - The address is cached per device for the life of the process: after a
+ *   cudaDeviceReset the cached address is stale and the call must not be used
+ *   on that device again.
  * - Every call shares the array: calls whose kernels overlap on the GPU (two
  *   streams, two threads) race and give wrong results; order them. Each call
  *   clears the parts that must start at zero itself.
@@ -305,8 +313,20 @@ dsa_status_t dsa_topk_noalloc(const dsa_params_t* params, const float* scores, i
                               int32_t* phys_rows, cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
- * workspace `ws` into *code (0 = no error; DSA_DEVERR_* bits otherwise). */
+ * workspace `ws` into *code (0 = no error; DSA_DEVERR_* bits otherwise).
+ * Returns DSA_ERR_TIMEOUT (with *code written) when the word holds
+ * DSA_DEVERR_TIMEOUT: a bounded in-kernel wait gave up, the kernel unwound
+ * (no copy or MMA left in flight, tensor memory freed) and the results of the
+ * calls since the last check are unspecified; the context and the workspace
+ * stay usable. DSA_OK otherwise; DSA_ERR_CUDA if the copy fails. */
 dsa_status_t dsa_get_device_error(void* ws, cudaStream_t stream, int32_t* code);
+
+/* Diagnostics: runs the bounded-wait abort path on purpose. One warp waits on
+ * an mbarrier that nothing arrives on, gives up after `poll_limit` polls
+ * (1 <= poll_limit <= 2^20) and ORs DSA_DEVERR_TIMEOUT into the error word of
+ * `ws` (>= 4 bytes, 16-B aligned), as a pipeline kernel that timed out does.
+ * Not part of the decode path. */
+dsa_status_t dsa_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t poll_limit, cudaStream_t stream);
 
 /* Static description of a status code. */
 const char* dsa_status_string(dsa_status_t status);

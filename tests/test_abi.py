@@ -202,3 +202,12 @@ def test_prefill_world_and_rank_checked(lib):
     assert call(3, 0) == dsa.DSA_ERR_INVALID       # 64 rows are not 6 slices of whole 8-row groups
     a = list((ctypes.byref(p), 4, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 640, FAKE, need - 1, None))
     assert lib.dsa_indexer_prefill_scores(*a) == dsa.DSA_ERR_WORKSPACE
+
+
+def test_selftest_wait_timeout_arguments_checked(lib):
+    L = lib
+    assert L.dsa_selftest_wait_timeout(None, 256, 100, None) == dsa.DSA_ERR_INVALID
+    assert L.dsa_selftest_wait_timeout(FAKE + 4, 256, 100, None) == dsa.DSA_ERR_INVALID
+    assert L.dsa_selftest_wait_timeout(FAKE, 2, 100, None) == dsa.DSA_ERR_INVALID
+    assert L.dsa_selftest_wait_timeout(FAKE, 256, 0, None) == dsa.DSA_ERR_INVALID
+    assert L.dsa_selftest_wait_timeout(FAKE, 256, (1 << 20) + 1, None) == dsa.DSA_ERR_INVALID

@@ -206,3 +206,21 @@ def test_dcp_attention_equals_attention_over_the_merged_set(W):
         assert np.array_equal(idx_np[b], D.merge(scores_np[b, :L], W, 2048)["idx"])
         ro, rl = O.sparse_mla(inp, b, 0, idx_np[b])
         check_attention(bf16_to_np(out[b]), lse[b].cpu().numpy(), ro, rl)
+
+
+@pytest.mark.parametrize("W", [2, 8])
+def test_merge_against_the_bf16_top_k_with_ties_at_tau(W):
+    """Against dsa_topk's rule on the bf16-rounded scores: the same tokens above
+    the K-th bf16 value and as many at it (the choice among those follows the
+    merge's (position, shard) order)."""
+    rng = np.random.default_rng(70 + W)
+    ctx = [30000, 12000]
+    mat = (rng.integers(0, 24, (2, 30000)) * 0.0625).astype(np.float32)
+    idx, _ = _check_rows(ctx, mat, W)
+    for b, L in enumerate(ctx):
+        bv = (D.bf16_rne_bits(mat[b, :L]).astype(np.uint32) << 16).view(np.float32)
+        ref = O.topk_select(bv, 2048)
+        tau = np.sort(bv)[::-1][2047]
+        g = idx[b][idx[b] >= 0]
+        assert set(g[bv[g] > tau]) == set(ref[bv[ref] > tau])
+        assert (bv[g] == tau).sum() == (bv[ref] == tau).sum() and (bv[g] >= tau).all()
