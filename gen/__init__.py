@@ -37,10 +37,18 @@ latent values, q, plants):
   chunk from its own PCG64 stream seeded by (seed, 1 for keys / 2 for latents,
   chunk index), so that they can be filled by several threads; the main stream
   then skips them.
+* tau ties (the 64-request tie workload): after the hot plants, the token the
+  oracle ranks K-th in each request (read from a stored table that
+  gen/make_tau_ties.py writes with the oracle; the generator itself scores
+  nothing) has its key copied into 16 random positions, and into 16 more with
+  its scale one fp32 ulp up or down.
 """
 from __future__ import annotations
 
+import hashlib
+import json
 import math
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -275,6 +283,7 @@ def make_inputs(
     lat_page_pad: int = 0,
     signed_w: bool = False,
     hot_plants: bool = False,
+    tau_ties: str | None = None,
     page_size: int = PAGE_SIZE,
     topk: int = TOPK,
 ) -> DSAInputs:
@@ -285,6 +294,11 @@ def make_inputs(
     256 tokens in 32 groups of 8 whose index keys are the E4M3 codes of
     ``2 * qbar / rms(qbar)`` with ``qbar = sum_h w_h q_h`` of the request's first
     query token; the 8 keys of a group share bytes and scale (exact ties).
+    ``tau_ties`` names a stored table (``gen/tau_ties/<name>.json``) that gives,
+    per request, the token ranked K-th by the oracle after the hot plants; its
+    key bytes and scale are then copied into 16 other random positions (exact
+    ties at tau) and into 16 more with the scale moved by one fp32 ulp, up or
+    down (near ties).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     if isinstance(ctx, tuple) and ctx[0] == "uniform":
@@ -365,11 +379,54 @@ def make_inputs(
             planted.append(pos)
         meta["hot_positions"] = planted
 
+    if tau_ties:
+        assert key_fmt == "fp8"
+        table = load_tau_table(tau_ties)
+        assert len(table) == batch, "the tie table was written for another batch"
+        exact, near = [], []
+        for b in range(batch):
+            s_tau = int(table[b]["s_tau"])
+            pg, sl = bt[b, s_tau // page_size], s_tau % page_size
+            kb = key_pool[pg, sl * IDX_DIM:(sl + 1) * IDX_DIM].copy()
+            off = page_size * IDX_DIM + 4 * sl
+            sb = key_pool[pg, off:off + 4].copy()
+            if _key_digest(kb, sb) != table[b]["key_digest"]:
+                raise ValueError(f"tie table {tau_ties!r} does not match the generated keys (request {b}); "
+                                 "rewrite it with gen/make_tau_ties.py")
+            taken = {s_tau} | set(meta.get("hot_positions", [[]] * batch)[b].tolist())
+            draw = rng.choice(int(ctx_arr[b]), size=min(int(ctx_arr[b]), 128), replace=False)
+            pos = [int(x) for x in draw if int(x) not in taken][:32]
+            scale = sb.view(np.float32)[0]
+            for j, s in enumerate(pos):
+                p2, l2 = bt[b, s // page_size], s % page_size
+                key_pool[p2, l2 * IDX_DIM:(l2 + 1) * IDX_DIM] = kb
+                v = scale if j < 16 else np.nextafter(scale, np.float32(np.inf) if j % 2 else np.float32(0))
+                o2 = page_size * IDX_DIM + 4 * l2
+                key_pool[p2, o2:o2 + 4] = np.array([v], np.float32).view(np.uint8)
+            exact.append(np.array(pos[:16]))
+            near.append(np.array(pos[16:]))
+        meta["tau_token"] = [int(t["s_tau"]) for t in table]
+        meta["tau_exact"] = exact
+        meta["tau_near"] = near
+
     return DSAInputs(
         name=name, batch=batch, n_q=n_q, ctx=ctx_arr, block_table=bt, num_pages=num_pages,
         q_idx=q_idx, w=w, key_pool=key_pool, q=q, lat_pool=lat_pool, key_fmt=key_fmt,
         lat_fmt=lat_fmt, page_size=page_size, topk=topk, meta=meta,
     )
+
+
+TAU_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tau_ties")
+
+
+def _key_digest(key_bytes: np.ndarray, scale_bytes: np.ndarray) -> str:
+    return hashlib.sha256(key_bytes.tobytes() + scale_bytes.tobytes()).hexdigest()[:16]
+
+
+def load_tau_table(name: str) -> list:
+    """Per request {"s_tau": token, "key_digest": ...} from gen/tau_ties/<name>.json."""
+    with open(os.path.join(TAU_DIR, name + ".json")) as f:
+        return json.load(f)["requests"]
 
 
 # The five workloads, by what they are. Sizes follow the DSA decode shapes of the
@@ -378,7 +435,7 @@ WORKLOADS = {
     "b1_ctx4k": dict(batch=1, n_q=1, ctx=4096, seed=0, bt_mode="identity"),
     "b8_ctx32k": dict(batch=8, n_q=1, ctx=32768, seed=1, bt_mode="permuted"),
     "b64_ctx16k_128k_ties": dict(batch=64, n_q=1, ctx=("uniform", 16384, 131072), seed=2,
-                                 bt_mode="shared_shuffled", hot_plants=True),
+                                 bt_mode="shared_shuffled", hot_plants=True, tau_ties="b64_ctx16k_128k_ties"),
     "b4_ctx1m": dict(batch=4, n_q=1, ctx=1 << 20, seed=3, bt_mode="permuted"),
     "b32x6_ctx256k_fp4": dict(batch=32, n_q=6, ctx=1 << 18, seed=4, bt_mode="permuted",
                               key_fmt="mxfp4", lat_fmt="nvfp4"),
