@@ -293,7 +293,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
   uint64_t* s_free = bars + 7;     // [2]
   uint64_t* p_full = bars + 9;
   uint64_t* x_full = bars + 10;    // [2]  the peer's partial scores have landed in X
-  uint64_t* x_free = bars + 12;    // [2]  the peer has read what this CTA wrote into its X
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
 
   const int half = int(ptx::cluster_ctarank());
@@ -325,7 +324,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
       ptx::mbar_init(s_full + i, 1);
       ptx::mbar_init(s_free + i, 3);
       ptx::mbar_init(x_full + i, 1);
-      ptx::mbar_init(x_free + i, 3);
     }
     ptx::mbar_init(p_full, 3);
     // the peer's first two score tiles may arrive as soon as the pair has synced
@@ -449,8 +447,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(s_free + bk);
       // exchange partial scores with the peer CTA: asynchronous remote stores
-      // whose bytes complete on the peer's x_full[bk]
-      if (k >= 2 && !ptx::mbar_wait_cluster(x_free + bk, kph ^ 1u)) { ok = false; break; }
+      // whose bytes complete on the peer's x_full[bk]. The peer's X[bk] is free
+      // again: this CTA got here after receiving the peer's tile k - 1, which
+      // every peer thread sent after reading its row of X[bk] (tile k - 2).
       {
         const uint32_t dst = x_peer + bk * kXBuf;
         const uint32_t rbar = ptx::mapa_shared(ptx::smem_u32(x_full + bk), peer);
@@ -465,14 +464,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
         const float4 x = xr[i];
         sv[4 * i] += x.x; sv[4 * i + 1] += x.y; sv[4 * i + 2] += x.z; sv[4 * i + 3] += x.w;
       }
-      // each warp tells the peer it has read its rows; warp 0 first re-arms
-      // x_full[bk] for tile k+2 (the peer sends only after all three arrivals)
-      // (only when the peer has a tile k + 2 to send into this buffer)
-      __syncwarp();
-      if (lane == 0 && k + 2 < nt) {
-        if (warp == 0) ptx::mbar_arrive_expect_tx(x_full + bk, kXBytes);
-        ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(x_free + bk), peer));
-      }
+      // warp 0 re-arms x_full[bk] for tile k + 2 (bytes that arrive first
+      // count down until the arrival; the phase cannot complete before it)
+      if (warp == 0 && lane == 0 && k + 2 < nt) ptx::mbar_arrive_expect_tx(x_full + bk, kXBytes);
       const unsigned long long vm = vmask[k];
       float tmax = -INFINITY;
 #pragma unroll

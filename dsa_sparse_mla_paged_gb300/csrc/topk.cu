@@ -656,7 +656,9 @@ cudaError_t launch_topk(const dsa_params_t& p, const WsLayout& L, char* ws, cons
   const TopkGrid tg = topk_grid(L);
   a.chunk = tg.chunk;
   const size_t smem = std::max(size_t(tg.chunk) * 4, size_t(2 * kTkThreads + 1 + 2 * tg.ctas) * 4);
-  if (e == cudaSuccess && smem > 48 * 1024)
+  // the kernel also has static shared memory: its dynamic part needs the
+  // opt-in whenever the two together pass the default 48 KB
+  if (e == cudaSuccess)
     e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e == cudaSuccess)
     e = launch_pdl(topk_kernel, dim3(tg.ctas, L.rows), dim3(kTkThreads), smem, st, a);

@@ -143,6 +143,19 @@ def test_topk_small_k_many_rows(k):
             assert np.array_equal(idx[b], O.topk_select(mat[b, :ctx[b]], k)), (rep, b)
 
 
+def test_topk_many_rows_mid_chunks():
+    """64 rows of 16K tokens: 8K-token chunks, whose staging (32 KB) plus the
+    kernel's static shared memory pass the default 48 KB limit."""
+    ctx = [16384] * 64
+    inp = gen.make_inputs(64, 1, ctx, seed=44)
+    d = Dev(inp)
+    mat = np.random.default_rng(44).standard_normal((64, 16384)).astype(np.float32)
+    idx, _ = d.topk(mat)
+    idx = idx.cpu().numpy()
+    for b in (0, 17, 63):
+        assert np.array_equal(idx[b], O.topk_select(mat[b], 2048)), b
+
+
 def test_topk_multi_token_rows_and_phys_rows():
     import dsa_sparse_mla_paged_gb300 as dsa
 
