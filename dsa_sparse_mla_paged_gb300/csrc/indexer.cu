@@ -89,7 +89,8 @@ cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* w
 //                score = sum_h w'_h * max(scale * D_h, 0), coalesced store
 // MXFP4 keys (68 B: 128 E2M1 + one E8M0 exponent per 32) take the same MMA and
 // epilogue. The producer then bulk-copies raw page pairs into a ring of their
-// own, and warps 6..9 rewrite each token as E4M3 values k * 2^(e_b - e_max)
+// own, and four converter warps (after the epilogue warps) rewrite each token
+// as E4M3 values k * 2^(e_b - e_max)
 // (block b's exponent relative to the token's largest) plus a per-token scale
 // 2^(e_max - 127): exact whenever the token's block exponents lie within 8 of
 // one another (E4M3 reaches 2^-9), the nearest E4M3 value otherwise.
@@ -97,7 +98,7 @@ cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* w
 namespace {
 
 constexpr int kTcThreads = 192;    // FP8 keys
-constexpr int kMxThreads = 320;    // MXFP4 keys: + 4 converter warps
+constexpr int kMxConvThreads = 128;  // MXFP4 keys: 4 converter warps after the epilogue warps
 constexpr int kMxPageBytes = kPage * (kIdxDim / 2 + kIdxDim / 32);  // 4,352
 constexpr int kMxRawTile = 2 * kMxPageBytes;
 constexpr int kTileTok = 128;
@@ -268,10 +269,13 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
   return r;
 }
 
-// Several query rows with two epilogue warpgroups: the warp keeps the current
-// unit's head weights in its own shared-memory copy (wme[t][h]), read four at a
-// time by every lane, and reduces in packed pairs -- the same operations, in the
-// same order, as the scalar loop of epi_block, so the same bits.
+// Several query rows with several epilogue warpgroups: the warp keeps the
+// current unit's head weights in its own shared-memory copy (wme[t][h]), read
+// four at a time by every lane, and reduces in packed pairs -- the same
+// operations, in the same order, as the scalar loop of epi_block, so the same
+// bits. With a key scale >= 0, max(scale * d, 0) = scale * max(d, 0): the scale
+// multiplies the head sum once instead of every head (a negative or NaN scale
+// takes the per-head form).
 __device__ __forceinline__ void epi_block_wide(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
                                                int lane, TileWalk& w, EpiState& e, int& cur_b, UnitInfo& ui,
                                                float* wme) {
@@ -289,18 +293,30 @@ __device__ __forceinline__ void epi_block_wide(const IdxTc& a, const float (&v)[
   for (int g = 1; g < 4; ++g)
     if (e.g == g) scale = sc[g];
   const float4* wrow = reinterpret_cast<const float4*>(wme + e.t * kIdxHeads);
-  const unsigned long long s2 = f2_pack(scale, scale);
   unsigned long long p01 = f2_pack(0.f, 0.f), p23 = p01;  // partial sums of heads 4i + {0, 1} and 4i + {2, 3}
+  float sum;
+  if (scale >= 0.f) {
 #pragma unroll
-  for (int i = 0; i < kIdxHeads / 4; ++i) {
-    const float4 w4 = wrow[i];
-    float2 x = f2_unpack(f2_mul(s2, f2_pack(v[4 * i], v[4 * i + 1])));
-    float2 y = f2_unpack(f2_mul(s2, f2_pack(v[4 * i + 2], v[4 * i + 3])));
-    p01 = f2_fma(f2_pack(w4.x, w4.y), f2_pack(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), p01);
-    p23 = f2_fma(f2_pack(w4.z, w4.w), f2_pack(fmaxf(y.x, 0.f), fmaxf(y.y, 0.f)), p23);
+    for (int i = 0; i < kIdxHeads / 4; ++i) {
+      const float4 w4 = wrow[i];
+      p01 = f2_fma(f2_pack(w4.x, w4.y), f2_pack(fmaxf(v[4 * i], 0.f), fmaxf(v[4 * i + 1], 0.f)), p01);
+      p23 = f2_fma(f2_pack(w4.z, w4.w), f2_pack(fmaxf(v[4 * i + 2], 0.f), fmaxf(v[4 * i + 3], 0.f)), p23);
+    }
+    const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
+    sum = scale * ((a01.x + a01.y) + (a23.x + a23.y));
+  } else {
+    const unsigned long long s2 = f2_pack(scale, scale);
+#pragma unroll
+    for (int i = 0; i < kIdxHeads / 4; ++i) {
+      const float4 w4 = wrow[i];
+      float2 x = f2_unpack(f2_mul(s2, f2_pack(v[4 * i], v[4 * i + 1])));
+      float2 y = f2_unpack(f2_mul(s2, f2_pack(v[4 * i + 2], v[4 * i + 3])));
+      p01 = f2_fma(f2_pack(w4.x, w4.y), f2_pack(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), p01);
+      p23 = f2_fma(f2_pack(w4.z, w4.w), f2_pack(fmaxf(y.x, 0.f), fmaxf(y.y, 0.f)), p23);
+    }
+    const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
+    sum = (a01.x + a01.y) + (a23.x + a23.y);
   }
-  const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
-  const float sum = (a01.x + a01.y) + (a23.x + a23.y);
   epi_store(a, sum, rowt, lane, w, e, ui);
 }
 
@@ -334,16 +350,20 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
   // four independent partial sums (heads h = 4i + j), added pairwise: a short
   // dependency chain per block. One query row: every thread holds all 32 head
   // weights; several rows: lane h holds w'_h of each row and shares it.
+  // (a key scale >= 0 leaves the head sum: max(scale * d, 0) = scale * max(d, 0))
   float part[4] = {0.f, 0.f, 0.f, 0.f};
+  const bool factor = scale >= 0.f;
+  const float hs = factor ? 1.f : scale;
   if (a.n_q == 1) {
 #pragma unroll
-    for (int h = 0; h < kIdxHeads; ++h) part[h & 3] = fmaf(wr[h], fmaxf(scale * v[h], 0.f), part[h & 3]);
+    for (int h = 0; h < kIdxHeads; ++h) part[h & 3] = fmaf(wr[h], fmaxf(hs * v[h], 0.f), part[h & 3]);
   } else {
 #pragma unroll
     for (int h = 0; h < kIdxHeads; ++h)
-      part[h & 3] = fmaf(__shfl_sync(0xffffffffu, wt, h), fmaxf(scale * v[h], 0.f), part[h & 3]);
+      part[h & 3] = fmaf(__shfl_sync(0xffffffffu, wt, h), fmaxf(hs * v[h], 0.f), part[h & 3]);
   }
-  const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+  const float hsum = (part[0] + part[1]) + (part[2] + part[3]);
+  const float sum = factor ? scale * hsum : hsum;
   epi_store(a, sum, rowt, lane, w, e, ui);
 }
 
@@ -394,9 +414,8 @@ __device__ __forceinline__ void mx_convert_row(const uint8_t* vals, uint32_t e4,
 // is bound by HBM; 2 when a unit has several rows (decode with n_q > 1,
 // prefill), where the reduction of 32 x rows columns per token is the work.
 template <bool kMx, int kEwg>
-__global__ void __launch_bounds__(kMx ? kMxThreads : 64 + 128 * kEwg, (kMx || kEwg > 1) ? 1 : 2)
+__global__ void __launch_bounds__(64 + 128 * kEwg + (kMx ? kMxConvThreads : 0), (kMx || kEwg > 1) ? 1 : 2)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, IdxTc a) {
-  static_assert(!kMx || kEwg == 1, "the MXFP4 kernel's warps 6..9 convert keys");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages, NA = a.nacc, G = a.group;
@@ -596,10 +615,10 @@ __global__ void __launch_bounds__(kMx ? kMxThreads : 64 + 128 * kEwg, (kMx || kE
           if (++acc == NA) { acc = 0; aph ^= 1u; }
         }
       }
-    } else if (kMx && warp >= 6) {
+    } else if (kMx && warp >= 2 + 4 * kEwg) {
       // ------------------------------------------------------------ MXFP4 converters
       // thread ct rewrites token row ct of every tile (page ct / 64, slot ct % 64)
-      const int ct = threadIdx.x - 192;
+      const int ct = threadIdx.x - (64 + 128 * kEwg);
       const int half = ct >> 6, slot = ct & 63;
       int rs = 0, s = 0, g = 0;
       uint32_t rph = 0, ph = 0;
@@ -788,7 +807,9 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   while (cols < a.nacc * slot_cols) cols <<= 1;
   a.tmem_cols = cols;
   const size_t stage_bytes = size_t(a.group) * (kKeyTileBytes + kScaleTileBytes);
-  const bool wide = !mx && gsz > 1;  // two epilogue warpgroups
+  // several query rows: more epilogue warpgroups (three with FP8 keys, two
+  // beside the MXFP4 converters), whose weights are staged in shared memory
+  const bool wide = gsz > 1;
   const size_t fixed = 1024 + 2 * size_t(gsz) * kIdxHeads * kIdxDim + 512 +
                        (wide ? size_t(12) * kMaxNQ * kIdxHeads * 4 : 0);
   const size_t budget = (cps == 2 ? 113 * 1024 : 227 * 1024) - fixed;
@@ -802,7 +823,8 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   }
   a.err = err;
   const size_t smem = fixed + size_t(a.stages) * stage_bytes + size_t(a.raw_slots) * kMxRawTile;
-  const void* fn = mx ? reinterpret_cast<const void*>(indexer_tc_kernel<true, 1>)
+  const void* fn = mx ? (wide ? reinterpret_cast<const void*>(indexer_tc_kernel<true, 2>)
+                             : reinterpret_cast<const void*>(indexer_tc_kernel<true, 1>))
                  : wide ? reinterpret_cast<const void*>(indexer_tc_kernel<false, 3>)
                         : reinterpret_cast<const void*>(indexer_tc_kernel<false, 1>);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
@@ -810,7 +832,9 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   // enough tiles for every SM is the common case; with fewer, one CTA per tile
   const long long max_tiles = (long long)a.units * ((L.cap + kTileTok - 1) / kTileTok);
   const int grid = int(std::min<long long>(cps * sm_count(), std::max<long long>(1, max_tiles)));
-  if (mx) return launch_pdl(indexer_tc_kernel<true, 1>, dim3(grid), dim3(kMxThreads), smem, st, kmap, qmap, a);
+  if (mx && wide)
+    return launch_pdl(indexer_tc_kernel<true, 2>, dim3(grid), dim3(64 + 256 + kMxConvThreads), smem, st, kmap, qmap, a);
+  if (mx) return launch_pdl(indexer_tc_kernel<true, 1>, dim3(grid), dim3(64 + 128 + kMxConvThreads), smem, st, kmap, qmap, a);
   if (wide) return launch_pdl(indexer_tc_kernel<false, 3>, dim3(grid), dim3(64 + 384), smem, st, kmap, qmap, a);
   return launch_pdl(indexer_tc_kernel<false, 1>, dim3(grid), dim3(kTcThreads), smem, st, kmap, qmap, a);
 }
