@@ -90,10 +90,11 @@ cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* w
 // MXFP4 keys (68 B: 128 E2M1 + one E8M0 exponent per 32) take the same MMA and
 // epilogue. The producer then bulk-copies raw page pairs into a ring of their
 // own, and four converter warps (after the epilogue warps) rewrite each token
-// as E4M3 values k * 2^(e_b - e_max)
-// (block b's exponent relative to the token's largest) plus a per-token scale
-// 2^(e_max - 127): exact whenever the token's block exponents lie within 8 of
-// one another (E4M3 reaches 2^-9), the nearest E4M3 value otherwise.
+// as E4M3 values k * 2^(6 + e_b - e_max) (the token's largest block lands in
+// [32, 384], below E4M3's 448) plus a per-token scale 2^(e_max - 133): exact
+// whenever the token's block exponents lie within 14 of one another (E4M3
+// reaches 2^-9); beyond that a small block's values round to the nearest
+// multiple of 2^-9, an error of at most 2^-10 x 2^(e_max - 133) per key value.
 // ---------------------------------------------------------------------------
 namespace {
 
@@ -369,18 +370,20 @@ __device__ __forceinline__ void epi_block(const IdxTc& a, const float (&v)[32], 
 
 
 // One MXFP4 token (64 B of E2M1 pairs, element 2i in the low nibble; 4 E8M0
-// exponents) -> 128 E4M3 values into its 128-B swizzled row, and its scale.
+// exponents) -> 128 E4M3 values v * 2^(6 + e_b - e_max) into its 128-B swizzled
+// row, and its scale 2^(e_max - 133).
 __device__ __forceinline__ void mx_convert_row(const uint8_t* vals, uint32_t e4, uint8_t* row, int r, float* scale) {
   const uint32_t e0 = e4 & 0xFFu, e1 = (e4 >> 8) & 0xFFu, e2 = (e4 >> 16) & 0xFFu, e3 = e4 >> 24;
   const uint32_t emax = max(max(e0, e1), max(e2, e3));
-  *scale = emax == 0u ? __uint_as_float(0x00400000u) : emax == 255u ? __uint_as_float(0x7FC00000u)
-                                                                    : __uint_as_float(emax << 23);
+  // 2^(emax - 133): an fp32 normal for emax >= 7, a subnormal (bit emax + 16) below
+  *scale = emax == 255u ? __uint_as_float(0x7FC00000u)
+                        : emax >= 7u ? __uint_as_float((emax - 6u) << 23) : __uint_as_float(1u << (emax + 16u));
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
     const uint32_t eb = (e4 >> (8 * b)) & 0xFFu;
-    const uint32_t d = emax - eb;  // 2^-d as f16 (exact down to 2^-24, zero below)
-    const unsigned short mbits = d <= 14u ? (unsigned short)((15u - d) << 10)
-                                 : d <= 24u ? (unsigned short)(1u << (24u - d)) : (unsigned short)0;
+    const uint32_t d = emax - eb;  // 2^(6 - d) as f16 (normal to d = 20, subnormal to d = 30, zero below)
+    const unsigned short mbits = d <= 20u ? (unsigned short)((21u - d) << 10)
+                                 : d <= 30u ? (unsigned short)(1u << (30u - d)) : (unsigned short)0;
     const __half2 m2 = __halves2half2(__ushort_as_half(mbits), __ushort_as_half(mbits));
     const uint4 v = *reinterpret_cast<const uint4*>(vals + 16 * b);
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};

@@ -552,10 +552,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
 }
 
 // LSE merge of the splits of one row: out = sum_i e^{lse_i - lse} O_i, lse = ln sum_i e^{lse_i}.
-// One CTA per (row, 2 heads): 128 threads per head, 4 dims each. In every warp
+// One CTA per (row, 3 heads): 128 threads per head, 4 dims each (32 CTAs a
+// row: a batch of 4 rows is one wave). In every warp
 // lane i < splits holds split i's lse, so the weights come from two shuffle
 // reductions; every split's partial row is read at once.
-constexpr int kCombThreads = 256;
+constexpr int kCombThreads = 384;
 constexpr int kCombHeads = kCombThreads / 128;
 
 __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* __restrict__ opart,

@@ -131,8 +131,10 @@ dsa_status_t dsa_workspace_size(const dsa_params_t* params, size_t* bytes);
  * for s < L_{b,t}; entries s >= L_{b,t} are left untouched. The key k_s is
  * E4M3(k) * scale_s (DSA_KEY_FP8_132) or E2M1(k) * 2^(e_blk - 127) with one
  * E8M0 exponent e_blk per 32 values (DSA_KEY_MXFP4_68, section "量化：原生 MXFP4
- * 索引器"); exact while a token's four exponents lie within 8 of each other,
- * the nearest E4M3 rewrite of the smaller blocks beyond that.
+ * 索引器"); exact while a token's four exponents lie within 14 of each other;
+ * beyond that each value of a block more than 14 below the token's largest is
+ * off by at most 2^(e_max - 143) (it is scored as the nearest multiple of 2^-9
+ * of 2^(e_max - 133)).
  *   q_idx  bf16 [B, n_q, idx_heads, idx_dim]      (16-B aligned)
  *   w      fp32 [B, n_q, idx_heads]
  *   key_pool   num_pages pages of key_page_stride bytes (16-B aligned)
