@@ -445,6 +445,10 @@ WORKLOADS = {
     # small cases for kernel profiles: each kernel's own inputs still exceed the 129 MB L2
     "b4_ctx256k": dict(batch=4, n_q=1, ctx=1 << 18, seed=5, bt_mode="permuted"),
     "b64_ctx16k": dict(batch=64, n_q=1, ctx=1 << 14, seed=6, bt_mode="permuted"),
+    # six-row scorer cases (keys above L2): FP8 and MXFP4 keys
+    "b8x6_ctx256k": dict(batch=8, n_q=6, ctx=1 << 18, seed=9, bt_mode="permuted"),
+    "b8x6_ctx256k_fp4": dict(batch=8, n_q=6, ctx=1 << 18, seed=10, bt_mode="permuted", key_fmt="mxfp4",
+                             lat_fmt="nvfp4"),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
