@@ -9,6 +9,8 @@
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "dsa_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -17,7 +19,13 @@ namespace dsa {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Tensor-core split-KV attention (sm_103a), one 2-CTA cluster per (row, split).
+// Tensor-core split-KV attention (sm_103a) on 2-CTA clusters. A work unit is
+// one (row, split): kSplitTok consecutive slots of the row's top-k list. Each
+// cluster takes a contiguous run of units in (row, split) order, keeps the
+// query while the row does not change, and streams the units' 64-token tiles
+// through one pipeline: tile indices, barrier phases and the score exchange
+// run on across unit boundaries, so a unit's epilogue overlaps the next unit's
+// gathers and QK^T. (A batch of a few rows gets one unit per cluster.)
 //
 // A 96-head x 512-dim fp32 output needs all 512 TMEM columns, so the pair
 // splits the work by latent dims: CTA c owns nope dims [256c, 256c+256) (its
@@ -31,9 +39,14 @@ namespace {
 //               base 2 with lazy rescale of O (when the max grows by > 2^8)
 //   warp  3     TMEM owner, Q by TMA, MMA issuer (QK^T of tile k+1 is issued
 //               before PV of tile k, so it overlaps the softmax)
-//   warps 4..7  converters: gather the split's selected latent rows (paged,
-//               16-B loads one tile ahead) and expand this CTA's dims E4M3 ->
-//               bf16 exactly into a 128-B swizzled K-major tile (2 buffers)
+//   warps 4..7  converters: resolve each unit's selected slots to latent rows
+//               (four buffers, by unit), gather the rows (paged, 16-B loads one
+//               tile ahead) and expand this CTA's dims E4M3 -> bf16 exactly
+//               into a 128-B swizzled K-major tile (2 buffers)
+// The epilogue stages O / l per warp as 32 x 32 swizzled tiles and writes the
+// split partials with TMA stores (the tile buffers belong to the next unit);
+// a cluster's last unit stages whole rows in the freed tile buffers instead and
+// writes them with one 1-KB bulk store per head.
 // ---------------------------------------------------------------------------
 constexpr int kNT = 64;                     // tokens per tile
 constexpr int kQBlk = kHeads * 128;         // 12,288 B per Q K-block (96 rows of 64 bf16)
@@ -49,10 +62,13 @@ constexpr int kTcMlaThreads = 256;
 constexpr uint32_t kSCol = 256;             // score tiles at TMEM columns [256, 384)
 constexpr int kSplitTiles = kSplitTok / kNT;
 constexpr int kNumBars = 16;
-constexpr int kORow = 256 * 4 + 16;         // staged output row (+16 B against bank conflicts)
+constexpr int kUnitBufs = 4;                // row-address buffers, by unit
+constexpr int kStage = 32 * 128;            // one softmax warp's 32 x 32 fp32 output tile
+constexpr int kORow = 256 * 4 + 16;         // a head's output row staged in the free tile buffers
 static_assert(kHeads * kORow <= 2 * kLatBuf + kPBytes + 2 * kXBuf, "output staging overlaps the tile buffers");
-constexpr size_t kTcMlaSmem =
-    1024 + kQBytes + 2 * kLatBuf + kPBytes + 2 * kXBuf + kSplitTok * 8 + kSplitTiles * 8 + kNumBars * 8 + 16;
+constexpr size_t kTcMlaSmem = 1024 + kQBytes + 2 * kLatBuf + kPBytes + 2 * kXBuf + 3 * kStage +
+                              kUnitBufs * (kSplitTok * 8 + kSplitTiles * 8) + kNumBars * 8 + 16;
+static_assert(kTcMlaSmem <= 232448, "shared memory of one CTA");
 
 struct MlaTc {
   const int32_t* block_table;
@@ -61,7 +77,7 @@ struct MlaTc {
   const uint8_t* lat_pool;
   int64_t lat_stride;
   int lat_row, lat_nvfp4;  // bytes per latent row; 1 for the NVFP4 row format
-  int max_pages, num_pages, n_q, cap, K, splits, per_split;
+  int max_pages, num_pages, n_q, cap, K, splits, per_split, rows;
   float sm_scale_log2, lat_scale;
   float* opart;
   float* lpart;
@@ -117,7 +133,7 @@ __device__ __forceinline__ void conv_load(uint4 (&buf)[NPC / 2], const uint8_t* 
   }
 }
 
-// Expand tile k into LAT[k & 1] once the tile that last used that buffer is done.
+// Expand stream tile k into LAT[k & 1] once the tile that last used that buffer is done.
 template <int NPC>
 __device__ __forceinline__ bool conv_store(const uint4 (&buf)[NPC / 2], const MlaTc& a, int ct, int lane, int k,
                                            uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free) {
@@ -144,19 +160,20 @@ __device__ __forceinline__ bool conv_store(const uint4 (&buf)[NPC / 2], const Ml
   return ok;
 }
 
-// Converter warps (128 threads): tiles 0..nt-1 into LAT[k & 1], the loads of
-// tile k+1 in flight while tile k waits for its buffer and is expanded.
+// Converter warps (128 threads): a unit's tiles 0..nt-1 (stream tiles g0 + k)
+// into LAT[(g0 + k) & 1], the loads of tile k+1 in flight while tile k waits
+// for its buffer and is expanded.
 template <int NPC>
-__device__ void converter_role(const MlaTc& a, int ct, int lane, int nt, const uint8_t* const* rowptr,
+__device__ void converter_role(const MlaTc& a, int ct, int lane, int nt, int g0, const uint8_t* const* rowptr,
                                uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free, bool& ok) {
   uint4 bufa[NPC / 2], bufb[NPC / 2];
   conv_load<NPC>(bufa, rowptr, ct, 0);
   for (int k = 0; k < nt; k += 2) {
     if (k + 1 < nt) conv_load<NPC>(bufb, rowptr, ct, k + 1);
-    if (!conv_store<NPC>(bufa, a, ct, lane, k, LAT, lat_full, lat_free)) { ok = false; return; }
+    if (!conv_store<NPC>(bufa, a, ct, lane, g0 + k, LAT, lat_full, lat_free)) { ok = false; return; }
     if (k + 1 >= nt) break;
     if (k + 2 < nt) conv_load<NPC>(bufa, rowptr, ct, k + 2);
-    if (!conv_store<NPC>(bufb, a, ct, lane, k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
+    if (!conv_store<NPC>(bufb, a, ct, lane, g0 + k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
   }
 }
 
@@ -262,30 +279,35 @@ __device__ __forceinline__ bool conv_store_nv(const NvUnit (&buf)[NvUnits<HALF>:
 }
 
 template <int HALF>
-__device__ void converter_role_nv(const MlaTc& a, int ct, int lane, int nt, const uint8_t* const* rowptr,
+__device__ void converter_role_nv(const MlaTc& a, int ct, int lane, int nt, int g0, const uint8_t* const* rowptr,
                                   uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free, bool& ok) {
   NvUnit bufa[NvUnits<HALF>::kPerThread], bufb[NvUnits<HALF>::kPerThread];
   conv_load_nv<HALF>(bufa, rowptr, ct, 0);
   for (int k = 0; k < nt; k += 2) {
     if (k + 1 < nt) conv_load_nv<HALF>(bufb, rowptr, ct, k + 1);
-    if (!conv_store_nv<HALF>(bufa, a, ct, lane, k, LAT, lat_full, lat_free)) { ok = false; return; }
+    if (!conv_store_nv<HALF>(bufa, a, ct, lane, g0 + k, LAT, lat_full, lat_free)) { ok = false; return; }
     if (k + 1 >= nt) break;
     if (k + 2 < nt) conv_load_nv<HALF>(bufa, rowptr, ct, k + 2);
-    if (!conv_store_nv<HALF>(bufb, a, ct, lane, k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
+    if (!conv_store_nv<HALF>(bufb, a, ct, lane, g0 + k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
   }
 }
 
+// kNv: NVFP4 latent rows (else FP8); one converter kind per instance keeps the
+// registers of the other out of the unit loop.
+template <bool kNv>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
-    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, MlaTc a) {
+    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                         MlaTc a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = sm;
   uint8_t* LAT = Qs + kQBytes;                     // 2 buffers
   uint8_t* Ps = LAT + 2 * kLatBuf;
   uint8_t* X = Ps + kPBytes;                       // 2 buffers: the peer's partial scores
-  const uint8_t** rowptr = reinterpret_cast<const uint8_t**>(X + 2 * kXBuf);          // [kSplitTok]
-  unsigned long long* vmask = reinterpret_cast<unsigned long long*>(rowptr + kSplitTok);  // [kSplitTiles]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(vmask + kSplitTiles);
+  uint8_t* ST = X + 2 * kXBuf;                     // 3 output staging tiles (1024-B aligned)
+  const uint8_t** rowptr = reinterpret_cast<const uint8_t**>(ST + 3 * kStage);                 // [4][kSplitTok]
+  unsigned long long* vmask = reinterpret_cast<unsigned long long*>(rowptr + kUnitBufs * kSplitTok);  // [4][tiles]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(vmask + kUnitBufs * kSplitTiles);
   uint64_t* q_full = bars + 0;
   uint64_t* lat_full = bars + 1;   // [2]
   uint64_t* lat_free = bars + 3;   // [2]  (PV of the buffer's last tile done)
@@ -293,31 +315,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
   uint64_t* s_free = bars + 7;     // [2]
   uint64_t* p_full = bars + 9;
   uint64_t* x_full = bars + 10;    // [2]  the peer's partial scores have landed in X
+  uint64_t* q_free = bars + 12;    // every MMA on the current query done (before a new one lands)
+  uint64_t* mma_done = bars + 13;  // every MMA issued has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
 
   const int half = int(ptx::cluster_ctarank());
   const int peer = half ^ 1;
-  const int split = blockIdx.x >> 1, r = blockIdx.y;
-  const int b = r / a.n_q, t = r - b * a.n_q;
-  const int j0 = split * a.per_split;
-  const int j1 = min(a.K, j0 + a.per_split);
-  const int nt = j1 > j0 ? (j1 - j0 + kNT - 1) / kNT : 0;
-  const int nkb = half == 0 ? 5 : 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* op = a.opart + (size_t(r) * a.splits + split) * kHeads * kDNope + half * 256;
-  float* lp = a.lpart + (size_t(r) * a.splits + split) * kHeads;
-
-  if (nt == 0) {  // a split past the top-k list (both CTAs of the pair return here)
-    pdl_wait();
-    pdl_trigger();
-    for (int i = threadIdx.x; i < kHeads * 256; i += blockDim.x) op[(i >> 8) * kDNope + (i & 255)] = 0.f;
-    if (half == 0)
-      for (int i = threadIdx.x; i < kHeads; i += blockDim.x) lp[i] = -INFINITY;
-    return;
-  }
+  const int nkb = half == 0 ? 5 : 4;
+  // this cluster's units [u0, u1) of rows * splits, and its total tiles (all
+  // units of a call have ceil(min(K - j0, kSplitTok) / 64) tiles by split)
+  const int U = a.rows * a.splits;
+  const int nclu = int(gridDim.x) >> 1, clu = int(blockIdx.x) >> 1;
+  const int u0 = int(int64_t(clu) * U / nclu), u1 = int(int64_t(clu + 1) * U / nclu);
+  auto unit_tiles = [&](int u) {
+    const int j0 = (u % a.splits) * a.per_split;
+    const int j1 = min(a.K, j0 + a.per_split);
+    return (j1 - j0 + kNT - 1) / kNT;
+  };
+  int gtot = 0;
+  for (int u = u0; u < u1; ++u) gtot += unit_tiles(u);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_free, 1);
+    ptx::mbar_init(mma_done, 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(lat_full + i, 4);
       ptx::mbar_init(lat_free + i, 1);
@@ -327,8 +349,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
     }
     ptx::mbar_init(p_full, 3);
     // the peer's first two score tiles may arrive as soon as the pair has synced
-    ptx::mbar_arrive_expect_tx(x_full + 0, kXBytes);
-    ptx::mbar_arrive_expect_tx(x_full + 1, kXBytes);
+    if (gtot > 0) ptx::mbar_arrive_expect_tx(x_full + 0, kXBytes);
+    if (gtot > 1) ptx::mbar_arrive_expect_tx(x_full + 1, kXBytes);
     ptx::fence_mbar_init();
   }
   if (warp == 3) {
@@ -341,205 +363,286 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
-  // this CTA's K-blocks of the query (rows r * 96 ..): CTA 0 nope 0..3 and the rope, CTA 1 nope 4..7
-  auto issue_q = [&]() {
+  // this CTA's K-blocks of the query of row r: CTA 0 nope 0..3 and the rope, CTA 1 nope 4..7
+  auto issue_q = [&](int r) {
     ptx::mbar_arrive_expect_tx(q_full, nkb * kQBlk);
     for (int kl = 0; kl < nkb; ++kl) {
       const int kbg = half == 0 ? (kl < 4 ? kl : 8) : 4 + kl;
       ptx::tma_load_2d(Qs + kl * kQBlk, &qmap, q_full, kbg * 64, r * kHeads);
     }
   };
-  if (a.early && warp == 3 && lane == 0) issue_q();
+  int q_row = -1;
+  bool q_pending = false;
+  if (a.early && warp == 3 && lane == 0 && u0 < u1) {
+    q_row = u0 / a.splits;
+    issue_q(q_row);
+    q_pending = true;
+  }
   // everything above is on-chip set-up or a read of the caller's query; what
   // comes next reads the top-k list of the previous kernel
   pdl_wait();
   pdl_trigger();  // the split combine may take free SMs now (it waits for this grid)
-  const int ctx = a.ctx_lens[b];
-  const int L = (ctx < a.n_q || ctx > a.cap) ? 0 : ctx - a.n_q + t + 1;
 
   if (warp == 3) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      if (!a.early) issue_q();
-      if (!ptx::mbar_wait(q_full, 0)) ok = false;
       const uint32_t id_qk = ptx::idesc(1, 1, 128, kNT);
       const uint32_t id_pv = ptx::idesc(1, 1, 128, 256, 0, 1);
       const uint32_t q0 = ptx::smem_u32(Qs), l0 = ptx::smem_u32(LAT), p0 = ptx::smem_u32(Ps);
-      auto pv = [&](int j) {
+      int g = 0, qn = 0, qf = 0, last_k = 0;
+      // PV of stream tile j, the kj-th of its unit: O (+)= P . V[j & 1]
+      auto pv = [&](int j, int kj) {
         if (!ok || !ptx::mbar_wait(p_full, uint32_t(j) & 1u)) { ok = false; return; }
         ptx::tc_fence_after();
         const uint32_t lat = l0 + (j & 1) * kLatBuf;
 #pragma unroll
         for (int kk = 0; kk < kNT / 16; ++kk)
           ptx::mma_f16(tmem, ptx::sdesc_sw128(p0 + kk * 32), ptx::sdesc_sw128_mn(lat + kk * 16 * 128, kLBlk, 1024),
-                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                       id_pv, (kj > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(lat_free + (j & 1));
       };
-      for (int k = 0; k < nt && ok; ++k) {
-        const int bk = k & 1;
-        const uint32_t kph = uint32_t(k >> 1) & 1u;
-        if (!ptx::mbar_wait(lat_full + bk, kph)) { ok = false; break; }
-        if (k >= 2 && !ptx::mbar_wait(s_free + bk, kph ^ 1u)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t lat = l0 + bk * kLatBuf;
-        for (int kl = 0; kl < nkb; ++kl)
+      for (int u = u0; u < u1 && ok; ++u) {
+        const int r = u / a.splits, nt = unit_tiles(u);
+        for (int k = 0; k < nt && ok; ++k, ++g) {
+          // at a unit boundary the previous unit's last PV goes first, so that
+          // its epilogue never waits for a query reload
+          if (k == 0 && g >= 1) pv(g - 1, last_k);
+          if (k == 0 && r != q_row) {
+            if (q_row >= 0) {  // every MMA reading the old query is done before it is overwritten
+              ptx::mma_commit(q_free);
+              if (!ptx::mbar_wait(q_free, uint32_t(qf++) & 1u)) { ok = false; break; }
+            }
+            issue_q(r);
+            q_row = r;
+            q_pending = true;
+          }
+          if (q_pending) {
+            if (!ptx::mbar_wait(q_full, uint32_t(qn++) & 1u)) { ok = false; break; }
+            q_pending = false;
+          }
+          const int bk = g & 1;
+          const uint32_t kph = uint32_t(g >> 1) & 1u;
+          if (!ptx::mbar_wait(lat_full + bk, kph)) { ok = false; break; }
+          if (g >= 2 && !ptx::mbar_wait(s_free + bk, kph ^ 1u)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t lat = l0 + bk * kLatBuf;
+          for (int kl = 0; kl < nkb; ++kl)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_f16(tmem + kSCol + bk * kNT, ptx::sdesc_sw128(q0 + kl * kQBlk + kk * 32),
-                         ptx::sdesc_sw128(lat + kl * kLBlk + kk * 32), id_qk, (kl | kk) ? 1u : 0u);
-        ptx::mma_commit(s_full + bk);
-        if (k >= 1) pv(k - 1);
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_f16(tmem + kSCol + bk * kNT, ptx::sdesc_sw128(q0 + kl * kQBlk + kk * 32),
+                           ptx::sdesc_sw128(lat + kl * kLBlk + kk * 32), id_qk, (kl | kk) ? 1u : 0u);
+          ptx::mma_commit(s_full + bk);
+          if (k >= 1) pv(g - 1, k - 1);
+          last_k = k;
+        }
       }
-      if (ok) pv(nt - 1);
+      if (ok && g >= 1) pv(g - 1, last_k);
+      // nothing of this thread's left in flight when TMEM is released
+      ptx::mma_commit(mma_done);
+      ptx::mbar_wait(mma_done, 0);
+      if (q_pending) ptx::mbar_wait(q_full, uint32_t(qn) & 1u);
     }
+    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ converters
     const int ct = threadIdx.x - 128;
-    // Resolve every selected slot of the split once (slot -> page -> row address);
-    // the loads are independent, so their latency overlaps the Q copy.
-    for (int jj = ct; jj < nt * kNT; jj += 128) {
-      const int j = j0 + jj;
-      const uint8_t* rp = nullptr;
-      if (j < j1) {
-        const int sidx = a.topk_idx[size_t(r) * a.K + j];
-        if (sidx >= 0 && sidx < L) {
-          const int pg = a.block_table[size_t(b) * a.max_pages + sidx / kPage];
-          if (pg >= 0 && pg < a.num_pages)
-            rp = a.lat_pool + size_t(pg) * a.lat_stride + size_t(sidx % kPage) * a.lat_row;
-          else if (half == 0)
-            atomicOr(a.err, DSA_DEVERR_BLOCK_TABLE);
-        } else if (sidx != -1 && half == 0) {
-          atomicOr(a.err, DSA_DEVERR_TOPK_INDEX);
+    int g = 0;
+    for (int u = u0, ui = 0; u < u1 && ok; ++u, ++ui) {
+      const int r = u / a.splits, split = u % a.splits, nt = unit_tiles(u);
+      const int b = r / a.n_q, t = r - b * a.n_q;
+      const int j0 = split * a.per_split, j1 = min(a.K, j0 + a.per_split);
+      const int ctx = a.ctx_lens[b];
+      const int L = (ctx < a.n_q || ctx > a.cap) ? 0 : ctx - a.n_q + t + 1;
+      const uint8_t** rp = rowptr + (ui % kUnitBufs) * kSplitTok;
+      unsigned long long* vm = vmask + (ui % kUnitBufs) * kSplitTiles;
+      // Resolve every selected slot of the unit once (slot -> page -> row address).
+      // The buffer was last used by unit ui - 4, whose tiles are all past PV
+      // (the converters' own buffer waits ordered them), so it is free.
+      for (int jj = ct; jj < nt * kNT; jj += 128) {
+        const int j = j0 + jj;
+        const uint8_t* p = nullptr;
+        if (j < j1) {
+          const int sidx = a.topk_idx[size_t(r) * a.K + j];
+          if (sidx >= 0 && sidx < L) {
+            const int pg = a.block_table[size_t(b) * a.max_pages + sidx / kPage];
+            if (pg >= 0 && pg < a.num_pages)
+              p = a.lat_pool + size_t(pg) * a.lat_stride + size_t(sidx % kPage) * a.lat_row;
+            else if (half == 0)
+              atomicOr(a.err, DSA_DEVERR_BLOCK_TABLE);
+          } else if (sidx != -1 && half == 0) {
+            atomicOr(a.err, DSA_DEVERR_TOPK_INDEX);
+          }
         }
+        rp[jj] = p;
+        const unsigned m = __ballot_sync(0xffffffffu, p != nullptr);
+        if (lane == 0) reinterpret_cast<uint32_t*>(vm)[jj >> 5] = m;
       }
-      rowptr[jj] = rp;
-      const unsigned m = __ballot_sync(0xffffffffu, rp != nullptr);
-      if (lane == 0) reinterpret_cast<uint32_t*>(vmask)[jj >> 5] = m;
-    }
-    ptx::named_bar_sync(1, 128);
-    if (a.lat_nvfp4) {
-      if (half == 0)
-        converter_role_nv<0>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
-      else
-        converter_role_nv<1>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
-    } else if (half == 0) {
-      converter_role<20>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
-    } else {
-      converter_role<16>(a, ct, lane, nt, rowptr, LAT, lat_full, lat_free, ok);
+      ptx::named_bar_sync(1, 128);
+      if constexpr (kNv) {
+        if (half == 0)
+          converter_role_nv<0>(a, ct, lane, nt, g, rp, LAT, lat_full, lat_free, ok);
+        else
+          converter_role_nv<1>(a, ct, lane, nt, g, rp, LAT, lat_full, lat_free, ok);
+      } else if (half == 0) {
+        converter_role<20>(a, ct, lane, nt, g, rp, LAT, lat_full, lat_free, ok);
+      } else {
+        converter_role<16>(a, ct, lane, nt, g, rp, LAT, lat_full, lat_free, ok);
+      }
+      g += nt;
     }
   } else if (warp < 3) {
     // ------------------------------------------------------------ softmax / epilogue
     const int h = warp * 32 + lane;
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
-    float m_use = -INFINITY, l = 0.f;
     const uint32_t x_mine = ptx::smem_u32(X) + h * kXRow;
     const uint32_t x_peer = ptx::mapa_shared(x_mine, peer);
-    for (int k = 0; k < nt; ++k) {
-      const int bk = k & 1;
-      const uint32_t kph = uint32_t(k >> 1) & 1u;
-      // lat_full orders the converters' validity mask before this read
-      if (!ptx::mbar_wait(lat_full + bk, kph) || !ptx::mbar_wait(s_full + bk, kph)) { ok = false; break; }
+    uint8_t* stg = ST + warp * kStage;
+    int g = 0;
+    for (int u = u0, ui = 0; u < u1 && ok; ++u, ++ui) {
+      const int r = u / a.splits, split = u % a.splits, nt = unit_tiles(u);
+      const unsigned long long* vmu = vmask + (ui % kUnitBufs) * kSplitTiles;
+      float m_use = -INFINITY, l = 0.f;
+      for (int k = 0; k < nt; ++k, ++g) {
+        const int bk = g & 1;
+        const uint32_t kph = uint32_t(g >> 1) & 1u;
+        // lat_full orders the converters' validity mask before this read
+        if (!ptx::mbar_wait(lat_full + bk, kph) || !ptx::mbar_wait(s_full + bk, kph)) { ok = false; break; }
+        ptx::tc_fence_after();
+        float sv[64];
+        ptx::tmem_ld32(tmem + lane_base + kSCol + bk * kNT, *reinterpret_cast<float(*)[32]>(&sv[0]));
+        ptx::tmem_ld32(tmem + lane_base + kSCol + bk * kNT + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(s_free + bk);
+        // exchange partial scores with the peer CTA: asynchronous remote stores
+        // whose bytes complete on the peer's x_full[bk]. The peer's X[bk] is free
+        // again: this CTA got here after receiving the peer's tile g - 1, which
+        // every peer thread sent after reading its row of X[bk] (tile g - 2).
+        {
+          const uint32_t dst = x_peer + bk * kXBuf;
+          const uint32_t rbar = ptx::mapa_shared(ptx::smem_u32(x_full + bk), peer);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            ptx::st_async_f4(dst + i * 16, make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), rbar);
+        }
+        if (!ptx::mbar_wait_cluster(x_full + bk, kph)) { ok = false; break; }
+        const float4* xr = reinterpret_cast<const float4*>(X + bk * kXBuf + h * kXRow);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 x = xr[i];
+          sv[4 * i] += x.x; sv[4 * i + 1] += x.y; sv[4 * i + 2] += x.z; sv[4 * i + 3] += x.w;
+        }
+        // warp 0 re-arms x_full[bk] for stream tile g + 2 (bytes that arrive
+        // first count down until the arrival; the phase cannot complete before it)
+        if (warp == 0 && lane == 0 && g + 2 < gtot) ptx::mbar_arrive_expect_tx(x_full + bk, kXBytes);
+        unsigned long long vm = vmu[0];
+#pragma unroll
+        for (int i = 1; i < kSplitTiles; ++i)
+          if (k == i) vm = vmu[i];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          sv[i] = ((vm >> i) & 1ull) ? sv[i] * a.sm_scale_log2 : -INFINITY;
+          tmax = fmaxf(tmax, sv[i]);
+        }
+        // P and O are free once the previous stream tile's PV has completed
+        if (g >= 1 && !ptx::mbar_wait(lat_free + ((g - 1) & 1), uint32_t((g - 1) >> 1) & 1u)) { ok = false; break; }
+        ptx::tc_fence_after();
+        bool need = false;
+        float alpha = 1.f;
+        if (m_use == -INFINITY) {
+          m_use = tmax;
+        } else if (tmax > m_use + 8.f) {
+          need = true;
+          alpha = ptx::ex2_approx(m_use - tmax);
+          m_use = tmax;
+        }
+        if (__any_sync(0xffffffffu, need)) {
+          l *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < 256; c += 32) {
+            float o[32];
+            ptx::tmem_ld32(tmem + lane_base + c, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            ptx::tmem_st32(tmem + lane_base + c, o);
+          }
+        }
+        float psum = 0.f;
+        uint8_t* prow = Ps + h * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 8 * c + 2 * e;
+            const float p0 = m_use == -INFINITY ? 0.f : ptx::ex2_approx(sv[i] - m_use);
+            const float p1 = m_use == -INFINITY ? 0.f : ptx::ex2_approx(sv[i + 1] - m_use);
+            psum += p0 + p1;
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
+          }
+          *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        l += psum;
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      // epilogue: O / l of this head row and this CTA's 256 dims once the unit's
+      // last PV is done
+      const int gl = g - 1;
+      if (!ptx::mbar_wait(lat_free + (gl & 1), uint32_t(gl >> 1) & 1u)) { ok = false; break; }
       ptx::tc_fence_after();
-      float sv[64];
-      ptx::tmem_ld32(tmem + lane_base + kSCol + bk * kNT, *reinterpret_cast<float(*)[32]>(&sv[0]));
-      ptx::tmem_ld32(tmem + lane_base + kSCol + bk * kNT + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(s_free + bk);
-      // exchange partial scores with the peer CTA: asynchronous remote stores
-      // whose bytes complete on the peer's x_full[bk]. The peer's X[bk] is free
-      // again: this CTA got here after receiving the peer's tile k - 1, which
-      // every peer thread sent after reading its row of X[bk] (tile k - 2).
-      {
-        const uint32_t dst = x_peer + bk * kXBuf;
-        const uint32_t rbar = ptx::mapa_shared(ptx::smem_u32(x_full + bk), peer);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          ptx::st_async_f4(dst + i * 16, make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), rbar);
-      }
-      if (!ptx::mbar_wait_cluster(x_full + bk, kph)) { ok = false; break; }
-      const float4* xr = reinterpret_cast<const float4*>(X + bk * kXBuf + h * kXRow);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 x = xr[i];
-        sv[4 * i] += x.x; sv[4 * i + 1] += x.y; sv[4 * i + 2] += x.z; sv[4 * i + 3] += x.w;
-      }
-      // warp 0 re-arms x_full[bk] for tile k + 2 (bytes that arrive first
-      // count down until the arrival; the phase cannot complete before it)
-      if (warp == 0 && lane == 0 && k + 2 < nt) ptx::mbar_arrive_expect_tx(x_full + bk, kXBytes);
-      const unsigned long long vm = vmask[k];
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        sv[i] = ((vm >> i) & 1ull) ? sv[i] * a.sm_scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, sv[i]);
-      }
-      // P and O are free once the previous tile's PV has completed
-      if (k >= 1 && !ptx::mbar_wait(lat_free + ((k - 1) & 1), uint32_t((k - 1) >> 1) & 1u)) { ok = false; break; }
-      ptx::tc_fence_after();
-      bool need = false;
-      float alpha = 1.f;
-      if (m_use == -INFINITY) {
-        m_use = tmax;
-      } else if (tmax > m_use + 8.f) {
-        need = true;
-        alpha = ptx::ex2_approx(m_use - tmax);
-        m_use = tmax;
-      }
-      if (__any_sync(0xffffffffu, need)) {
-        l *= alpha;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int orow = (r * a.splits + split) * kHeads + warp * 32;
+      if (u + 1 == u1) {
+        // the cluster's last unit: every tile buffer, P and X are free (the
+        // last PV has read them, every peer score has landed), so each thread
+        // stages its whole 1-KB row there and sends it with one bulk store
+        uint8_t* orow_s = LAT + size_t(h) * kORow;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           float o[32];
           ptx::tmem_ld32(tmem + lane_base + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          ptx::tmem_st32(tmem + lane_base + c, o);
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(orow_s + (c + i) * 4) =
+                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
         }
-      }
-      float psum = 0.f;
-      uint8_t* prow = Ps + h * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 8 * c + 2 * e;
-          const float p0 = m_use == -INFINITY ? 0.f : ptx::ex2_approx(sv[i] - m_use);
-          const float p1 = m_use == -INFINITY ? 0.f : ptx::ex2_approx(sv[i + 1] - m_use);
-          psum += p0 + p1;
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
-        }
-        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-      l += psum;
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_full);
-    }
-    if (ok && !ptx::mbar_wait(lat_free + ((nt - 1) & 1), uint32_t((nt - 1) >> 1) & 1u)) ok = false;
-    if (ok) {
-      // O / l of this head row: TMEM -> the free tile buffers (one padded row
-      // per head) -> one 1-KB bulk store per row
-      ptx::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint8_t* orow_s = LAT + size_t(h) * kORow;
+        ptx::fence_proxy_async_smem();
+        ptx::bulk_store(a.opart + (size_t(orow) + lane) * kDNope + half * 256, orow_s, 256 * 4);
+        ptx::bulk_commit();
+      } else {
+        // 32 heads x 32 dims at a time, TMEM -> this warp's swizzled staging tile
+        // (row = head, 16-B chunk j at j ^ (row & 7)) -> one TMA store
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
-        float o[32];
-        ptx::tmem_ld32(tmem + lane_base + c, o);
+        for (int c = 0; c < 256; c += 32) {
+          float o[32];
+          ptx::tmem_ld32(tmem + lane_base + c, o);
+          if (lane == 0) ptx::bulk_wait_read();  // the previous chunk has left the staging tile
+          __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(orow_s + (c + i) * 4) =
-              make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_float4(o[4 * j] * inv, o[4 * j + 1] * inv, o[4 * j + 2] * inv, o[4 * j + 3] * inv);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&omap, stg, half * 256 + c, orow);
+            ptx::bulk_commit();
+          }
+        }
       }
-      ptx::fence_proxy_async_smem();
-      ptx::bulk_store(op + size_t(h) * kDNope, orow_s, 256 * 4);
-      ptx::bulk_store_commit_wait_read();
-      if (half == 0) lp[h] = l > 0.f ? (m_use + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      if (half == 0)
+        a.lpart[(size_t(r) * a.splits + split) * kHeads + h] = l > 0.f ? (m_use + log2f(l)) * 0.6931471805599453f
+                                                                        : -INFINITY;
+      // the reads of O are ordered before the next unit's first PV (p_full)
+      ptx::tc_fence_before();
     }
+    ptx::bulk_wait_all();  // the partials are written before the grid ends
   }
   if (!ok) atomicOr(a.err, DSA_DEVERR_TIMEOUT);
   ptx::tc_fence_before();
@@ -619,6 +722,15 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
     if (!encode_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 2, dims, strides, box, true))
       return cudaErrorInvalidValue;
   }
+  CUtensorMap omap;
+  {
+    // the split partials [rows * splits * 96][512] fp32, written in 32 x 32 tiles
+    const uint64_t dims[2] = {uint64_t(kDNope), uint64_t(L.rows) * L.splits * kHeads};
+    const uint64_t strides[1] = {uint64_t(kDNope) * 4};
+    const uint32_t box[2] = {32, 32};
+    if (!encode_map(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + L.opart, 2, dims, strides, box, true))
+      return cudaErrorInvalidValue;
+  }
   MlaTc t;
   t.block_table = block_table;
   t.ctx_lens = ctx_lens;
@@ -634,16 +746,20 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   t.K = p.topk;
   t.splits = L.splits;
   t.per_split = kSplitTok;
+  t.rows = L.rows;
   t.sm_scale_log2 = p.softmax_scale * 1.4426950408889634f;
   t.lat_scale = p.latent_scale;
   t.opart = reinterpret_cast<float*>(ws + L.opart);
   t.lpart = reinterpret_cast<float*>(ws + L.lpart);
   t.err = reinterpret_cast<int*>(ws + L.err);
   t.early = early ? 1 : 0;
-  cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kTcMlaSmem));
+  auto kern = t.lat_nvfp4 ? sparse_mla_tc_kernel<true> : sparse_mla_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTcMlaSmem));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(sparse_mla_tc_kernel, dim3(2 * L.splits, L.rows), dim3(kTcMlaThreads), kTcMlaSmem, st, qmap, t);
+  // one cluster per unit, or a cluster per pair of SMs each taking a run of units
+  const int units = L.rows * L.splits;
+  const int clusters = std::max(1, std::min(units, sm_count() / 2));
+  e = launch_pdl(kern, dim3(2 * clusters), dim3(kTcMlaThreads), kTcMlaSmem, st, qmap, omap, t);
   if (e != cudaSuccess) return e;
   return launch_pdl(mla_combine_kernel, dim3(L.rows, kHeads / kCombHeads), dim3(kCombThreads), 0, st,
                     static_cast<const float*>(t.opart), static_cast<const float*>(t.lpart), int(L.splits),
