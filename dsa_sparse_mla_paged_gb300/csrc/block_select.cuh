@@ -149,15 +149,16 @@ namespace dsa {
 // totals, then that warp's bins). LOWER: stop after one round and return the
 // bin's lowest key (at least k keys reach it). Otherwise: stop when the bin is
 // one key wide, or holds at most 32 keys (one warp ranks them), and return
-// the exact k-th largest key. NT = 1024; `hist` holds 4096 ints (two
-// buffers: a round's bins are cleared while the other round's are read), `smw`
-// 64, `list` 32.
+// the exact k-th largest key, and in *n_gt / *n_eq (when not null) how many
+// keys lie above it and how many equal it. NT = 1024; `hist` holds 4096 ints
+// (two buffers: a round's bins are cleared while the other round's are read),
+// `smw` 64, `list` 32.
 template <int NT, int PER, bool LOWER>
 __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t floor, int* hist, int* smw,
-                                    uint32_t* list) {
+                                    uint32_t* list, int* n_gt = nullptr, int* n_eq = nullptr) {
   static_assert(NT == 1024, "two bins per thread");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __shared__ int s_bin, s_rank, s_cnt, s_n;
+  __shared__ int s_bin, s_rank, s_cnt, s_n, s_gt, s_eq;
   __shared__ uint32_t s_lo, s_hi, s_key;
   if (warp == 0) {
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
@@ -264,7 +265,12 @@ __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t
     if (LOWER) return below ? floor : nlo;
     lo = nlo;
     hi = nhi;
-    if (lo == hi) return lo;
+    if (lo == hi) {
+      // the bin is one key wide: its n keys all equal the answer, and the
+      // k - kk keys of the bins above it are larger
+      if (n_gt) { *n_gt = k - kk; *n_eq = n; }
+      return lo;
+    }
     if (n <= 32) break;
   }
   // at most 32 keys lie in [lo, hi]: one warp ranks them
@@ -284,16 +290,22 @@ __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t
       gt += x > mine;
       eq += x == mine;
     }
-    if (lane < n && gt < kk && kk <= gt + eq) s_key = mine;
+    if (lane < n && gt < kk && kk <= gt + eq) {
+      s_key = mine;
+      s_gt = k - kk + gt;  // the keys of the bins above this one, and those above it in the bin
+      s_eq = eq;
+    }
   }
   __syncthreads();
+  if (n_gt) { *n_gt = s_gt; *n_eq = s_eq; }
   return s_key;
 }
 
 template <int NT, int PER>
 __device__ __forceinline__ uint32_t block_kth_fast(const uint32_t (&keys)[PER], int k, uint32_t floor, int* hist,
-                                                   int* smw, uint32_t* list) {
-  return block_kth_range<NT, PER, false>(keys, k, floor, hist, smw, list);
+                                                   int* smw, uint32_t* list, int* n_gt = nullptr,
+                                                   int* n_eq = nullptr) {
+  return block_kth_range<NT, PER, false>(keys, k, floor, hist, smw, list, n_gt, n_eq);
 }
 
 // A key at or below the k-th largest such that at least k keys reach it.

@@ -661,6 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
 // reductions; every split's partial row is read at once.
 constexpr int kCombThreads = 384;
 constexpr int kCombHeads = kCombThreads / 128;
+constexpr size_t kCombSpreadSmem = 120 * 1024;  // more than half an SM's shared memory: one CTA per SM
 
 __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* __restrict__ opart,
                                                                    const float* __restrict__ lpart, int splits,
@@ -671,6 +672,14 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* 
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y * kCombHeads + (threadIdx.x >> 7);
   const int d4 = threadIdx.x & 127;  // dims 4*d4 .. 4*d4+3
+  // every split's partial in flight at once, together with the splits' lse
+  // (splits <= kMaxSplits; a slot past the last split reads split 0 again and
+  // gets weight 0), then added in split order
+  const float4* src = reinterpret_cast<const float4*>(opart + (size_t(r) * splits * kHeads + h) * kDNope) + d4;
+  const size_t split_stride = size_t(kHeads) * kDNope / 4;  // float4 per split
+  float4 v[kMaxSplits];
+#pragma unroll
+  for (int u = 0; u < kMaxSplits; ++u) v[u] = __ldg(src + (u < splits ? u : 0) * split_stride);
   const float li = lane < splits ? __ldg(lpart + (size_t(r) * splits + lane) * kHeads + h) : -INFINITY;
   float m = li;
 #pragma unroll
@@ -681,19 +690,12 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float* 
   for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const float L = m == -INFINITY ? -INFINITY : m + logf(tot);
   const float wgt = m == -INFINITY ? 0.f : expf(li - L);
-  const float4* src = reinterpret_cast<const float4*>(opart + (size_t(r) * splits * kHeads + h) * kDNope) + d4;
-  const size_t split_stride = size_t(kHeads) * kDNope / 4;  // float4 per split
-  // every split's partial in flight at once (splits <= kMaxSplits; a slot past
-  // the last split reads split 0 again with weight 0), then added in split order
   float wv[kMaxSplits];
 #pragma unroll
   for (int u = 0; u < kMaxSplits; ++u) {
     const float wi = __shfl_sync(0xffffffffu, wgt, u & 31);
     wv[u] = u < splits ? wi : 0.f;
   }
-  float4 v[kMaxSplits];
-#pragma unroll
-  for (int u = 0; u < kMaxSplits; ++u) v[u] = __ldg(src + (u < splits ? u : 0) * split_stride);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int u = 0; u < kMaxSplits; ++u) {
@@ -761,7 +763,15 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   const int clusters = std::max(1, std::min(units, sm_count() / 2));
   e = launch_pdl(kern, dim3(2 * clusters), dim3(kTcMlaThreads), kTcMlaSmem, st, qmap, omap, t);
   if (e != cudaSuccess) return e;
-  return launch_pdl(mla_combine_kernel, dim3(L.rows, kHeads / kCombHeads), dim3(kCombThreads), 0, st,
+  // The combine's CTAs become resident while the attention still holds most
+  // SMs; with fewer CTAs than SMs, a shared-memory request that leaves room for
+  // one per SM keeps them from stacking on the few free SMs (their loads would
+  // then share one SM's bandwidth) and spreads them as the attention's SMs free up.
+  const int cctas = L.rows * (kHeads / kCombHeads);
+  const size_t csmem = cctas <= sm_count() ? kCombSpreadSmem : 0;
+  e = cudaFuncSetAttribute(mla_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kCombSpreadSmem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(mla_combine_kernel, dim3(L.rows, kHeads / kCombHeads), dim3(kCombThreads), csmem, st,
                     static_cast<const float*>(t.opart), static_cast<const float*>(t.lpart), int(L.splits),
                     static_cast<__nv_bfloat16*>(out), lse);
 }

@@ -521,19 +521,13 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     uint32_t mk[kCandPer];
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) mk[u] = uint32_t(cv[u] >> 32);
-    const uint32_t tau = block_kth_fast<kTkThreads, kCandPer>(mk, a.K, g, hw, smw, s_list);
-    int gt = 0, eq = 0;
-#pragma unroll
-    for (int u = 0; u < kCandPer; ++u) {
-      gt += mk[u] > tau;
-      eq += mk[u] == tau;  // an empty slot has key 0 < tau
-    }
-    int t2;
-    block_excl_scan<kTkThreads>((gt << 16) | eq, &t2, smw);
-    const int need = a.K - (t2 >> 16);
+    // tau, and how many candidates lie above it (n_gt) and equal it (n_eq)
+    int n_gt, n_eq;
+    const uint32_t tau = block_kth_fast<kTkThreads, kCandPer>(mk, a.K, g, hw, smw, s_list, &n_gt, &n_eq);
+    const int need = a.K - n_gt;
     // ties at tau: the `need` lowest tokens (the need-th largest of ~token)
     uint32_t tie_max = 0xFFFFFFFFu;
-    if ((t2 & 0xFFFF) > need) {
+    if (n_eq > need) {
       uint32_t tk[kCandPer];
 #pragma unroll
       for (int u = 0; u < kCandPer; ++u) tk[u] = mk[u] == tau ? 0xFFFFFFFFu - uint32_t(cv[u]) : 0u;

@@ -208,6 +208,25 @@ def test_sparse_mla_over_oracle_indices(case):
     check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
 
 
+@pytest.mark.parametrize("lat_fmt", ["fp8", "nvfp4"])
+def test_sparse_mla_latent_scale(lat_fmt):
+    """A per-tensor latent scale other than 1 (and not a power of two) multiplies every
+    dequantised latent value (the expansion then rounds each product to bf16)."""
+    import dataclasses
+
+    import torch
+
+    key_fmt = "mxfp4" if lat_fmt == "nvfp4" else "fp8"
+    inp = gen.make_inputs(2, 1, [5000, 3100], seed=21, bt_mode="permuted", key_fmt=key_fmt, lat_fmt=lat_fmt)
+    inp = dataclasses.replace(inp, latent_scale=0.75)
+    d = Dev(inp)
+    ref = {r: O.topk_select(s, 2048) for r, s in rows_scores_oracle(inp).items()}
+    idx = np.stack([ref[r] for r in range(d.rows)])
+    out, lse = d.mla(torch.from_numpy(idx).cuda())
+    ro, rl = _oracle_mla_all(inp, idx)
+    check_attention(bf16_to_np(out), lse.cpu().numpy(), ro, rl)
+
+
 def test_sparse_mla_holes_in_index_list():
     """-1 entries anywhere in the list are skipped; an all -1 row gives zeros and -inf."""
     import torch
