@@ -50,7 +50,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait: false after `limit` unsuccessful polls (the caller reports a timeout).
+// (The poll loop stays rolled: unrolled at each of a kernel's many waits it
+// multiplied the code, and the instruction cache misses slowed every role.)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 24)) {
+#pragma unroll 1
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
@@ -207,6 +210,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // Bounded wait that acquires at cluster scope (data written by another CTA).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 24)) {
+#pragma unroll 1
   for (uint32_t i = 0; i < limit; ++i) {
     uint32_t ok;
     asm volatile(

@@ -92,24 +92,15 @@ __device__ __forceinline__ uint32_t bf16x2_from_e4m3x2(uint16_t two) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// 16 E4M3 bytes -> 16 bf16 (exact when scale == 1), as two 16-B chunks.
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float scale) {
-  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
-  const __nv_bfloat162 o = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-  return *reinterpret_cast<const uint32_t*>(&o);
-}
-
-__device__ __forceinline__ void expand_e4m3x16(const uint4 w, float scale, uint4& lo, uint4& hi) {
+// 16 E4M3 bytes -> 16 bf16 (exactly), as two 16-B chunks. The per-tensor
+// latent scale is not applied here: it multiplies the scores' scale and the
+// output instead (one factor of the whole sum), so the tiles hold the exact
+// quantised values.
+__device__ __forceinline__ void expand_e4m3x16(const uint4 w, uint4& lo, uint4& hi) {
   lo.x = bf16x2_from_e4m3x2(uint16_t(w.x)); lo.y = bf16x2_from_e4m3x2(uint16_t(w.x >> 16));
   lo.z = bf16x2_from_e4m3x2(uint16_t(w.y)); lo.w = bf16x2_from_e4m3x2(uint16_t(w.y >> 16));
   hi.x = bf16x2_from_e4m3x2(uint16_t(w.z)); hi.y = bf16x2_from_e4m3x2(uint16_t(w.z >> 16));
   hi.z = bf16x2_from_e4m3x2(uint16_t(w.w)); hi.w = bf16x2_from_e4m3x2(uint16_t(w.w >> 16));
-  if (scale != 1.0f) {
-    lo.x = scale_bf16x2(lo.x, scale); lo.y = scale_bf16x2(lo.y, scale);
-    lo.z = scale_bf16x2(lo.z, scale); lo.w = scale_bf16x2(lo.w, scale);
-    hi.x = scale_bf16x2(hi.x, scale); hi.y = scale_bf16x2(hi.y, scale);
-    hi.z = scale_bf16x2(hi.z, scale); hi.w = scale_bf16x2(hi.w, scale);
-  }
 }
 
 // Byte offset inside a 576-B latent row of this CTA's 16-B piece q, for
@@ -148,7 +139,7 @@ __device__ __forceinline__ bool conv_store(const uint4 (&buf)[NPC / 2], const Ml
       const int jj = pc / NPC, q = pc - jj * NPC;
       const int kl = q >> 2, c = (q & 3) * 2;
       uint4 lo, hi;
-      expand_e4m3x16(buf[u], a.lat_scale, lo, hi);
+      expand_e4m3x16(buf[u], lo, hi);
       uint8_t* rowb = lat + kl * kLBlk + jj * 128;
       *reinterpret_cast<uint4*>(rowb + ((c ^ (jj & 7)) << 4)) = lo;
       *reinterpret_cast<uint4*>(rowb + (((c + 1) ^ (jj & 7)) << 4)) = hi;
@@ -163,17 +154,19 @@ __device__ __forceinline__ bool conv_store(const uint4 (&buf)[NPC / 2], const Ml
 // Converter warps (128 threads): a unit's tiles 0..nt-1 (stream tiles g0 + k)
 // into LAT[(g0 + k) & 1], the loads of tile k+1 in flight while tile k waits
 // for its buffer and is expanded.
+// (One call site of each step: the expansion is long, and the kernel's code
+// already strains the instruction cache.)
 template <int NPC>
 __device__ void converter_role(const MlaTc& a, int ct, int lane, int nt, int g0, const uint8_t* const* rowptr,
                                uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free, bool& ok) {
-  uint4 bufa[NPC / 2], bufb[NPC / 2];
-  conv_load<NPC>(bufa, rowptr, ct, 0);
-  for (int k = 0; k < nt; k += 2) {
-    if (k + 1 < nt) conv_load<NPC>(bufb, rowptr, ct, k + 1);
-    if (!conv_store<NPC>(bufa, a, ct, lane, g0 + k, LAT, lat_full, lat_free)) { ok = false; return; }
-    if (k + 1 >= nt) break;
-    if (k + 2 < nt) conv_load<NPC>(bufa, rowptr, ct, k + 2);
-    if (!conv_store<NPC>(bufb, a, ct, lane, g0 + k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
+  uint4 cur[NPC / 2], nxt[NPC / 2];
+  conv_load<NPC>(cur, rowptr, ct, 0);
+#pragma unroll 1
+  for (int k = 0; k < nt; ++k) {
+    if (k + 1 < nt) conv_load<NPC>(nxt, rowptr, ct, k + 1);
+    if (!conv_store<NPC>(cur, a, ct, lane, g0 + k, LAT, lat_full, lat_free)) { ok = false; return; }
+#pragma unroll
+    for (int u = 0; u < NPC / 2; ++u) cur[u] = nxt[u];
   }
 }
 
@@ -254,8 +247,8 @@ __device__ __forceinline__ bool conv_store_nv(const NvUnit (&buf)[NvUnits<HALF>:
       if (q < 8) {
         // nope dims [32q, 32q + 32) of this CTA: K-block q / 2, chunks 4 (q & 1) .. + 3
         rowb = lat + (q >> 1) * kLBlk + jj * 128;
-        const float s0 = e4m3_to_float(buf[u].s) * a.lat_scale;
-        const float s1 = e4m3_to_float(buf[u].s >> 8) * a.lat_scale;
+        const float s0 = e4m3_to_float(buf[u].s);  // E2M1 x E4M3: exact in bf16
+        const float s1 = e4m3_to_float(buf[u].s >> 8);
         const int c0 = (q & 1) * 4;
         *reinterpret_cast<uint4*>(rowb + (((c0 + 0) ^ (jj & 7)) << 4)) = e2m1x8_scaled(buf[u].v.x, s0);
         *reinterpret_cast<uint4*>(rowb + (((c0 + 1) ^ (jj & 7)) << 4)) = e2m1x8_scaled(buf[u].v.y, s0);
@@ -266,7 +259,7 @@ __device__ __forceinline__ bool conv_store_nv(const NvUnit (&buf)[NvUnits<HALF>:
         rowb = lat + 4 * kLBlk + jj * 128;
         const int c = (q - 8) * 2;
         uint4 lo, hi;
-        expand_e4m3x16(buf[u].v, a.lat_scale, lo, hi);
+        expand_e4m3x16(buf[u].v, lo, hi);
         *reinterpret_cast<uint4*>(rowb + ((c ^ (jj & 7)) << 4)) = lo;
         *reinterpret_cast<uint4*>(rowb + (((c + 1) ^ (jj & 7)) << 4)) = hi;
       }
@@ -281,14 +274,14 @@ __device__ __forceinline__ bool conv_store_nv(const NvUnit (&buf)[NvUnits<HALF>:
 template <int HALF>
 __device__ void converter_role_nv(const MlaTc& a, int ct, int lane, int nt, int g0, const uint8_t* const* rowptr,
                                   uint8_t* LAT, uint64_t* lat_full, uint64_t* lat_free, bool& ok) {
-  NvUnit bufa[NvUnits<HALF>::kPerThread], bufb[NvUnits<HALF>::kPerThread];
-  conv_load_nv<HALF>(bufa, rowptr, ct, 0);
-  for (int k = 0; k < nt; k += 2) {
-    if (k + 1 < nt) conv_load_nv<HALF>(bufb, rowptr, ct, k + 1);
-    if (!conv_store_nv<HALF>(bufa, a, ct, lane, g0 + k, LAT, lat_full, lat_free)) { ok = false; return; }
-    if (k + 1 >= nt) break;
-    if (k + 2 < nt) conv_load_nv<HALF>(bufa, rowptr, ct, k + 2);
-    if (!conv_store_nv<HALF>(bufb, a, ct, lane, g0 + k + 1, LAT, lat_full, lat_free)) { ok = false; return; }
+  NvUnit cur[NvUnits<HALF>::kPerThread], nxt[NvUnits<HALF>::kPerThread];
+  conv_load_nv<HALF>(cur, rowptr, ct, 0);
+#pragma unroll 1
+  for (int k = 0; k < nt; ++k) {
+    if (k + 1 < nt) conv_load_nv<HALF>(nxt, rowptr, ct, k + 1);
+    if (!conv_store_nv<HALF>(cur, a, ct, lane, g0 + k, LAT, lat_full, lat_free)) { ok = false; return; }
+#pragma unroll
+    for (int u = 0; u < NvUnits<HALF>::kPerThread; ++u) cur[u] = nxt[u];
   }
 }
 
@@ -373,9 +366,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
   };
   int q_row = -1;
   bool q_pending = false;
-  if (a.early && warp == 3 && lane == 0 && u0 < u1) {
+  if (a.early && warp == 3 && u0 < u1) {
     q_row = u0 / a.splits;
-    issue_q(q_row);
+    if (ptx::elect_one()) issue_q(q_row);
+    __syncwarp();
     q_pending = true;
   }
   // everything above is on-chip set-up or a read of the caller's query; what
@@ -385,7 +379,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
 
   if (warp == 3) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the loop (so every operand below is computed in
+    // converged code); one elected lane issues each batch of MMAs, commits and
+    // copies.
+    {
       const uint32_t id_qk = ptx::idesc(1, 1, 128, kNT);
       const uint32_t id_pv = ptx::idesc(1, 1, 128, 256, 0, 1);
       const uint32_t q0 = ptx::smem_u32(Qs), l0 = ptx::smem_u32(LAT), p0 = ptx::smem_u32(Ps);
@@ -395,11 +392,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
         if (!ok || !ptx::mbar_wait(p_full, uint32_t(j) & 1u)) { ok = false; return; }
         ptx::tc_fence_after();
         const uint32_t lat = l0 + (j & 1) * kLatBuf;
+        if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kNT / 16; ++kk)
-          ptx::mma_f16(tmem, ptx::sdesc_sw128(p0 + kk * 32), ptx::sdesc_sw128_mn(lat + kk * 16 * 128, kLBlk, 1024),
-                       id_pv, (kj > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(lat_free + (j & 1));
+          for (int kk = 0; kk < kNT / 16; ++kk)
+            ptx::mma_f16(tmem, ptx::sdesc_sw128(p0 + kk * 32), ptx::sdesc_sw128_mn(lat + kk * 16 * 128, kLBlk, 1024),
+                         id_pv, (kj > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(lat_free + (j & 1));
+        }
+        __syncwarp();
       };
       for (int u = u0; u < u1 && ok; ++u) {
         const int r = u / a.splits, nt = unit_tiles(u);
@@ -409,10 +409,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
           if (k == 0 && g >= 1) pv(g - 1, last_k);
           if (k == 0 && r != q_row) {
             if (q_row >= 0) {  // every MMA reading the old query is done before it is overwritten
-              ptx::mma_commit(q_free);
+              if (ptx::elect_one()) ptx::mma_commit(q_free);
+              __syncwarp();
               if (!ptx::mbar_wait(q_free, uint32_t(qf++) & 1u)) { ok = false; break; }
             }
-            issue_q(r);
+            if (ptx::elect_one()) issue_q(r);
+            __syncwarp();
             q_row = r;
             q_pending = true;
           }
@@ -426,19 +428,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
           if (g >= 2 && !ptx::mbar_wait(s_free + bk, kph ^ 1u)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t lat = l0 + bk * kLatBuf;
-          for (int kl = 0; kl < nkb; ++kl)
+          if (ptx::elect_one()) {
+            for (int kl = 0; kl < nkb; ++kl)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              ptx::mma_f16(tmem + kSCol + bk * kNT, ptx::sdesc_sw128(q0 + kl * kQBlk + kk * 32),
-                           ptx::sdesc_sw128(lat + kl * kLBlk + kk * 32), id_qk, (kl | kk) ? 1u : 0u);
-          ptx::mma_commit(s_full + bk);
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_f16(tmem + kSCol + bk * kNT, ptx::sdesc_sw128(q0 + kl * kQBlk + kk * 32),
+                             ptx::sdesc_sw128(lat + kl * kLBlk + kk * 32), id_qk, (kl | kk) ? 1u : 0u);
+            ptx::mma_commit(s_full + bk);
+          }
+          __syncwarp();
           if (k >= 1) pv(g - 1, k - 1);
           last_k = k;
         }
       }
       if (ok && g >= 1) pv(g - 1, last_k);
-      // nothing of this thread's left in flight when TMEM is released
-      ptx::mma_commit(mma_done);
+      // nothing of this warp's left in flight when TMEM is released
+      if (ptx::elect_one()) ptx::mma_commit(mma_done);
+      __syncwarp();
       ptx::mbar_wait(mma_done, 0);
       if (q_pending) ptx::mbar_wait(q_full, uint32_t(qn) & 1u);
     }
@@ -596,7 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
       const int gl = g - 1;
       if (!ptx::mbar_wait(lat_free + (gl & 1), uint32_t(gl >> 1) & 1u)) { ok = false; break; }
       ptx::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? a.lat_scale / l : 0.f;  // O = latent_scale * (sum p c) / l
       const int orow = (r * a.splits + split) * kHeads + warp * 32;
       if (u + 1 == u1) {
         // the cluster's last unit: every tile buffer, P and X are free (the
@@ -749,7 +755,9 @@ cudaError_t launch_sparse_mla(const dsa_params_t& p, const WsLayout& L, char* ws
   t.splits = L.splits;
   t.per_split = kSplitTok;
   t.rows = L.rows;
-  t.sm_scale_log2 = p.softmax_scale * 1.4426950408889634f;
+  // the tiles hold the latents without the per-tensor scale: it joins the
+  // scores' scale here and the output's 1 / l in the epilogue
+  t.sm_scale_log2 = p.softmax_scale * p.latent_scale * 1.4426950408889634f;
   t.lat_scale = p.latent_scale;
   t.opart = reinterpret_cast<float*>(ws + L.opart);
   t.lpart = reinterpret_cast<float*>(ws + L.lpart);
