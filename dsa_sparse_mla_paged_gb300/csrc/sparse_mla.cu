@@ -604,30 +604,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
       ptx::tc_fence_after();
       const float inv = l > 0.f ? a.lat_scale / l : 0.f;  // O = latent_scale * (sum p c) / l
       const int orow = (r * a.splits + split) * kHeads + warp * 32;
-      if (u + 1 == u1) {
-        // the cluster's last unit: every tile buffer, P and X are free (the
-        // last PV has read them, every peer score has landed), so each thread
-        // stages its whole 1-KB row there and sends it with one bulk store
-        uint8_t* orow_s = LAT + size_t(h) * kORow;
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          float o[32];
-          ptx::tmem_ld32(tmem + lane_base + c, o);
+      // 32 columns at a time, the next chunk's TMEM load in flight while this
+      // one is scaled and stored (a wait covers every load issued before it)
+      const bool tail = u + 1 == u1;
+      uint8_t* orow_s = LAT + size_t(h) * kORow;
+      auto emit = [&](const float (&o)[32], int c) {
+        if (tail) {
+          // the cluster's last unit: every tile buffer, P and X are free (the
+          // last PV has read them, every peer score has landed), so each
+          // thread stages its whole 1-KB row there for one bulk store
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(orow_s + (c + i) * 4) =
                 make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::bulk_store(a.opart + (size_t(orow) + lane) * kDNope + half * 256, orow_s, 256 * 4);
-        ptx::bulk_commit();
-      } else {
-        // 32 heads x 32 dims at a time, TMEM -> this warp's swizzled staging tile
-        // (row = head, 16-B chunk j at j ^ (row & 7)) -> one TMA store
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          float o[32];
-          ptx::tmem_ld32(tmem + lane_base + c, o);
+        } else {
+          // 32 heads x 32 dims -> this warp's swizzled staging tile (row =
+          // head, 16-B chunk j at j ^ (row & 7)) -> one TMA store
           if (lane == 0) ptx::bulk_wait_read();  // the previous chunk has left the staging tile
           __syncwarp();
 #pragma unroll
@@ -641,6 +633,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
             ptx::bulk_commit();
           }
         }
+      };
+      {
+        float oa[32], ob[32];
+        ptx::tmem_ld32_nowait(tmem + lane_base, oa);
+        ptx::tmem_ld_wait(oa);
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 64) {
+          ptx::tmem_ld32_nowait(tmem + lane_base + c + 32, ob);
+          emit(oa, c);
+          ptx::tmem_ld_wait(ob);
+          if (c + 64 < 256) ptx::tmem_ld32_nowait(tmem + lane_base + c + 64, oa);
+          emit(ob, c + 32);
+          if (c + 64 < 256) ptx::tmem_ld_wait(oa);
+        }
+      }
+      if (tail) {
+        ptx::fence_proxy_async_smem();
+        ptx::bulk_store(a.opart + (size_t(orow) + lane) * kDNope + half * 256, orow_s, 256 * 4);
+        ptx::bulk_commit();
       }
       if (half == 0)
         a.lpart[(size_t(r) * a.splits + split) * kHeads + h] = l > 0.f ? (m_use + log2f(l)) * 0.6931471805599453f
