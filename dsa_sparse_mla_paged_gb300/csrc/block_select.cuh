@@ -150,12 +150,13 @@ namespace dsa {
 // bin's lowest key (at least k keys reach it). Otherwise: stop when the bin is
 // one key wide, or holds at most 32 keys (one warp ranks them), and return
 // the exact k-th largest key, and in *n_gt / *n_eq (when not null) how many
-// keys lie above it and how many equal it. NT = 1024; `hist` holds 4096 ints
-// (two buffers: a round's bins are cleared while the other round's are read),
-// `smw` 64, `list` 32.
+// keys lie above it and how many equal it. Only each thread's first `nper`
+// slots are read (a bound the whole CTA shares, so the loops stop together).
+// NT = 1024; `hist` holds 4096 ints (two buffers: a round's bins are cleared
+// while the other round's are read), `smw` 64, `list` 32.
 template <int NT, int PER, bool LOWER>
 __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t floor, int* hist, int* smw,
-                                    uint32_t* list, int* n_gt = nullptr, int* n_eq = nullptr) {
+                                    uint32_t* list, int* n_gt = nullptr, int* n_eq = nullptr, int nper = PER) {
   static_assert(NT == 1024, "two bins per thread");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ int s_bin, s_rank, s_cnt, s_n, s_gt, s_eq;
@@ -163,8 +164,10 @@ __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t
   if (warp == 0) {
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
+    for (int i = 0; i < PER; ++i) {
+      if (i >= nper) break;
       if (keys[i]) { mn = min(mn, keys[i]); mx = max(mx, keys[i]); }
+    }
     mn = __reduce_min_sync(0xffffffffu, mn);
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0) {
@@ -187,6 +190,7 @@ __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t
     const int sh = span == 0u ? 0 : max(0, 21 - __clz(span));  // (span >> sh) < 2048
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
+      if (i >= nper) break;
       const uint32_t x = keys[i];
       if (x == 0u) continue;
       int b;
@@ -275,11 +279,13 @@ __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t
   }
   // at most 32 keys lie in [lo, hi]: one warp ranks them
 #pragma unroll
-  for (int i = 0; i < PER; ++i)
+  for (int i = 0; i < PER; ++i) {
+    if (i >= nper) break;
     if (keys[i] && keys[i] >= lo && keys[i] <= hi) {
       const int at = atomicAdd(&s_n, 1);
       if (at < 32) list[at] = keys[i];
     }
+  }
   __syncthreads();
   if (warp == 0) {
     const int n = min(s_n, 32);
@@ -304,15 +310,15 @@ __device__ uint32_t block_kth_range(const uint32_t (&keys)[PER], int k, uint32_t
 template <int NT, int PER>
 __device__ __forceinline__ uint32_t block_kth_fast(const uint32_t (&keys)[PER], int k, uint32_t floor, int* hist,
                                                    int* smw, uint32_t* list, int* n_gt = nullptr,
-                                                   int* n_eq = nullptr) {
-  return block_kth_range<NT, PER, false>(keys, k, floor, hist, smw, list, n_gt, n_eq);
+                                                   int* n_eq = nullptr, int nper = PER) {
+  return block_kth_range<NT, PER, false>(keys, k, floor, hist, smw, list, n_gt, n_eq, nper);
 }
 
 // A key at or below the k-th largest such that at least k keys reach it.
 template <int NT, int PER>
 __device__ __forceinline__ uint32_t block_kth_lower(const uint32_t (&keys)[PER], int k, int* hist, int* smw,
-                                                    uint32_t* list) {
-  return block_kth_range<NT, PER, true>(keys, k, 0u, hist, smw, list);
+                                                    uint32_t* list, int nper = PER) {
+  return block_kth_range<NT, PER, true>(keys, k, 0u, hist, smw, list, nullptr, nullptr, nper);
 }
 
 }  // namespace dsa

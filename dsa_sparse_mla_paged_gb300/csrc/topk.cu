@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
         }
       }
     }
-    g = block_kth_lower<kTkThreads, kBoundPer>(mk, a.K, hw, smw, s_list);
+    // group gi sits in slot gi / threads: only the first ceil(ng / threads) slots hold any
+    g = block_kth_lower<kTkThreads, kBoundPer>(mk, a.K, hw, smw, s_list, (ng + kTkThreads - 1) / kTkThreads);
   } else if (bd.kind == kSample) {
     // sample i at position floor(i * L / ns); the r-th largest, r for ~2K tokens
     const int ns = min(w.L, kBoundKeys);
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
       sk[u] = i < ns ? order_key(__ldcg(row + int(int64_t(i) * w.L / ns))) : 0u;
     }
     const int r = int(min(int64_t(ns), (int64_t(2) * a.K * ns + w.L - 1) / w.L));
-    g = block_kth_lower<kTkThreads, kBoundPer>(sk, r, hw, smw, s_list);
+    g = block_kth_lower<kTkThreads, kBoundPer>(sk, r, hw, smw, s_list, (ns + kTkThreads - 1) / kTkThreads);
   }
   if (nbytes && !ptx::mbar_wait(&s_bar, 0)) {
     if (tid == 0) atomicOr(a.err, DSA_DEVERR_TIMEOUT);
@@ -509,12 +510,17 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     // winner's output place is (winners of the chunks before its own) +
     // (winners of its chunk before it), its chunk being token / chunk. The
     // chunk records load with the candidates.
+    // Thread t holds candidates t * per .. t * per + per - 1, per = ceil(total /
+    // threads) (at most kCandPer): every loop over a thread's slots stops after
+    // `per` of them. (This CTA's phases are bound by instruction issue, eight
+    // warps per scheduler, so slots that would hold nothing still cost time.)
+    const int per = (total + kTkThreads - 1) / kTkThreads;
     const uint64_t* cand = a.cand + size_t(w.r) * kCandCap;
     uint64_t cv[kCandPer];
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) {
-      const int p = tid * kCandPer + u;
-      cv[u] = p < total ? __ldcg(cand + p) : 0ull;
+      const int p = tid * per + u;
+      cv[u] = (u < per && p < total) ? __ldcg(cand + p) : 0ull;
     }
     const int* recs = a.chunkinfo + size_t(w.r) * a.max_chunks * 2;
     int2 rec = tid < C ? __ldcg(reinterpret_cast<const int2*>(recs) + tid) : make_int2(0, 0);
@@ -523,7 +529,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     for (int u = 0; u < kCandPer; ++u) mk[u] = uint32_t(cv[u] >> 32);
     // tau, and how many candidates lie above it (n_gt) and equal it (n_eq)
     int n_gt, n_eq;
-    const uint32_t tau = block_kth_fast<kTkThreads, kCandPer>(mk, a.K, g, hw, smw, s_list, &n_gt, &n_eq);
+    const uint32_t tau = block_kth_fast<kTkThreads, kCandPer>(mk, a.K, g, hw, smw, s_list, &n_gt, &n_eq, per);
     const int need = a.K - n_gt;
     // ties at tau: the `need` lowest tokens (the need-th largest of ~token)
     uint32_t tie_max = 0xFFFFFFFFu;
@@ -531,15 +537,17 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
       uint32_t tk[kCandPer];
 #pragma unroll
       for (int u = 0; u < kCandPer; ++u) tk[u] = mk[u] == tau ? 0xFFFFFFFFu - uint32_t(cv[u]) : 0u;
-      tie_max = 0xFFFFFFFFu - block_kth_fast<kTkThreads, kCandPer>(tk, need, 0u, hw, smw, s_list);
+      tie_max = 0xFFFFFFFFu - block_kth_fast<kTkThreads, kCandPer>(tk, need, 0u, hw, smw, s_list, nullptr, nullptr, per);
     }
     unsigned win = 0;
 #pragma unroll
-    for (int u = 0; u < kCandPer; ++u)
+    for (int u = 0; u < kCandPer; ++u) {
+      if (u >= per) break;
       if (mk[u] > tau || (mk[u] == tau && uint32_t(cv[u]) <= tie_max)) win |= 1u << u;
+    }
     int tw;
     const int wbase = block_excl_scan<kTkThreads>(__popc(win), &tw, smw);  // winners before mine
-    // winners before reservation position p: s_wb[p / 32] + those of its thread below p % 32
+    // winners before reservation position p: s_wb[p / per] + those of its thread below p % per
     int* s_wb = reinterpret_cast<int*>(stage);    // [kTkThreads + 1]
     int* s_wm = s_wb + kTkThreads + 1;            // [kTkThreads] winner bits per thread
     int* s_first = s_wm + kTkThreads;             // [C] winners before the chunk's first candidate
@@ -549,9 +557,9 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     if (tid == 0) s_wb[kTkThreads] = tw;
     __syncthreads();
     auto wbefore = [&](int p) {
-      const int t = p / kCandPer;
+      const int t = p / per;
       return t >= kTkThreads ? s_wb[kTkThreads]
-                             : s_wb[t] + __popc(unsigned(s_wm[t]) & ((1u << (p % kCandPer)) - 1u));
+                             : s_wb[t] + __popc(unsigned(s_wm[t]) & ((1u << (p - t * per)) - 1u));
     };
     int carry = 0;
     for (int c0 = 0; c0 < C; c0 += kTkThreads) {
@@ -572,11 +580,18 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     }
     __syncthreads();
     int wb = wbase;
+    // a token's chunk, s / chunk, through the reciprocal: for any s < 2^31 and
+    // chunk >= 1,024 the rounded product is within one of the quotient, and the
+    // two comparisons correct it
+    const float inv_chunk = 1.0f / float(a.chunk);
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) {
+      if (u >= per) break;
       if ((win >> u) & 1u) {
         const int s = int(uint32_t(cv[u]));
-        const int ch = s / a.chunk;
+        int ch = int(float(s) * inv_chunk);
+        if (ch * a.chunk > s) --ch;
+        else if ((ch + 1) * a.chunk <= s) ++ch;
         const int pos = s_pre[ch] + (wb - s_first[ch]);
         if (pos < a.K) {
           out[pos] = s;
