@@ -66,6 +66,7 @@ constexpr int kUnitBufs = 4;                // row-address buffers, by unit
 constexpr int kStage = 32 * 128;            // one softmax warp's 32 x 32 fp32 output tile
 constexpr int kORow = 256 * 4 + 16;         // a head's output row staged in the free tile buffers
 static_assert(kHeads * kORow <= 2 * kLatBuf + kPBytes + 2 * kXBuf, "output staging overlaps the tile buffers");
+static_assert(3 * kStage <= kPBytes, "each softmax warp's quarter of P holds a staging tile");
 constexpr size_t kTcMlaSmem = 1024 + kQBytes + 2 * kLatBuf + kPBytes + 2 * kXBuf + 3 * kStage +
                               kUnitBufs * (kSplitTok * 8 + kSplitTiles * 8) + kNumBars * 8 + 16;
 static_assert(kTcMlaSmem <= 232448, "shared memory of one CTA");
@@ -503,6 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
     const uint32_t x_mine = ptx::smem_u32(X) + h * kXRow;
     const uint32_t x_peer = ptx::mapa_shared(x_mine, peer);
     uint8_t* stg = ST + warp * kStage;
+    uint8_t* pstg = Ps + warp * kStage;  // this warp's quarter of P, a second staging tile in the epilogue
     int g = 0;
     for (int u = u0, ui = 0; u < u1 && ok; ++u, ++ui) {
       const int r = u / a.splits, split = u % a.splits, nt = unit_tiles(u);
@@ -618,18 +620,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
             *reinterpret_cast<float4*>(orow_s + (c + i) * 4) =
                 make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
         } else {
-          // 32 heads x 32 dims -> this warp's swizzled staging tile (row =
-          // head, 16-B chunk j at j ^ (row & 7)) -> one TMA store
-          if (lane == 0) ptx::bulk_wait_read();  // the previous chunk has left the staging tile
+          // 32 heads x 32 dims -> a swizzled staging tile (row = head, 16-B
+          // chunk j at j ^ (row & 7)) -> one TMA store. The warp alternates two
+          // tiles, its own and its quarter of P (free from the unit's last PV
+          // until this warp writes the next P), so each wait is for the store
+          // two chunks back, which has long read its tile.
+          uint8_t* st = ((c >> 5) & 1) ? pstg : stg;
+          if (lane == 0) ptx::bulk_wait_read1();
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<float4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                 make_float4(o[4 * j] * inv, o[4 * j + 1] * inv, o[4 * j + 2] * inv, o[4 * j + 3] * inv);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_2d(&omap, stg, half * 256 + c, orow);
+            ptx::tma_store_2d(&omap, st, half * 256 + c, orow);
             ptx::bulk_commit();
           }
         }
@@ -652,6 +658,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcMlaThreads, 1)
         ptx::fence_proxy_async_smem();
         ptx::bulk_store(a.opart + (size_t(orow) + lane) * kDNope + half * 256, orow_s, 256 * 4);
         ptx::bulk_commit();
+      } else {
+        // the stores have read P's quarter before this warp writes the next P
+        if (lane == 0) ptx::bulk_wait_read();
+        __syncwarp();
       }
       if (half == 0)
         a.lpart[(size_t(r) * a.splits + split) * kHeads + h] = l > 0.f ? (m_use + log2f(l)) * 0.6931471805599453f
