@@ -156,6 +156,22 @@ def test_topk_many_rows_mid_chunks():
         assert np.array_equal(idx[b], O.topk_select(mat[b], 2048)), b
 
 
+@pytest.mark.parametrize("k", [2048, 256])
+def test_topk_many_long_rows(k):
+    """More rows than SMs, rows of 40K-70K tokens: three 32K-token chunks a row
+    (the last one partial, some CTAs past the row's end), several waves of CTAs
+    (a sampled bound at k = 2048, the group maxima at k = 256)."""
+    rng = np.random.default_rng(46)
+    ctx = [int(c) for c in rng.integers(40000, 70001, 160)]
+    inp = gen.make_inputs(160, 1, ctx, seed=46, topk=k)
+    d = Dev(inp)
+    mat = rng.standard_normal((160, d.cap)).astype(np.float32)
+    idx, _ = d.topk(mat)
+    idx = idx.cpu().numpy()
+    for b in (0, 1, 77, 151, 152, 159):
+        assert np.array_equal(idx[b], O.topk_select(mat[b, :ctx[b]], k)), b
+
+
 def test_topk_multi_token_rows_and_phys_rows():
     import dsa_sparse_mla_paged_gb300 as dsa
 
