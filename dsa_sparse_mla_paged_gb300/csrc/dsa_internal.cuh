@@ -241,8 +241,9 @@ __device__ __forceinline__ void build_tile_plan(const int32_t* __restrict__ ctx_
 cudaError_t launch_idx_q_quant(const dsa_params_t& p, const WsLayout& L, char* ws, const void* q_idx,
                                const float* w, const int32_t* ctx_lens, cudaStream_t st, int world = 1,
                                int rank = 0);
-// keep128: also fold each 128 tokens' largest score key into the workspace's
-// 128-token maxima (dsa_decode, whose top-k clears them after use).
+// keep128: also keep the score keys' group maxima in the workspace (each 32
+// tokens' largest, and each 128 tokens' folded by atomic max) for the top-k of
+// the same call (dsa_decode, whose top-k clears the 128-token ones after use).
 cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, const void* key_pool,
                            const int32_t* block_table, const int32_t* ctx_lens, float* scores,
                            int64_t score_stride, cudaStream_t st, int world = 1, int rank = 0,

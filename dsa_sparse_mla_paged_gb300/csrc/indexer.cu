@@ -238,10 +238,13 @@ __device__ __forceinline__ void epi_store(const IdxTc& a, float sum, int rowt, i
   const bool keep = e.t < ui.valid && tok < Lt && tok < a.score_stride;
   if (keep) a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
   // the warp's 32 tokens are one group: the key of their largest stored score
-  const uint32_t m = __reduce_max_sync(0xffffffffu, keep ? score_order_key(sum) : 0u);
-  if (lane == 0 && m != 0u) {
-    a.gmax[(size_t(ui.row0) + e.t) * a.gstride + (tok >> 5)] = m;
-    if (a.gmax128) atomicMax(a.gmax128 + (size_t(ui.row0) + e.t) * a.g128stride + (tok >> 7), m);
+  // (kept only for the fused step's top-k, which takes its bound from them)
+  if (a.gmax) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, keep ? score_order_key(sum) : 0u);
+    if (lane == 0 && m != 0u) {
+      a.gmax[(size_t(ui.row0) + e.t) * a.gstride + (tok >> 5)] = m;
+      atomicMax(a.gmax128 + (size_t(ui.row0) + e.t) * a.g128stride + (tok >> 7), m);
+    }
   }
   epi_skip(a, w, e);
 }
@@ -786,7 +789,9 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   a.wq = wq;
   a.key_pool = static_cast<const uint8_t*>(key_pool);
   a.scores = scores;
-  a.gmax = reinterpret_cast<uint32_t*>(ws + L.gmax);
+  // the group maxima feed only dsa_decode's top-k (a stand-alone dsa_topk
+  // computes its own), so other calls skip them
+  a.gmax = keep128 ? reinterpret_cast<uint32_t*>(ws + L.gmax) : nullptr;
   a.gmax128 = keep128 ? reinterpret_cast<uint32_t*>(ws + L.gmax128) : nullptr;
   a.gstride = L.gstride;
   a.g128stride = L.g128stride;

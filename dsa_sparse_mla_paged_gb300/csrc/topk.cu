@@ -489,12 +489,28 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     // the attention gathers the winners' latent rows next: start pulling this
     // chunk's candidates (a superset of its winners) into L2
     if (a.lat_pool) {
-      for (uint32_t m = pass; m; m &= m - 1u) {
-        const int j = __ffs(m) - 1;
-        const int s = wb + 4 * (lane + 32 * (j >> 2)) + (j & 3);
-        const int pg = a.block_table[size_t(w.b) * a.max_pages + s / kPage];
-        if (pg >= 0 && pg < a.num_pages)
-          ptx::prefetch_l2_bulk(a.lat_pool + size_t(pg) * a.lat_stride + size_t(s % kPage) * a.lat_row, a.lat_row);
+      // up to 32 candidates per thread (every token of a short row): the
+      // block-table entries of eight at a time are loaded together, so the
+      // grid does not end a chain of dependent loads after its last CTA
+      const int32_t* bt = a.block_table + size_t(w.b) * a.max_pages;
+      for (uint32_t m = pass; m;) {
+        int ts[8], pg[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          ts[q] = -1;
+          if (m) {
+            const int j = __ffs(m) - 1;
+            m &= m - 1u;
+            ts[q] = wb + 4 * (lane + 32 * (j >> 2)) + (j & 3);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pg[q] = ts[q] >= 0 ? __ldg(bt + ts[q] / kPage) : -1;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (pg[q] >= 0 && pg[q] < a.num_pages)
+            ptx::prefetch_l2_bulk(a.lat_pool + size_t(pg[q]) * a.lat_stride + size_t(ts[q] % kPage) * a.lat_row,
+                                  a.lat_row);
       }
     }
     return;
