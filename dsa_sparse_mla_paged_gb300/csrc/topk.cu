@@ -488,10 +488,13 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
   if (!s_last) {
     // the attention gathers the winners' latent rows next: start pulling this
     // chunk's candidates (a superset of its winners) into L2
-    if (a.lat_pool) {
-      // up to 32 candidates per thread (every token of a short row): the
-      // block-table entries of eight at a time are loaded together, so the
-      // grid does not end a chain of dependent loads after its last CTA
+    // (Only where the bound filters: a row short enough that every token is a
+    // candidate has few latent rows, and an SM works through bulk prefetches
+    // at ~25 ns each, which would hold the grid, and the attention waiting on
+    // it, for tens of microseconds. Likewise a CTA with many candidates.)
+    if (a.lat_pool && bd.kind != kAll && s_run <= 512) {
+      // the block-table entries of eight candidates at a time are loaded
+      // together, not one dependent load per candidate
       const int32_t* bt = a.block_table + size_t(w.b) * a.max_pages;
       for (uint32_t m = pass; m;) {
         int ts[8], pg[8];
