@@ -119,7 +119,6 @@ struct IdxTc {
   int64_t score_stride;
   int64_t key_page_stride;
   int units, n_q, max_pages, num_pages, stages, nacc, group, ncol, tmem_cols;  // n_q: rows per unit
-  int topk;       // K of the top-k that reads the group maxima
   int raw_slots;  // MXFP4: raw page-pair slots
   UnitMap map;
   int* err;
@@ -239,19 +238,12 @@ __device__ __forceinline__ void epi_store(const IdxTc& a, float sum, int rowt, i
   const bool keep = e.t < ui.valid && tok < Lt && tok < a.score_stride;
   if (keep) a.scores[(size_t(ui.row0) + e.t) * a.score_stride + tok] = sum;
   // the warp's 32 tokens are one group: the key of their largest stored score
-  // (kept only for the fused step's top-k, which takes its bound from them).
-  // The top-k bounds a row by its 128-token maxima when there are at least
-  // 9/8 K of them, else by its 32-token maxima when those are, else (and for
-  // rows of at most kCandCap tokens) by neither: only that kind is kept.
-  if (a.gmax && Lt > kCandCap) {
-    const bool by128 = int64_t((Lt + 127) >> 7) * 8 >= int64_t(a.topk) * 9;
-    const bool by32 = !by128 && int64_t((Lt + 31) >> 5) * 8 >= int64_t(a.topk) * 9;
-    if (by128 || by32) {
-      const uint32_t m = __reduce_max_sync(0xffffffffu, keep ? score_order_key(sum) : 0u);
-      if (lane == 0 && m != 0u) {
-        if (by32) a.gmax[(size_t(ui.row0) + e.t) * a.gstride + (tok >> 5)] = m;
-        else atomicMax(a.gmax128 + (size_t(ui.row0) + e.t) * a.g128stride + (tok >> 7), m);
-      }
+  // (kept only for the fused step's top-k, which takes its bound from them)
+  if (a.gmax) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, keep ? score_order_key(sum) : 0u);
+    if (lane == 0 && m != 0u) {
+      a.gmax[(size_t(ui.row0) + e.t) * a.gstride + (tok >> 5)] = m;
+      atomicMax(a.gmax128 + (size_t(ui.row0) + e.t) * a.g128stride + (tok >> 7), m);
     }
   }
   epi_skip(a, w, e);
@@ -800,7 +792,6 @@ cudaError_t launch_indexer(const dsa_params_t& p, const WsLayout& L, char* ws, c
   // the group maxima feed only dsa_decode's top-k (a stand-alone dsa_topk
   // computes its own), so other calls skip them
   a.gmax = keep128 ? reinterpret_cast<uint32_t*>(ws + L.gmax) : nullptr;
-  a.topk = p.topk;
   a.gmax128 = keep128 ? reinterpret_cast<uint32_t*>(ws + L.gmax128) : nullptr;
   a.gstride = L.gstride;
   a.g128stride = L.g128stride;
