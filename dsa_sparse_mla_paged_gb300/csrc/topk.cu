@@ -53,9 +53,11 @@ constexpr int kRoundTok = kTkWarps * 1024;          // tokens a CTA filters at m
 constexpr int kGmaxThreads = 256;
 
 // row state words
-constexpr int kStCursor = 1;   // candidates reserved so far
-constexpr int kStOverflow = 2; // a chunk did not fit the buffer
-constexpr int kStArrived = 3;  // CTAs of the row done with their chunk
+// words 2 and 3 as one 64-bit counter: the candidates reserved so far (low
+// half) and the CTAs of the row done with their chunk (high half), so that the
+// last CTA's arrival returns the final count with it (every CTA reserves
+// before it arrives); more than kCandCap means some chunk did not fit
+constexpr int kStPair = 2;
 
 struct TopkArgs {
   const float* scores;
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kGmaxThreads) topk_gmax_kernel(TopkArgs a) {
   pdl_wait();
   const Row w = row_of(a, blockIdx.y);
   int* st = a.state + size_t(w.r) * kRowState;
-  if (blockIdx.x == 0 && threadIdx.x < 3) st[kStCursor + threadIdx.x] = 0;
+  if (blockIdx.x == 0 && threadIdx.x < 2) st[kStPair + threadIdx.x] = 0;
   if (w.L <= a.K || bound_of(w.L, a.K).kind != kMaxima) return;
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * (kGmaxThreads / 32);
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
   __shared__ int hw[4096];  // histograms of the selections
   __shared__ int smw[64];
   __shared__ uint32_t s_list[32];
-  __shared__ int s_base, s_last, s_run;
+  __shared__ int s_base, s_last, s_run, s_total;
   __shared__ int s_wt[kTkWarps];  // per warp: candidates, then their offset
   __shared__ __align__(8) uint64_t s_bar;
   extern __shared__ __align__(16) float stage[];
@@ -443,8 +445,9 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     if (lane == 0) {
       int base = 0;
       if (run > 0) {
-        base = atomicAdd(st + kStCursor, run);
-        if (base + run > kCandCap) atomicOr(st + kStOverflow, 1);
+        // (the low half never carries into the high one: at most cap tokens)
+        base = int(uint32_t(atomicAdd(reinterpret_cast<unsigned long long*>(st + kStPair),
+                                      static_cast<unsigned long long>(run))));
       }
       s_base = base;
       s_run = run;
@@ -482,7 +485,9 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    s_last = atomicAdd(st + kStArrived, 1) == C - 1;
+    const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(st + kStPair), 1ull << 32);
+    s_last = int(old >> 32) == C - 1;
+    s_total = int(uint32_t(old));
   }
   __syncthreads();
   if (!s_last) {
@@ -519,9 +524,8 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
     return;
   }
   __threadfence();
-  const int total = __ldcg(st + kStCursor);
-  const int ovf = __ldcg(st + kStOverflow);
-  if (ovf != 0 || total < a.K) {
+  const int total = s_total;
+  if (total > kCandCap || total < a.K) {
     select_whole_row(a, w, hw, smw, out, phys);
   } else {
     // candidates in reservation order: each CTA's are contiguous and in index
@@ -623,11 +627,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(TopkArgs a) {
   // the row's 128-token maxima and state start from zero at the next call
   for (int i = tid; i < (w.L + 127) >> 7; i += kTkThreads) gm128[i] = 0u;
   __syncthreads();
-  if (tid == 0) {
-    st[kStCursor] = 0;
-    st[kStOverflow] = 0;
-    st[kStArrived] = 0;
-  }
+  if (tid == 0) *reinterpret_cast<unsigned long long*>(st + kStPair) = 0ull;
 }
 
 }  // namespace
