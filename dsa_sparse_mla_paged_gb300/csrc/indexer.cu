@@ -277,9 +277,8 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
 // current unit's head weights in its own shared-memory copy (wme[t][h]), read
 // four at a time by every lane, and reduces in packed pairs -- the same
 // operations, in the same order, as the scalar loop of epi_block, so the same
-// bits. With a key scale >= 0, max(scale * d, 0) = scale * max(d, 0): the scale
-// multiplies the head sum once instead of every head (a negative or NaN scale
-// takes the per-head form).
+// bits. (Factoring a non-negative key scale out of the head sum, as the one-row
+// epilogue does, measured slower here: one code path is smaller.)
 __device__ __forceinline__ void epi_block_wide(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
                                                int lane, TileWalk& w, EpiState& e, int& cur_b, UnitInfo& ui,
                                                float* wme) {
@@ -298,29 +297,17 @@ __device__ __forceinline__ void epi_block_wide(const IdxTc& a, const float (&v)[
     if (e.g == g) scale = sc[g];
   const float4* wrow = reinterpret_cast<const float4*>(wme + e.t * kIdxHeads);
   unsigned long long p01 = f2_pack(0.f, 0.f), p23 = p01;  // partial sums of heads 4i + {0, 1} and 4i + {2, 3}
-  float sum;
-  if (scale >= 0.f) {
+  const unsigned long long s2 = f2_pack(scale, scale);
 #pragma unroll
-    for (int i = 0; i < kIdxHeads / 4; ++i) {
-      const float4 w4 = wrow[i];
-      p01 = f2_fma(f2_pack(w4.x, w4.y), f2_pack(fmaxf(v[4 * i], 0.f), fmaxf(v[4 * i + 1], 0.f)), p01);
-      p23 = f2_fma(f2_pack(w4.z, w4.w), f2_pack(fmaxf(v[4 * i + 2], 0.f), fmaxf(v[4 * i + 3], 0.f)), p23);
-    }
-    const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
-    sum = scale * ((a01.x + a01.y) + (a23.x + a23.y));
-  } else {
-    const unsigned long long s2 = f2_pack(scale, scale);
-#pragma unroll
-    for (int i = 0; i < kIdxHeads / 4; ++i) {
-      const float4 w4 = wrow[i];
-      float2 x = f2_unpack(f2_mul(s2, f2_pack(v[4 * i], v[4 * i + 1])));
-      float2 y = f2_unpack(f2_mul(s2, f2_pack(v[4 * i + 2], v[4 * i + 3])));
-      p01 = f2_fma(f2_pack(w4.x, w4.y), f2_pack(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), p01);
-      p23 = f2_fma(f2_pack(w4.z, w4.w), f2_pack(fmaxf(y.x, 0.f), fmaxf(y.y, 0.f)), p23);
-    }
-    const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
-    sum = (a01.x + a01.y) + (a23.x + a23.y);
+  for (int i = 0; i < kIdxHeads / 4; ++i) {
+    const float4 w4 = wrow[i];
+    float2 x = f2_unpack(f2_mul(s2, f2_pack(v[4 * i], v[4 * i + 1])));
+    float2 y = f2_unpack(f2_mul(s2, f2_pack(v[4 * i + 2], v[4 * i + 3])));
+    p01 = f2_fma(f2_pack(w4.x, w4.y), f2_pack(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), p01);
+    p23 = f2_fma(f2_pack(w4.z, w4.w), f2_pack(fmaxf(y.x, 0.f), fmaxf(y.y, 0.f)), p23);
   }
+  const float2 a01 = f2_unpack(p01), a23 = f2_unpack(p23);
+  const float sum = (a01.x + a01.y) + (a23.x + a23.y);
   epi_store(a, sum, rowt, lane, w, e, ui);
 }
 
