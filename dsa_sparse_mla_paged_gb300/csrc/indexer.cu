@@ -275,10 +275,10 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
 
 // Several query rows with several epilogue warpgroups: the warp keeps the
 // current unit's head weights in its own shared-memory copy (wme[t][h]), read
-// four at a time by every lane, and reduces in packed pairs -- the same
-// operations, in the same order, as the scalar loop of epi_block, so the same
-// bits. (Factoring a non-negative key scale out of the head sum, as the one-row
-// epilogue does, measured slower here: one code path is smaller.)
+// four at a time by every lane, and reduces w'_h * max(scale * d_h, 0) in
+// packed pairs (heads 4i + {0, 1} and 4i + {2, 3}, each half rounding as its
+// scalar op would). (Factoring a non-negative key scale out of the head sum, as
+// the one-row epilogue does, measured slower here: one code path is smaller.)
 __device__ __forceinline__ void epi_block_wide(const IdxTc& a, const float (&v)[32], const float (&sc)[4], int rowt,
                                                int lane, TileWalk& w, EpiState& e, int& cur_b, UnitInfo& ui,
                                                float* wme) {
