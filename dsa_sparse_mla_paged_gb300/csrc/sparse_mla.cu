@@ -42,11 +42,14 @@ namespace {
 //   warps 4..7  converters: resolve each unit's selected slots to latent rows
 //               (four buffers, by unit), gather the rows (paged, 16-B loads one
 //               tile ahead) and expand this CTA's dims E4M3 -> bf16 exactly
-//               into a 128-B swizzled K-major tile (2 buffers)
-// The epilogue stages O / l per warp as 32 x 32 swizzled tiles and writes the
-// split partials with TMA stores (the tile buffers belong to the next unit);
-// a cluster's last unit stages whole rows in the freed tile buffers instead and
-// writes them with one 1-KB bulk store per head.
+//               into a 128-B swizzled K-major tile (2 buffers); the per-tensor
+//               latent scale is not applied there but to the scores' scale and
+//               the output's 1 / l
+// The epilogue stages O / l per warp as 32 x 32 swizzled tiles, alternating the
+// warp's own staging tile and its quarter of P, and writes the split partials
+// with TMA stores (the tile buffers belong to the next unit); a cluster's last
+// unit stages whole rows in the freed tile buffers instead and writes them with
+// one 1-KB bulk store per head.
 // ---------------------------------------------------------------------------
 constexpr int kNT = 64;                     // tokens per tile
 constexpr int kQBlk = kHeads * 128;         // 12,288 B per Q K-block (96 rows of 64 bf16)
